@@ -1,0 +1,149 @@
+/*
+ * w4a16.h - C ABI of the GB300 (sm_103a) int4 weight-only affine linear layer.
+ *
+ * The operation: a linear layer Y = X * W^T whose weight W[N][K] is stored as
+ * 4-bit codes q in 0..15 with one binary16 scale and one binary16 bias per
+ * group of 64 consecutive k, so that w[n][k] = scale[n][k/64]*q[n][k] +
+ * bias[n][k/64].  Sources (page title, section):
+ *   "The inference engine - Mojo 1.0 on Metal", "Crossing Mojo 1.0": decode
+ *     is a weight-streaming multi-row GEMV plus on-device token selection;
+ *     prefill dequantises each weight once into a transposed half-precision
+ *     scratch and runs a half-precision GEMM.
+ *   same page, "What's inside the engine today": int4 projections and LM
+ *     head; greedy and top-k selection on the device.
+ *   "engine-mlx", "Tech details": MLX 4-bit quantised format.
+ *   "Engineering investigation ... 10x faster?", "Selective quantization":
+ *     affine quantisation with group size 64.
+ *
+ * Storage format (shared by every call):
+ *   qweight  uint32 [N][K/8], row-major.  Word j of row n holds q[n][8j+i]
+ *            in bits 4i..4i+3 (lowest nibble = lowest k).
+ *   scales   binary16 [N][K/64], row-major.
+ *   biases   binary16 [N][K/64], row-major.
+ *   Activations and outputs are binary16 (IEEE half, passed as uint16_t bit
+ *   patterns), row-major.
+ *
+ * Conventions:
+ *   - Every pointer is a DEVICE pointer on the current CUDA device, owned by
+ *     the caller.  The library allocates no device memory and keeps no
+ *     per-call state.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     only enqueues work and returns before it completes.
+ *   - The return value is a status code (W4A16_OK = 0).  All argument checks
+ *     happen on the host before anything is enqueued; a failing check
+ *     enqueues nothing.  W4_ERR_LAUNCH reports a launch error from the CUDA
+ *     runtime.  No kernel traps.
+ *   - Pointers must be 16-byte aligned.
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define W4A16_API __attribute__((visibility("default")))
+#else
+#define W4A16_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define W4A16_OK          0
+#define W4_ERR_NULL       1  /* a required pointer is NULL */
+#define W4_ERR_SHAPE      2  /* a dimension is out of the supported range */
+#define W4_ERR_ALIGN      3  /* a pointer or row stride is not 16-byte aligned */
+#define W4_ERR_GROUP      4  /* group size other than 64 */
+#define W4_ERR_LAUNCH     5  /* the CUDA runtime rejected a launch */
+#define W4_ERR_WORKSPACE  6  /* workspace missing or smaller than required */
+#define W4_ERR_DEVICE     7  /* current device is not sm_103 or lacks a needed driver entry point */
+#define W4_ERR_TIMEOUT    8  /* a device-side bounded wait expired (reported by w4a16_device_status) */
+
+/*
+ * w4_gemv - decode GEMV, y[m][n] = sum_k w[n][k] * x[m][k].
+ *   ("The inference engine - Mojo 1.0 on Metal", "Crossing Mojo 1.0": the
+ *   multi-row weight-streaming GEMV.)
+ *   x       binary16 [M][K]          activations
+ *   qweight, scales, biases          int4 weight in the format above
+ *   y       binary16 [M][N]          output; fp32 accumulation, rounded to
+ *                                     nearest even once at the end
+ *   M       1..16 activation rows, all sharing one pass over the weights
+ *   N       >= 1 output features;  K  multiple of 64, >= 64;  group == 64
+ * Errors: W4_ERR_NULL, W4_ERR_SHAPE, W4_ERR_GROUP, W4_ERR_ALIGN, W4_ERR_LAUNCH.
+ */
+W4A16_API int w4_gemv(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+            const uint16_t *biases, uint16_t *y, int M, int N, int K, int group,
+            void *stream);
+
+/*
+ * lm_head_argmax_topk - LM-head GEMV fused with token selection.
+ *   ("The inference engine - Mojo 1.0 on Metal", "Crossing Mojo 1.0" and
+ *   "What's inside the engine today": greedy / top-k selection on the GPU so
+ *   that no logits vector crosses to the host.)
+ *   Computes the fp32 logits l[m][n] = sum_k w[n][k] * x[m][k] for every
+ *   n < N and returns, for each activation row m, the k largest:
+ *   idx int32 [M][k] and val float32 [M][k], ordered by value descending,
+ *   ties broken by the lowest index (k == 1 is greedy argmax).  No logits
+ *   tensor is written: a first pass leaves per-block candidates in
+ *   `workspace`, a second pass merges them.
+ *   M 1..16;  N >= k;  K multiple of 64;  group == 64;  1 <= k <= 64;
+ *   N * k must not exceed 16,777,216.
+ *   workspace  device buffer of at least lm_head_workspace_bytes(M, N, k)
+ *              bytes, 16-byte aligned; contents on entry are ignored.
+ * Errors: as w4_gemv, plus W4_ERR_WORKSPACE.
+ */
+W4A16_API int lm_head_argmax_topk(const uint16_t *x, const uint32_t *qweight,
+                        const uint16_t *scales, const uint16_t *biases,
+                        int M, int N, int K, int group, int k,
+                        int32_t *idx, float *val,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace lm_head_argmax_topk needs for these sizes (0 if the
+ * sizes are invalid).  Depends only on its arguments. */
+W4A16_API size_t lm_head_workspace_bytes(int M, int N, int k);
+
+/*
+ * w4_dequant_f16 - dequantise once into the transposed half scratch.
+ *   ("The inference engine - Mojo 1.0 on Metal", "Crossing Mojo 1.0": each
+ *   weight is dequantised once per prefill into a transposed half-precision
+ *   scratch.)
+ *   w16  binary16 [K][N] (= W transposed), w16[k][n] = the correctly rounded
+ *        (nearest, ties to even) binary16 of the exact scale*q + bias.
+ *   N >= 1;  K multiple of 64;  group == 64.
+ * Errors: W4_ERR_NULL, W4_ERR_SHAPE, W4_ERR_GROUP, W4_ERR_ALIGN, W4_ERR_LAUNCH.
+ */
+W4A16_API int w4_dequant_f16(const uint32_t *qweight, const uint16_t *scales,
+                   const uint16_t *biases, uint16_t *w16, int N, int K, int group,
+                   void *stream);
+
+/*
+ * f16_gemm - dense half GEMM for prefill, y = x16 * w16.
+ *   ("The inference engine - Mojo 1.0 on Metal", "Crossing Mojo 1.0": the
+ *   half-precision GEMM that follows the dequantise-once step.)
+ *   x16  binary16 [M][K] row-major;  w16  binary16 [K][N] row-major;
+ *   y    binary16 [M][N] row-major; fp32 accumulation on the tensor cores,
+ *        rounded to nearest even once at the end.
+ *   M >= 1;  N >= 8 and a multiple of 8;  K >= 8 and a multiple of 8
+ *   (row strides must be 16-byte multiples for the tensor-memory copies).
+ * Errors: W4_ERR_NULL, W4_ERR_SHAPE, W4_ERR_ALIGN, W4_ERR_DEVICE, W4_ERR_LAUNCH.
+ */
+W4A16_API int f16_gemm(const uint16_t *x16, const uint16_t *w16, uint16_t *y,
+             int M, int N, int K, void *stream);
+
+/* Human-readable name of a status code (static string). */
+W4A16_API const char *w4a16_status_string(int status);
+
+/*
+ * Synchronises the current device and reports whether any kernel of this
+ * library gave up a bounded device-side wait since the last call
+ * (W4_ERR_TIMEOUT), then clears the record.  W4A16_OK otherwise.
+ */
+W4A16_API int w4a16_device_status(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

@@ -1,0 +1,166 @@
+"""GB300-native (sm_103a) int4 weight-only affine linear layer (W4A16).
+
+Thin Python binding of ``libw4a16.so``: every function here validates and
+marshals torch tensors into the C ABI declared in ``include/w4a16.h`` and
+enqueues the library's CUDA kernels on the current torch stream.  There is no
+CPU or PyTorch fallback: if the library is missing, importing this package
+fails.
+
+Weight format: ``qweight`` int32/uint32 [N][K/8] (8 four-bit codes per word,
+lowest nibble = lowest k), ``scales`` and ``biases`` float16 [N][K/64];
+w[n][k] = scale * q + bias.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = ["w4_gemv", "lm_head_argmax_topk", "lm_head_workspace_bytes", "w4_dequant_f16",
+           "f16_gemm", "device_status", "W4A16Error", "LIB_PATH", "lib"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libw4a16.so")
+
+STATUS = {0: "W4A16_OK", 1: "W4_ERR_NULL", 2: "W4_ERR_SHAPE", 3: "W4_ERR_ALIGN", 4: "W4_ERR_GROUP",
+          5: "W4_ERR_LAUNCH", 6: "W4_ERR_WORKSPACE", 7: "W4_ERR_DEVICE", 8: "W4_ERR_TIMEOUT"}
+
+
+class W4A16Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)} "
+                         f"({lib.w4a16_status_string(status).decode()})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run __graft_entry__.build() "
+                          "(nvcc, sm_103a) before importing this package")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.w4_gemv.argtypes = [P, P, P, P, P, I, I, I, I, P]
+    L.lm_head_argmax_topk.argtypes = [P, P, P, P, I, I, I, I, I, P, P, P, Z, P]
+    L.lm_head_workspace_bytes.argtypes = [I, I, I]
+    L.lm_head_workspace_bytes.restype = Z
+    L.w4_dequant_f16.argtypes = [P, P, P, P, I, I, I, P]
+    L.f16_gemm.argtypes = [P, P, P, I, I, I, P]
+    L.w4a16_status_string.argtypes = [I]
+    L.w4a16_status_string.restype = ctypes.c_char_p
+    L.w4a16_device_status.argtypes = []
+    for f in ("w4_gemv", "lm_head_argmax_topk", "w4_dequant_f16", "f16_gemm", "w4a16_device_status"):
+        getattr(L, f).restype = I
+    return L
+
+
+lib = _load()
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise W4A16Error(fn, status)
+
+
+def _dev(t: torch.Tensor, name: str, dtypes) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+_QW = (torch.int32, getattr(torch, "uint32", torch.int32))
+_H = (torch.float16,)
+
+
+def _weight_dims(qweight, scales, biases, group):
+    N, KW = qweight.shape
+    K = KW * 8
+    if scales.shape != (N, K // group) or biases.shape != (N, K // group):
+        raise ValueError(f"scales/biases must be [{N}][{K // group}]")
+    return N, K
+
+
+def w4_gemv(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
+            y: torch.Tensor | None = None, group: int = 64, stream=None) -> torch.Tensor:
+    """y[M][N] = x[M][K] @ W^T for the int4 weight (M <= 16)."""
+    N, K = _weight_dims(qweight, scales, biases, group)
+    x2 = x.reshape(-1, K) if x.dim() != 2 else x
+    M = x2.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    _check("w4_gemv", lib.w4_gemv(_dev(x2, "x", _H), _dev(qweight, "qweight", _QW),
+                                  _dev(scales, "scales", _H), _dev(biases, "biases", _H),
+                                  _dev(y, "y", _H), M, N, K, group, _stream(stream)))
+    return y
+
+
+def lm_head_workspace_bytes(M: int, N: int, k: int) -> int:
+    return int(lib.lm_head_workspace_bytes(M, N, k))
+
+
+def lm_head_argmax_topk(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor,
+                        biases: torch.Tensor, k: int = 1, idx: torch.Tensor | None = None,
+                        val: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                        group: int = 64, stream=None):
+    """(idx int32 [M][k], val float32 [M][k]): the k largest logits of x @ W^T per row."""
+    N, K = _weight_dims(qweight, scales, biases, group)
+    x2 = x.reshape(-1, K) if x.dim() != 2 else x
+    M = x2.shape[0]
+    if idx is None:
+        idx = torch.empty((M, k), dtype=torch.int32, device=x.device)
+    if val is None:
+        val = torch.empty((M, k), dtype=torch.float32, device=x.device)
+    need = lm_head_workspace_bytes(M, N, k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _check("lm_head_argmax_topk",
+           lib.lm_head_argmax_topk(_dev(x2, "x", _H), _dev(qweight, "qweight", _QW),
+                                   _dev(scales, "scales", _H), _dev(biases, "biases", _H),
+                                   M, N, K, group, k, _dev(idx, "idx", (torch.int32,)),
+                                   _dev(val, "val", (torch.float32,)),
+                                   _dev(workspace, "workspace", (torch.uint8,)),
+                                   workspace.numel(), _stream(stream)))
+    return idx, val
+
+
+def w4_dequant_f16(qweight: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
+                   w16: torch.Tensor | None = None, group: int = 64, stream=None) -> torch.Tensor:
+    """Transposed half scratch w16[K][N] = RNE(scale * q + bias)."""
+    N, K = _weight_dims(qweight, scales, biases, group)
+    if w16 is None:
+        w16 = torch.empty((K, N), dtype=torch.float16, device=qweight.device)
+    _check("w4_dequant_f16",
+           lib.w4_dequant_f16(_dev(qweight, "qweight", _QW), _dev(scales, "scales", _H),
+                              _dev(biases, "biases", _H), _dev(w16, "w16", _H), N, K, group,
+                              _stream(stream)))
+    return w16
+
+
+def f16_gemm(x16: torch.Tensor, w16: torch.Tensor, y: torch.Tensor | None = None,
+             stream=None) -> torch.Tensor:
+    """y[M][N] = x16[M][K] @ w16[K][N] (fp32 accumulation, half output)."""
+    M, K = x16.shape
+    K2, N = w16.shape
+    if K2 != K:
+        raise ValueError("inner dimensions differ")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x16.device)
+    _check("f16_gemm", lib.f16_gemm(_dev(x16, "x16", _H), _dev(w16, "w16", _H), _dev(y, "y", _H),
+                                    M, N, K, _stream(stream)))
+    return y
+
+
+def device_status() -> int:
+    """Synchronise and return the library's device-side status (0 = ok, 8 = a bounded wait expired)."""
+    return int(lib.w4a16_device_status())

@@ -1,0 +1,396 @@
+// f16_gemm: dense half GEMM of the prefill path, Y[M][N] = X[M][K] * W16[K][N].
+//
+// "The inference engine - Mojo 1.0 on Metal", "Crossing Mojo 1.0": after the
+// dequantise-once step prefill runs a half-precision GEMM on the transposed
+// scratch; the same page credits hoisting tile-edge guards out of the GEMM
+// hot loop.  Here the hot loop has no edge guards at all: tensor-memory
+// copies zero-fill out-of-range rows/columns and only the epilogue masks.
+//
+// sm_103a design:
+//  * Persistent grid (one CTA per SM), static tile schedule over 128 x 256
+//    output tiles, m-fastest so CTAs in flight share W16 columns in L2.
+//  * Warp 0: one thread issues TMA copies (128B-swizzled boxes) of the A
+//    tile (X, K-major, 128 x 64) and B tile (W16, N-major, 64 x 256 as four
+//    64 x 64 boxes) into a 4-stage shared-memory ring (mbarrier tx counts).
+//  * Warp 1: allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
+//    and one thread issues tcgen05.mma.kind::f16 (M=128, N=256, K=16; four
+//    per 64-k stage), releasing each stage with tcgen05.commit.
+//  * Warps 2-5: epilogue.  Each reads its 32 TMEM lanes (tcgen05.ld), rounds
+//    to binary16 and stores; the accumulator is released as soon as it has
+//    been read, so the next tile's MMAs overlap the stores.
+//  * Every mbarrier wait is bounded (2 s); on expiry the kernel records
+//    W4_ERR_TIMEOUT in a device flag, drains its own copies and MMAs, frees
+//    TMEM and returns.
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace w4a16 {
+
+__device__ int g_wait_expired = 0;
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_TILE = BM * BK * 2;     // 16 KB
+constexpr int B_BOX = BK * 64 * 2;      // 8 KB: 64 k rows x 64 n
+constexpr int B_TILE = BK * BN * 2;     // 32 KB
+constexpr int STAGE_BYTES = A_TILE + B_TILE;
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
+constexpr uint32_t kMaxSpins = 1u << 26;
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of parity `parity` to complete.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t spin = 0; spin < kMaxSpins; ++spin) {
+        if (mbar_try(bar, parity)) return true;
+        if ((spin & 63) == 63 && global_ns() - t0 > kWaitNs) break;
+    }
+    atomicExch(&g_wait_expired, 1);
+    return false;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(dst),
+        "l"(map), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor (sm_100 family): start address, leading and
+// stride byte offsets (>> 4), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, A and B binary16, A
+// K-major, B MN-major, N = 256, M = 128.
+constexpr uint32_t kInstrDesc = (1u << 4)                 // D format: f32
+                                | (0u << 7) | (0u << 10)  // A, B: f16
+                                | (0u << 15)              // A K-major
+                                | (1u << 16)              // B MN-major
+                                | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(kInstrDesc), "r"(accum));
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_half2(uint32_t a, uint32_t b) {
+    const __half2 h = __floats2half2_rn(__uint_as_float(a), __uint_as_float(b));
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+                uint16_t *__restrict__ y, int M, int N, int K) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle atoms.
+    const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t bar0 = base + STAGES * STAGE_BYTES;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto accf_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto acce_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+    const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 5));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
+    const int ntiles = tiles_m * tiles_n;
+    const int nk = (K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(accf_bar(a), 1);
+            mbar_init(acce_bar(a), 4);
+        }
+        mbar_init(done_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tma_a) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tma_b) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         (uint32_t)__cvta_generic_to_shared(tmem_slot)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer ----------------
+            uint32_t issued_ph = 0, issued_any = 0;
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * BN;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (!mbar_wait(empty_bar(s), ph ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(full_bar(s), STAGE_BYTES);
+                    const uint32_t sa = base + s * STAGE_BYTES;
+                    const uint32_t sb = sa + A_TILE;
+                    tma_load_2d(sa, &tma_a, kb * BK, m0, full_bar(s));
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * B_BOX, &tma_b, n0 + 64 * j, kb * BK, full_bar(s));
+                    issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+                    issued_any |= 1u << s;
+                }
+            }
+            // Drain: every copy this thread issued has landed before exit.
+            for (int s = 0; s < STAGES; ++s)
+                if (issued_any & (1u << s)) mbar_wait(full_bar(s), (issued_ph >> s) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            int it = 0, tc = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tc) {
+                const int acc = tc & 1;
+                const uint32_t aph = (tc >> 1) & 1;
+                if (!mbar_wait(acce_bar(acc), aph ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t dst = tmem + acc * BN;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1;
+                    if (!mbar_wait(full_bar(s), ph)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + s * STAGE_BYTES;
+                    const uint32_t sb = sa + A_TILE;
+#pragma unroll
+                    for (int ks = 0; ks < BK / 16; ++ks) {
+                        const uint64_t ad = smem_desc(sa + ks * 32, 16, 1024);
+                        const uint64_t bd = smem_desc(sb + ks * 2048, B_BOX, 1024);
+                        mma_f16(dst, ad, bd, (kb | ks) != 0);
+                    }
+                    mma_commit(empty_bar(s));
+                }
+                if (!ok) break;
+                mma_commit(accf_bar(acc));
+            }
+            mma_commit(done_bar);
+            mbar_wait(done_bar, 0);
+        }
+    } else {
+        // ---------------- epilogue: warps 2..5 ----------------
+        const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+        int tc = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tc) {
+            const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * BN;
+            const int acc = tc & 1;
+            const uint32_t aph = (tc >> 1) & 1;
+            if (!mbar_wait(accf_bar(acc), aph)) break;
+            tc_fence_after();
+            const int row = m0 + quad * 32 + lane;
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + acc * BN + c * 32, r);
+                if (c == BN / 32 - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acce_bar(acc));
+                }
+                if (row < M) {
+                    uint16_t *dst = y + (size_t)row * N + n0 + c * 32;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        if (n0 + c * 32 + 8 * v < N) {
+                            uint4 o;
+                            o.x = pack_half2(r[8 * v + 0], r[8 * v + 1]);
+                            o.y = pack_half2(r[8 * v + 2], r[8 * v + 3]);
+                            o.z = pack_half2(r[8 * v + 4], r[8 * v + 5]);
+                            o.w = pack_half2(r[8 * v + 6], r[8 * v + 7]);
+                            *reinterpret_cast<uint4 *>(dst + 8 * v) = o;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side: tensor maps through the driver entry point (no libcuda link).
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+bool make_map(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+              uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace w4a16
+
+using namespace w4a16;
+
+extern "C" int f16_gemm(const uint16_t *x16, const uint16_t *w16, uint16_t *y, int M, int N, int K,
+                        void *stream) {
+    if (!x16 || !w16 || !y) return W4_ERR_NULL;
+    if (M < 1 || N < 8 || K < 8 || N % 8 != 0 || K % 8 != 0) return W4_ERR_SHAPE;
+    if (!aligned16(x16) || !aligned16(w16) || !aligned16(y)) return W4_ERR_ALIGN;
+    if (device_cc() != 103) return W4_ERR_DEVICE;
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, x16, (uint64_t)K, (uint64_t)M, BK, BM)) return W4_ERR_DEVICE;
+    if (!make_map(&tb, w16, (uint64_t)N, (uint64_t)K, 64, BK)) return W4_ERR_DEVICE;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) !=
+            cudaSuccess)
+            return W4_ERR_LAUNCH;
+        attr_set[dev] = true;
+    }
+    const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    int grid = sm_count();
+    if (grid > tiles) grid = tiles;
+    gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(ta, tb, y, M, N, K);
+    return launch_status();
+}
+
+extern "C" int w4a16_device_status(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return W4_ERR_LAUNCH;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_wait_expired, sizeof(int)) != cudaSuccess) return W4_ERR_LAUNCH;
+    if (v) {
+        const int zero = 0;
+        cudaMemcpyToSymbol(g_wait_expired, &zero, sizeof(int));
+        return W4_ERR_TIMEOUT;
+    }
+    return W4A16_OK;
+}
+
+extern "C" const char *w4a16_status_string(int status) {
+    switch (status) {
+        case W4A16_OK: return "ok";
+        case W4_ERR_NULL: return "null pointer";
+        case W4_ERR_SHAPE: return "unsupported shape";
+        case W4_ERR_ALIGN: return "pointer or stride not 16-byte aligned";
+        case W4_ERR_GROUP: return "group size must be 64";
+        case W4_ERR_LAUNCH: return "CUDA launch error";
+        case W4_ERR_WORKSPACE: return "workspace missing or too small";
+        case W4_ERR_DEVICE: return "unsupported device (needs sm_103) or missing driver entry point";
+        case W4_ERR_TIMEOUT: return "a device-side bounded wait expired";
+        default: return "unknown status";
+    }
+}

@@ -68,3 +68,8 @@ def make_x(seed: int, M: int, K: int) -> np.ndarray:
 
 def layer_seed(base: int, layer: int, proj: int) -> int:
     return base + 7 * layer + proj
+
+
+def make_half_matrix(seed: int, rows: int, cols: int, std: float = 1.0) -> np.ndarray:
+    """fp16 [rows][cols] ~ N(0, std^2) (dense operands for the half GEMM)."""
+    return (rng(seed).standard_normal((rows, cols)) * std).astype(np.float16)

@@ -1,0 +1,113 @@
+"""The C-ABI library loads, exports every function include/w4a16.h declares,
+and rejects bad arguments on the host (no CUDA call is made on these paths)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "w4a16.h")
+LIB = os.path.join(ROOT, "int4_weight_only_affine_gb300", "libw4a16.so")
+
+
+def _declared():
+    text = open(HEADER).read()
+    return re.findall(r"W4A16_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def _status_codes():
+    text = open(HEADER).read()
+    return {m[0]: int(m[1]) for m in re.findall(r"#define\s+(W4\w+)\s+(\d+)", text)}
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        from int4_weight_only_affine_gb300 import build
+        build.build()
+    return ctypes.CDLL(LIB)
+
+
+def test_header_declares_the_hot_path_calls():
+    names = set(_declared())
+    assert {"w4_gemv", "lm_head_argmax_topk", "lm_head_workspace_bytes", "w4_dequant_f16",
+            "f16_gemm", "w4a16_status_string", "w4a16_device_status"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def _args(lib):
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.w4_gemv.argtypes = [P, P, P, P, P, I, I, I, I, P]
+    lib.lm_head_argmax_topk.argtypes = [P, P, P, P, I, I, I, I, I, P, P, P, Z, P]
+    lib.lm_head_workspace_bytes.argtypes = [I, I, I]
+    lib.lm_head_workspace_bytes.restype = Z
+    lib.w4_dequant_f16.argtypes = [P, P, P, P, I, I, I, P]
+    lib.f16_gemm.argtypes = [P, P, P, I, I, I, P]
+    lib.w4a16_status_string.argtypes = [I]
+    lib.w4a16_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every case below fails a host check first
+
+
+def test_host_validation_codes(lib):
+    L = _args(lib)
+    c = _status_codes()
+    f = FAKE
+    # w4_gemv
+    assert L.w4_gemv(None, f, f, f, f, 1, 8, 64, 64, None) == c["W4_ERR_NULL"]
+    assert L.w4_gemv(f, f, f, f, None, 1, 8, 64, 64, None) == c["W4_ERR_NULL"]
+    assert L.w4_gemv(f, f, f, f, f, 1, 8, 64, 32, None) == c["W4_ERR_GROUP"]
+    assert L.w4_gemv(f, f, f, f, f, 0, 8, 64, 64, None) == c["W4_ERR_SHAPE"]
+    assert L.w4_gemv(f, f, f, f, f, 17, 8, 64, 64, None) == c["W4_ERR_SHAPE"]
+    assert L.w4_gemv(f, f, f, f, f, 1, 0, 64, 64, None) == c["W4_ERR_SHAPE"]
+    assert L.w4_gemv(f, f, f, f, f, 1, 8, 96, 64, None) == c["W4_ERR_SHAPE"]
+    assert L.w4_gemv(f + 8, f, f, f, f, 1, 8, 64, 64, None) == c["W4_ERR_ALIGN"]
+    assert L.w4_gemv(f, f, f, f, f + 2, 1, 8, 64, 64, None) == c["W4_ERR_ALIGN"]
+    # lm_head_argmax_topk
+    need = L.lm_head_workspace_bytes(1, 1000, 5)
+    assert need > 0
+    assert L.lm_head_argmax_topk(f, f, f, f, 1, 1000, 64, 64, 5, f, f, None, need, None) == c["W4_ERR_WORKSPACE"]
+    assert L.lm_head_argmax_topk(f, f, f, f, 1, 1000, 64, 64, 5, f, f, f, need - 1, None) == c["W4_ERR_WORKSPACE"]
+    assert L.lm_head_argmax_topk(f, f, f, f, 1, 1000, 64, 64, 0, f, f, f, need, None) == c["W4_ERR_SHAPE"]
+    assert L.lm_head_argmax_topk(f, f, f, f, 1, 1000, 64, 64, 65, f, f, f, 1 << 30, None) == c["W4_ERR_SHAPE"]
+    assert L.lm_head_argmax_topk(f, f, f, f, 1, 4, 64, 64, 5, f, f, f, 1 << 30, None) == c["W4_ERR_SHAPE"]
+    assert L.lm_head_argmax_topk(f, f, f, f, 1, 1000, 64, 64, 5, None, f, f, need, None) == c["W4_ERR_NULL"]
+    assert L.lm_head_argmax_topk(f, f, f, f, 1, 1000, 64, 48, 5, f, f, f, need, None) == c["W4_ERR_GROUP"]
+    # w4_dequant_f16
+    assert L.w4_dequant_f16(f, f, f, None, 8, 64, 64, None) == c["W4_ERR_NULL"]
+    assert L.w4_dequant_f16(f, f, f, f, 8, 100, 64, None) == c["W4_ERR_SHAPE"]
+    assert L.w4_dequant_f16(f, f, f, f, 8, 64, 128, None) == c["W4_ERR_GROUP"]
+    assert L.w4_dequant_f16(f, f + 4, f, f, 8, 64, 64, None) == c["W4_ERR_ALIGN"]
+    # f16_gemm
+    assert L.f16_gemm(None, f, f, 4, 8, 8, None) == c["W4_ERR_NULL"]
+    assert L.f16_gemm(f, f, f, 4, 12, 8, None) == c["W4_ERR_SHAPE"]
+    assert L.f16_gemm(f, f, f, 0, 8, 8, None) == c["W4_ERR_SHAPE"]
+    assert L.f16_gemm(f, f, f, 4, 8, 4, None) == c["W4_ERR_SHAPE"]
+    assert L.f16_gemm(f, f + 8, f, 4, 8, 8, None) == c["W4_ERR_ALIGN"]
+
+
+def test_workspace_bytes_formula(lib):
+    L = _args(lib)
+    # M * min(ceil(N/16), 16384 // k) * k * 8 bytes of candidate keys
+    assert L.lm_head_workspace_bytes(1, 151936, 1) == 1 * 9496 * 1 * 8
+    assert L.lm_head_workspace_bytes(1, 151936, 50) == 1 * (16384 // 50) * 50 * 8
+    assert L.lm_head_workspace_bytes(16, 1000, 5) == 16 * 63 * 5 * 8
+    assert L.lm_head_workspace_bytes(0, 1000, 5) == 0
+    assert L.lm_head_workspace_bytes(1, 1000, 65) == 0
+    assert L.lm_head_workspace_bytes(1, 4, 5) == 0
+
+
+def test_status_strings(lib):
+    L = _args(lib)
+    for name, code in _status_codes().items():
+        s = L.w4a16_status_string(code)
+        assert s and s != b"unknown status", name
+    assert L.w4a16_status_string(999) == b"unknown status"
