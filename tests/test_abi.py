@@ -25,8 +25,8 @@ def _status_codes():
 @pytest.fixture(scope="module")
 def lib():
     if not os.path.exists(LIB):
-        from int4_weight_only_affine_gb300 import build
-        build.build()
+        import __graft_entry__
+        __graft_entry__.build()
     return ctypes.CDLL(LIB)
 
 
