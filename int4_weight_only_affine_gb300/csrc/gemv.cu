@@ -289,26 +289,30 @@ __global__ void __launch_bounds__(NW * 32)
         }
     __syncthreads();
 
-    const int tid = threadIdx.x;
-    float part = 0.f;
-    if (tid < kTileRows * M) {
-        for (int w = 0; w < NW; ++w) part += red[w * kTileRows * M + tid];
-    }
+    const int nout = kTileRows * M;  // up to 256 outputs, more than the CTA's threads
     if (C == 1) {
-        if (tid < kTileRows * M) {
-            const int row = tid / M, col = tid % M;
+        for (int e = threadIdx.x; e < nout; e += blockDim.x) {
+            float part = 0.f;
+            for (int w = 0; w < NW; ++w) part += red[w * nout + e];
+            const int row = e / M, col = e % M;
             if (row0 + row < N) y[(size_t)col * N + row0 + row] = __half_as_ushort(__float2half_rn(part));
         }
         return;
     }
-    if (tid < kTileRows * M) cpart[tid] = part;
+    for (int e = threadIdx.x; e < nout; e += blockDim.x) {
+        float part = 0.f;
+        for (int w = 0; w < NW; ++w) part += red[w * nout + e];
+        cpart[e] = part;
+    }
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
-    if (cr == 0 && tid < kTileRows * M) {
-        float tot = 0.f;
-        for (int r = 0; r < C; ++r) tot += cluster.map_shared_rank(cpart, r)[tid];
-        const int row = tid / M, col = tid % M;
-        if (row0 + row < N) y[(size_t)col * N + row0 + row] = __half_as_ushort(__float2half_rn(tot));
+    if (cr == 0) {
+        for (int e = threadIdx.x; e < nout; e += blockDim.x) {
+            float tot = 0.f;
+            for (int r = 0; r < C; ++r) tot += cluster.map_shared_rank(cpart, r)[e];
+            const int row = e / M, col = e % M;
+            if (row0 + row < N) y[(size_t)col * N + row0 + row] = __half_as_ushort(__float2half_rn(tot));
+        }
     }
     cluster.sync();
 }
@@ -542,14 +546,28 @@ GemvPlan plan_gemv(int M, int N, int K) {
     return pl;
 }
 
+// Raise a kernel's dynamic shared-memory limit once per device (and only
+// upwards), so that launches captured into CUDA graphs issue no attribute calls.
+template <typename Kern>
+bool ensure_smem(Kern kern, size_t bytes) {
+    static size_t granted[64] = {0};
+    if (bytes <= 48 * 1024) return true;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (granted[dev] >= bytes) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+        return false;
+    granted[dev] = bytes;
+    return true;
+}
+
 template <int NT>
 int launch_gemv(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, const uint16_t *bi,
                 uint16_t *y, int M, int N, int K, cudaStream_t st) {
     const GemvPlan pl = plan_gemv(M, N, K);
     if (pl.smem > (size_t)kMaxSmem) return W4_ERR_SHAPE;
     auto kern = gemv_kernel<NT, kGemvWarps>;
-    if (pl.smem > 48 * 1024)
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+    if (!ensure_smem(kern, pl.smem)) return W4_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((N + kTileRows - 1) / kTileRows, pl.C, 1);
     cfg.blockDim = dim3(kGemvWarps * 32, 1, 1);
@@ -599,12 +617,9 @@ int launch_lmhead(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, con
                   int N, int K, int k, int32_t *idx, float *val, uint64_t *ws, const LmPlan &pl,
                   cudaStream_t st) {
     auto k1 = lmhead_pass1<NT, kLmWarps>;
-    if (pl.smem1 > 48 * 1024)
-        cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem1);
+    if (!ensure_smem(k1, pl.smem1) || !ensure_smem(lmhead_pass2, pl.smem2)) return W4_ERR_LAUNCH;
     k1<<<pl.G, kLmWarps * 32, pl.smem1, st>>>(x, qw, sc, bi, M, N, K, k, pl.rpc, ws);
     if (cudaGetLastError() != cudaSuccess) return W4_ERR_LAUNCH;
-    if (pl.smem2 > 48 * 1024)
-        cudaFuncSetAttribute(lmhead_pass2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem2);
     lmhead_pass2<<<M, 1024, pl.smem2, st>>>(ws, pl.G, k, idx, val);
     return launch_status();
 }

@@ -74,10 +74,12 @@ def test_gemv_deterministic_and_zero_cases(w4):
     y1 = w4.w4_gemv(*args)
     y2 = w4.w4_gemv(*args)
     assert torch.equal(y1, y2)
-    # codes 8 with bias -8*scale make every weight exactly zero
+    # Codes 8 with bias -8*scale make every weight exactly zero: sum_k |w x| = 0,
+    # so the tolerance is the absolute 1e-3 (the folded scale and bias terms
+    # cancel up to fp32 rounding).
     z = w4.w4_gemv(args[0], to_dev(np.full_like(qw, 0x88888888)), args[2],
                    to_dev((-8.0 * s.astype(np.float64)).astype(np.float16)))
-    assert torch.count_nonzero(z).item() == 0
+    assert torch.max(torch.abs(z.float())).item() <= 1e-3
 
 
 def test_gemv_closed_form_q8_zero_bias(w4):
