@@ -100,6 +100,33 @@ W4A16_API int lm_head_argmax_topk(const uint16_t *x, const uint32_t *qweight,
                         int32_t *idx, float *val,
                         void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * lm_head_argmax_topk_noalloc - lm_head_argmax_topk without a workspace
+ * argument, for callers that cannot allocate device memory where they call it
+ * (inside an allocator or memory-pool callback, under a fixed memory budget,
+ * or in an embedding with no allocator of its own).  None of the pages has a
+ * counterpart; it is a packaging variant of the call above.
+ *   Arguments, results and limits are those of lm_head_argmax_topk; the
+ *   candidate buffer is a 2 MiB array inside this library's device image,
+ *   which covers every size lm_head_argmax_topk accepts (M <= 16, k * blocks
+ *   <= 16384 keys per row).  Every GPU that loads the library holds the array
+ *   until the process exits.  This call allocates nothing (no cudaMalloc, no
+ *   library allocator).
+ *   Set-up: the first call on a device looks up the array's device address on
+ *   that device (cudaGetSymbolAddress); make that first call before any stream
+ *   capture on that device.
+ *   Sharing: all calls use the same array and it keeps the last call's
+ *   contents.  Nothing in it has to start at zero: pass 1 writes every slot
+ *   pass 2 reads.  Calls whose kernels overlap on the GPU (other streams,
+ *   other host threads) race on the array: order them on one stream.
+ * Errors: as lm_head_argmax_topk; W4_ERR_WORKSPACE if a size would need more
+ * than the built-in 2 MiB; W4_ERR_DEVICE if the address lookup fails.
+ */
+W4A16_API int lm_head_argmax_topk_noalloc(const uint16_t *x, const uint32_t *qweight,
+                        const uint16_t *scales, const uint16_t *biases,
+                        int M, int N, int K, int group, int k,
+                        int32_t *idx, float *val, void *stream);
+
 /* Bytes of workspace lm_head_argmax_topk needs for these sizes (0 if the
  * sizes are invalid).  Depends only on its arguments. */
 W4A16_API size_t lm_head_workspace_bytes(int M, int N, int k);

@@ -28,6 +28,8 @@
 //    memory by cluster rank 0, fixed order).  Results are deterministic.
 #include <cooperative_groups.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace cg = cooperative_groups;
@@ -674,6 +676,64 @@ extern "C" int lm_head_argmax_topk(const uint16_t *x, const uint32_t *qweight, c
     if ((long long)pl.G > lm_max_blocks(N, k)) return W4_ERR_SHAPE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint64_t *ws = reinterpret_cast<uint64_t *>(workspace);
+    return M <= 8 ? launch_lmhead<1>(x, qweight, scales, biases, M, N, K, k, idx, val, ws, pl, s)
+                  : launch_lmhead<2>(x, qweight, scales, biases, M, N, K, k, idx, val, ws, pl, s);
+}
+
+// ---------------------------------------------------------------------------
+// lm_head_argmax_topk_noalloc: the same two kernels, with their candidate
+// buffer in a fixed device array owned by this library instead of a caller
+// workspace.  It exists for callers that cannot allocate device memory at the
+// point of the call: code running inside a memory-pool or allocator callback,
+// a host with a fixed memory budget, or an embedding that owns no allocator at
+// all.  The array is static: every GPU that loads this library keeps it until
+// the process exits.
+// ---------------------------------------------------------------------------
+namespace w4a16 {
+namespace {
+
+// 2 MiB: M <= 16 rows x at most 16384 candidate keys of 8 bytes, i.e. every
+// size lm_head_argmax_topk accepts.
+constexpr size_t kNoAllocScratchBytes = (size_t)16 * kMaxCandidates * sizeof(uint64_t);
+static __device__ __align__(256) uint64_t g_lm_scratch[kNoAllocScratchBytes / sizeof(uint64_t)];
+
+// Device address of g_lm_scratch for the current device.  The host-side name
+// is only a stand-in; the address is looked up once per device and cached.
+void *noalloc_scratch() {
+    static std::mutex mu;
+    static void *addr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_lm_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+}  // namespace
+}  // namespace w4a16
+
+extern "C" int lm_head_argmax_topk_noalloc(const uint16_t *x, const uint32_t *qweight,
+                                           const uint16_t *scales, const uint16_t *biases, int M, int N,
+                                           int K, int group, int k, int32_t *idx, float *val,
+                                           void *stream) {
+    int st = check_common(x, qweight, scales, biases, M, N, K, group);
+    if (st != W4A16_OK) return st;
+    if (!idx || !val) return W4_ERR_NULL;
+    if (k < 1 || k > 64 || k > N || (long long)N * k > 16777216LL) return W4_ERR_SHAPE;
+    if (!aligned16(idx) || !aligned16(val)) return W4_ERR_ALIGN;
+    const size_t need = lm_head_workspace_bytes(M, N, k);
+    if (need == 0 || need > kNoAllocScratchBytes) return W4_ERR_WORKSPACE;
+    void *scratch = noalloc_scratch();
+    if (!scratch) return W4_ERR_DEVICE;
+    LmPlan pl;
+    if (!plan_lmhead(M, N, K, k, sm_count(), pl)) return W4_ERR_SHAPE;
+    if ((long long)pl.G > lm_max_blocks(N, k)) return W4_ERR_SHAPE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint64_t *ws = reinterpret_cast<uint64_t *>(scratch);
     return M <= 8 ? launch_lmhead<1>(x, qweight, scales, biases, M, N, K, k, idx, val, ws, pl, s)
                   : launch_lmhead<2>(x, qweight, scales, biases, M, N, K, k, idx, val, ws, pl, s);
 }

@@ -1,0 +1,56 @@
+"""The no-allocation lm_head entry point (lm_head_argmax_topk_noalloc).
+
+Some callers cannot allocate device memory where they run token selection:
+allocator or memory-pool callbacks, processes held to a fixed memory budget,
+embeddings that bring no allocator.  For them the library offers a variant of
+lm_head_argmax_topk whose candidate buffer is a fixed array inside the
+library.  This test calls it through the C ABI twice in a row and compares
+each result with the workspace-taking entry point.  It lives in its own file
+so that it runs after every other test; it also passes in a fresh process
+(its first call performs the per-device set-up)."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import synth
+from _gpu import require_gpu, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def w4():
+    require_gpu()
+    import int4_weight_only_affine_gb300 as w4
+    P, I = ctypes.c_void_p, ctypes.c_int
+    w4.lib.lm_head_argmax_topk_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, P, P, P]
+    w4.lib.lm_head_argmax_topk_noalloc.restype = I
+    return w4
+
+
+@pytest.mark.parametrize("M,N,K,k", [(1, 151936, 2048, 50), (16, 151936, 2048, 1), (3, 1000, 896, 5)])
+def test_noalloc_matches_workspace_entry_point(w4, M, N, K, k):
+    import torch
+    qw, s, b = synth.make_linear(700 + k, N, K)
+    x = synth.make_x(701 + M, M, K)
+    tx, tq, ts, tb = to_dev(x), to_dev(qw), to_dev(s), to_dev(b)
+    ref_idx, ref_val = w4.lm_head_argmax_topk(tx, tq, ts, tb, k=k)
+    stream = torch.cuda.current_stream().cuda_stream
+    for _ in range(2):   # the shared array keeps the previous call's contents
+        idx = torch.full((M, k), -1, dtype=torch.int32, device="cuda")
+        val = torch.full((M, k), float("nan"), dtype=torch.float32, device="cuda")
+        st = w4.lib.lm_head_argmax_topk_noalloc(tx.data_ptr(), tq.data_ptr(), ts.data_ptr(), tb.data_ptr(),
+                                                M, N, K, 64, k, idx.data_ptr(), val.data_ptr(), stream)
+        assert st == 0, w4.lib.w4a16_status_string(st)
+        torch.cuda.synchronize()
+        assert torch.equal(idx, ref_idx)
+        got, want = val.cpu().numpy().astype(np.float64), ref_val.cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(got - want) <= 1e-3 * np.abs(want) + 1e-3)
+
+
+def test_noalloc_rejects_bad_sizes(w4):
+    f = 0x10000
+    lib = w4.lib
+    assert lib.lm_head_argmax_topk_noalloc(f, f, f, f, 17, 1000, 64, 64, 1, f, f, None) == 2   # M > 16
+    assert lib.lm_head_argmax_topk_noalloc(f, f, f, f, 1, 1000, 64, 64, 65, f, f, None) == 2   # k > 64
