@@ -1,10 +1,13 @@
 """Benchmark of the W4A16 hot path on Qwen2.5-3B shapes (synthetic, seeded).
 
-One step is one pass of the whole hot path:
-  prefill  - w4_dequant_f16 of all 252 projection weights into the transposed
-             half scratch, then f16_gemm at M = 1570 for each projection;
-  decode   - one token at M = 1: 252 w4_gemv in layer order, then the lm_head
-             GEMV fused with top-50 selection;
+One step is one pass of the whole hot path (per layer the weights are held
+as four row blocks: q|k|v, o, gate|up, down, i.e. the 7 projections with the
+blocks that share an input stored contiguously):
+  prefill  - w4_dequant_f16 of all 144 weight blocks into the transposed half
+             scratch, then f16_gemm at M = 1570 for each block;
+  decode   - one token at M = 1: 144 w4_gemv in layer order (each allowed to
+             stream its weights while the previous kernel finishes), then the
+             lm_head GEMV fused with top-50 selection;
   batched  - the same projection set at M = 16 activation rows, then per-row
              greedy argmax over the lm_head.
 Each part is a CUDA graph replayed on one stream; CUDA events time each part.
@@ -133,19 +136,31 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- our arm
 
+# The projections of one layer as the engine stores them: q, k, v as one row
+# block (they read the same activations), gate and up as one row block.  The
+# bytes and the arithmetic are those of the separate projections.
+FUSED = [("qkv", 2048, 2048 + 256 + 256, ("q", "k", "v")), ("o", 2048, 2048, ("o",)),
+         ("gate_up", 2048, 2 * 11008, ("gate", "up")), ("down", 11008, 2048, ("down",))]
+SRC = {"qkv": "attn", "o": "o", "gate_up": "mlp", "down": "down"}
+PROJ_SRC = {"q": "attn", "k": "attn", "v": "attn", "o": "o", "gate": "mlp", "up": "mlp", "down": "down"}
+
+
 class Model:
     """Device-resident synthetic Qwen2.5-3B projection set + lm_head."""
 
     def __init__(self, torch, w4, dev):
         self.torch, self.w4, self.dev = torch, w4, dev
         t0 = time.time()
+        seeds = {name: p for p, (name, _, _) in enumerate(PROJ)}
+        rows = {name: n for name, _, n in PROJ}
         self.layers = []
         for l in range(LAYERS):
-            projs = {}
-            for p, (name, K, N) in enumerate(PROJ):
-                qw, s, b = synth.make_linear(synth.layer_seed(1000, l, p), N, K)
-                projs[name] = (self._up(qw.view(np.int32)), self._up(s), self._up(b), N, K)
-            self.layers.append(projs)
+            blocks = {}
+            for name, K, N, parts in FUSED:
+                mats = [synth.make_linear(synth.layer_seed(1000, l, seeds[q]), rows[q], K) for q in parts]
+                qw, s, b = (np.concatenate([m[i] for m in mats]) for i in range(3))
+                blocks[name] = (self._up(qw.view(np.int32)), self._up(s), self._up(b), N, K)
+            self.layers.append(blocks)
         qw, s, b = synth.make_linear(99, LM_N, LM_K)
         self.lm = (self._up(qw.view(np.int32)), self._up(s), self._up(b), LM_N, LM_K)
         self.setup_s = time.time() - t0
@@ -155,15 +170,12 @@ class Model:
 
 
 def x_inputs(torch, dev, M, seed):
-    """Activations per projection kind: attn (q,k,v share), o, mlp (gate, up share), down."""
+    """Activations per block: attn (q,k,v), o, mlp (gate, up), down, lm_head."""
     return {"attn": torch.from_numpy(synth.make_x(seed, M, 2048)).to(dev),
             "o": torch.from_numpy(synth.make_x(seed + 100, M, 2048)).to(dev),
             "mlp": torch.from_numpy(synth.make_x(seed + 200, M, 2048)).to(dev),
             "down": torch.from_numpy(synth.make_x(seed + 300, M, 11008)).to(dev),
             "lm": torch.from_numpy(synth.make_x(seed + 400, M, LM_K)).to(dev)}
-
-
-SRC = {"q": "attn", "k": "attn", "v": "attn", "o": "o", "gate": "mlp", "up": "mlp", "down": "down"}
 
 
 def run_ours(args, rank, world):
@@ -178,40 +190,42 @@ def run_ours(args, rank, world):
 
     xs1 = x_inputs(torch, dev, 1, 10)
     xs16 = x_inputs(torch, dev, BATCH_M, 20)
-    ys1 = {n: torch.empty((1, N), dtype=torch.float16, device=dev) for n, K, N in PROJ}
-    ys16 = {n: torch.empty((BATCH_M, N), dtype=torch.float16, device=dev) for n, K, N in PROJ}
+    ys1 = {n: torch.empty((1, N), dtype=torch.float16, device=dev) for n, K, N, _ in FUSED}
+    ys16 = {n: torch.empty((BATCH_M, N), dtype=torch.float16, device=dev) for n, K, N, _ in FUSED}
     idx1 = torch.empty((1, TOPK), dtype=torch.int32, device=dev)
     val1 = torch.empty((1, TOPK), dtype=torch.float32, device=dev)
     idx16 = torch.empty((BATCH_M, 1), dtype=torch.int32, device=dev)
     val16 = torch.empty((BATCH_M, 1), dtype=torch.float32, device=dev)
     ws1 = torch.empty(w4.lm_head_workspace_bytes(1, LM_N, TOPK), dtype=torch.uint8, device=dev)
     ws16 = torch.empty(w4.lm_head_workspace_bytes(BATCH_M, LM_N, 1), dtype=torch.uint8, device=dev)
-    # prefill buffers: one transposed scratch per weight; activations/outputs per kind
-    scratch = [{n: torch.empty((K, N), dtype=torch.float16, device=dev) for n, K, N in PROJ}
+    # prefill buffers: one transposed scratch per weight block; activations/outputs per kind
+    scratch = [{n: torch.empty((K, N), dtype=torch.float16, device=dev) for n, K, N, _ in FUSED}
                for _ in range(LAYERS)]
     xp = {"attn": torch.randn((PREFILL_M, 2048), device=dev).half(),
           "o": torch.randn((PREFILL_M, 2048), device=dev).half(),
           "mlp": torch.randn((PREFILL_M, 2048), device=dev).half(),
           "down": torch.randn((PREFILL_M, 11008), device=dev).half()}
-    yp = {n: torch.empty((PREFILL_M, N), dtype=torch.float16, device=dev) for n, K, N in PROJ}
+    yp = {n: torch.empty((PREFILL_M, N), dtype=torch.float16, device=dev) for n, K, N, _ in FUSED}
+    ov = w4.OVERLAP_PREVIOUS  # weights are constant: stream them while the previous kernel finishes
 
     def decode(xs, ys, M, k, idx, val, ws):
         for l in range(LAYERS):
-            for name, _, _ in PROJ:
+            for name, _, _, _ in FUSED:
                 qw, s, b, N, K = model.layers[l][name]
-                w4.w4_gemv(xs[SRC[name]], qw, s, b, y=ys[name], stream=stream)
+                w4.w4_gemv(xs[SRC[name]], qw, s, b, y=ys[name], stream=stream, flags=ov)
         qw, s, b, N, K = model.lm
-        w4.lm_head_argmax_topk(xs["lm"], qw, s, b, k=k, idx=idx, val=val, workspace=ws, stream=stream)
+        w4.lm_head_argmax_topk(xs["lm"], qw, s, b, k=k, idx=idx, val=val, workspace=ws, stream=stream,
+                               flags=ov)
 
     def dequant_all():
         for l in range(LAYERS):
-            for name, _, _ in PROJ:
+            for name, _, _, _ in FUSED:
                 qw, s, b, N, K = model.layers[l][name]
                 w4.w4_dequant_f16(qw, s, b, w16=scratch[l][name], stream=stream)
 
     def gemm_all():
         for l in range(LAYERS):
-            for name, _, _ in PROJ:
+            for name, _, _, _ in FUSED:
                 w4.f16_gemm(xp[SRC[name]], scratch[l][name], y=yp[name], stream=stream)
 
     parts = {
@@ -220,8 +234,8 @@ def run_ours(args, rank, world):
         "decode_m1": lambda: decode(xs1, ys1, 1, TOPK, idx1, val1, ws1),
         "decode_m16": lambda: decode(xs16, ys16, BATCH_M, 1, idx16, val16, ws16),
     }
-    launches = {"dequant": LAYERS * 7, "gemm": LAYERS * 7, "decode_m1": LAYERS * 7 + 2,
-                "decode_m16": LAYERS * 7 + 2}
+    nb = LAYERS * len(FUSED)
+    launches = {"dequant": nb, "gemm": nb, "decode_m1": nb + 2, "decode_m16": nb + 2}
     # eager warm-up (sets kernel attributes), then capture one graph per part
     with torch.cuda.stream(stream):
         for f in parts.values():
@@ -337,7 +351,7 @@ def oracle_decode_sample(budget_s, threads):
         for p, (name, K, N) in enumerate(PROJ):
             qw, s, b = synth.make_linear(synth.layer_seed(1000, l, p), N, K)
             t0 = time.perf_counter()
-            oracle.gemv(x[SRC[name]], qw, s, b, N, K, threads=threads)
+            oracle.gemv(x[PROJ_SRC[name]], qw, s, b, N, K, threads=threads)
             t_used += time.perf_counter() - t0
             done_bytes += weight_bytes(N, K)
             n_mats += 1
@@ -361,7 +375,7 @@ def profile_case(which, iters=3):
     import int4_weight_only_affine_gb300 as w4
     dev = torch.device("cuda:0")
     if which in ("gemv", "dequant"):
-        K, N = 2048, 11008
+        K, N = 2048, 22016   # gate and up projections stored as one matrix
         qw, s, b = synth.make_linear(1, N, K)
         a = [torch.from_numpy(t).to(dev) for t in (qw.view(np.int32), s, b)]
         x = torch.from_numpy(synth.make_x(2, 1, K)).to(dev)
@@ -460,7 +474,8 @@ def main():
         "dtype": "f16",
         "data": "synthetic",
         "config": {"workload": "qwen2.5-3b: prefill M=1570 (dequant-once + f16 GEMM), decode M=1 "
-                               "(252 GEMV + lm_head top-50), batched decode M=16 (+ per-row argmax)",
+                               "(36 layers x [qkv, o, gate_up, down] GEMVs + lm_head top-50), batched decode "
+                               "M=16 (+ per-row argmax); q/k/v and gate/up stored as fused row blocks",
                    "model": "Qwen2.5-3B-shaped projections x36 + lm_head 2048->151936",
                    "global_batch": 1, "seq_len": PREFILL_M, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (1.74 GB of weights per decode pass, 5.5 GB scratch)"},

@@ -62,6 +62,17 @@ extern "C" {
 #define W4_ERR_TIMEOUT    8  /* a device-side bounded wait expired (reported by w4a16_device_status) */
 
 /*
+ * Launch flag of the *_ex calls.  W4A16_OVERLAP_PREVIOUS lets the call's
+ * kernel start while the previous kernel on the same stream is still running
+ * (programmatic dependent launch): it streams its weights (qweight, scales,
+ * biases) at once and waits for the previous kernel only before it reads its
+ * activations and writes its outputs.  Use it when the weights are not
+ * written by the preceding kernel on the stream (the usual case: weights are
+ * loaded once).  Without the flag the call follows ordinary stream order.
+ */
+#define W4A16_OVERLAP_PREVIOUS 1u
+
+/*
  * w4_gemv - decode GEMV, y[m][n] = sum_k w[n][k] * x[m][k].
  *   ("The inference engine - Mojo 1.0 on Metal", "Crossing Mojo 1.0": the
  *   multi-row weight-streaming GEMV.)
@@ -76,6 +87,11 @@ extern "C" {
 W4A16_API int w4_gemv(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
             const uint16_t *biases, uint16_t *y, int M, int N, int K, int group,
             void *stream);
+
+/* w4_gemv with launch flags (W4A16_OVERLAP_PREVIOUS or 0); otherwise identical. */
+W4A16_API int w4_gemv_ex(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+            const uint16_t *biases, uint16_t *y, int M, int N, int K, int group,
+            unsigned flags, void *stream);
 
 /*
  * lm_head_argmax_topk - LM-head GEMV fused with token selection.
@@ -99,6 +115,13 @@ W4A16_API int lm_head_argmax_topk(const uint16_t *x, const uint32_t *qweight,
                         int M, int N, int K, int group, int k,
                         int32_t *idx, float *val,
                         void *workspace, size_t workspace_bytes, void *stream);
+
+/* lm_head_argmax_topk with launch flags (W4A16_OVERLAP_PREVIOUS or 0). */
+W4A16_API int lm_head_argmax_topk_ex(const uint16_t *x, const uint32_t *qweight,
+                        const uint16_t *scales, const uint16_t *biases,
+                        int M, int N, int K, int group, int k,
+                        int32_t *idx, float *val,
+                        void *workspace, size_t workspace_bytes, unsigned flags, void *stream);
 
 /*
  * lm_head_argmax_topk_noalloc - lm_head_argmax_topk without a workspace

@@ -17,7 +17,7 @@ import os
 
 import torch
 
-__all__ = ["w4_gemv", "lm_head_argmax_topk", "lm_head_workspace_bytes", "w4_dequant_f16",
+__all__ = ["OVERLAP_PREVIOUS", "w4_gemv", "lm_head_argmax_topk", "lm_head_workspace_bytes", "w4_dequant_f16",
            "f16_gemm", "device_status", "W4A16Error", "LIB_PATH", "lib"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -42,6 +42,8 @@ def _load() -> ctypes.CDLL:
     P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     L.w4_gemv.argtypes = [P, P, P, P, P, I, I, I, I, P]
     L.lm_head_argmax_topk.argtypes = [P, P, P, P, I, I, I, I, I, P, P, P, Z, P]
+    L.w4_gemv_ex.argtypes = [P, P, P, P, P, I, I, I, I, ctypes.c_uint, P]
+    L.lm_head_argmax_topk_ex.argtypes = [P, P, P, P, I, I, I, I, I, P, P, P, Z, ctypes.c_uint, P]
     L.lm_head_workspace_bytes.argtypes = [I, I, I]
     L.lm_head_workspace_bytes.restype = Z
     L.w4_dequant_f16.argtypes = [P, P, P, P, I, I, I, P]
@@ -49,7 +51,8 @@ def _load() -> ctypes.CDLL:
     L.w4a16_status_string.argtypes = [I]
     L.w4a16_status_string.restype = ctypes.c_char_p
     L.w4a16_device_status.argtypes = []
-    for f in ("w4_gemv", "lm_head_argmax_topk", "w4_dequant_f16", "f16_gemm", "w4a16_device_status"):
+    for f in ("w4_gemv", "w4_gemv_ex", "lm_head_argmax_topk", "lm_head_argmax_topk_ex", "w4_dequant_f16",
+              "f16_gemm", "w4a16_device_status"):
         getattr(L, f).restype = I
     return L
 
@@ -80,6 +83,7 @@ def _stream(stream) -> int:
 
 
 _QW = (torch.int32, getattr(torch, "uint32", torch.int32))
+OVERLAP_PREVIOUS = 1  # W4A16_OVERLAP_PREVIOUS: stream weights before the previous kernel finishes
 _H = (torch.float16,)
 
 
@@ -92,16 +96,17 @@ def _weight_dims(qweight, scales, biases, group):
 
 
 def w4_gemv(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
-            y: torch.Tensor | None = None, group: int = 64, stream=None) -> torch.Tensor:
-    """y[M][N] = x[M][K] @ W^T for the int4 weight (M <= 16)."""
+            y: torch.Tensor | None = None, group: int = 64, stream=None, flags: int = 0) -> torch.Tensor:
+    """y[M][N] = x[M][K] @ W^T for the int4 weight (M <= 16).  flags: 0 or
+    OVERLAP_PREVIOUS (the weights must not be written by the previous kernel)."""
     N, K = _weight_dims(qweight, scales, biases, group)
     x2 = x.reshape(-1, K) if x.dim() != 2 else x
     M = x2.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
-    _check("w4_gemv", lib.w4_gemv(_dev(x2, "x", _H), _dev(qweight, "qweight", _QW),
-                                  _dev(scales, "scales", _H), _dev(biases, "biases", _H),
-                                  _dev(y, "y", _H), M, N, K, group, _stream(stream)))
+    _check("w4_gemv", lib.w4_gemv_ex(_dev(x2, "x", _H), _dev(qweight, "qweight", _QW),
+                                     _dev(scales, "scales", _H), _dev(biases, "biases", _H),
+                                     _dev(y, "y", _H), M, N, K, group, flags, _stream(stream)))
     return y
 
 
@@ -112,7 +117,7 @@ def lm_head_workspace_bytes(M: int, N: int, k: int) -> int:
 def lm_head_argmax_topk(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor,
                         biases: torch.Tensor, k: int = 1, idx: torch.Tensor | None = None,
                         val: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                        group: int = 64, stream=None):
+                        group: int = 64, stream=None, flags: int = 0):
     """(idx int32 [M][k], val float32 [M][k]): the k largest logits of x @ W^T per row."""
     N, K = _weight_dims(qweight, scales, biases, group)
     x2 = x.reshape(-1, K) if x.dim() != 2 else x
@@ -125,12 +130,12 @@ def lm_head_argmax_topk(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Te
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
     _check("lm_head_argmax_topk",
-           lib.lm_head_argmax_topk(_dev(x2, "x", _H), _dev(qweight, "qweight", _QW),
-                                   _dev(scales, "scales", _H), _dev(biases, "biases", _H),
-                                   M, N, K, group, k, _dev(idx, "idx", (torch.int32,)),
-                                   _dev(val, "val", (torch.float32,)),
-                                   _dev(workspace, "workspace", (torch.uint8,)),
-                                   workspace.numel(), _stream(stream)))
+           lib.lm_head_argmax_topk_ex(_dev(x2, "x", _H), _dev(qweight, "qweight", _QW),
+                                      _dev(scales, "scales", _H), _dev(biases, "biases", _H),
+                                      M, N, K, group, k, _dev(idx, "idx", (torch.int32,)),
+                                      _dev(val, "val", (torch.float32,)),
+                                      _dev(workspace, "workspace", (torch.uint8,)),
+                                      workspace.numel(), flags, _stream(stream)))
     return idx, val
 
 

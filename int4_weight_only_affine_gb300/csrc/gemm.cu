@@ -27,7 +27,6 @@
 
 namespace w4a16 {
 
-__device__ int g_wait_expired = 0;
 
 namespace {
 
@@ -39,58 +38,6 @@ constexpr int STAGE_BYTES = A_TILE + B_TILE;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
-constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
-constexpr uint32_t kMaxSpins = 1u << 26;
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for the phase of parity `parity` to complete.
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    if (mbar_try(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (uint32_t spin = 0; spin < kMaxSpins; ++spin) {
-        if (mbar_try(bar, parity)) return true;
-        if ((spin & 63) == 63 && global_ns() - t0 > kWaitNs) break;
-    }
-    atomicExch(&g_wait_expired, 1);
-    return false;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-            "r"(dst),
-        "l"(map), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
-}
-
 // Shared-memory matrix descriptor (sm_100 family): start address, leading and
 // stride byte offsets (>> 4), descriptor version 1, 128-byte swizzle.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -302,40 +249,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-// ---------------------------------------------------------------------------
-// Host side: tensor maps through the driver entry point (no libcuda link).
-// ---------------------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
-                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                  CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
 bool make_map(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
               uint32_t box_outer) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {inner * 2};
-    const cuuint32_t box[2] = {box_inner, box_outer};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ptr, inner, outer, inner * 2, box_inner, box_outer,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace
@@ -368,16 +285,26 @@ extern "C" int f16_gemm(const uint16_t *x16, const uint16_t *w16, uint16_t *y, i
     return launch_status();
 }
 
-extern "C" int w4a16_device_status(void) {
-    if (cudaDeviceSynchronize() != cudaSuccess) return W4_ERR_LAUNCH;
+namespace w4a16 {
+int gemv_wait_flag();  // gemv.cu
+
+// Reads and clears this translation unit's expired-wait record.
+static int gemm_wait_flag() {
     int v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_wait_expired, sizeof(int)) != cudaSuccess) return W4_ERR_LAUNCH;
+    if (cudaMemcpyFromSymbol(&v, g_wait_expired, sizeof(int)) != cudaSuccess) return -1;
     if (v) {
         const int zero = 0;
         cudaMemcpyToSymbol(g_wait_expired, &zero, sizeof(int));
-        return W4_ERR_TIMEOUT;
     }
-    return W4A16_OK;
+    return v;
+}
+}  // namespace w4a16
+
+extern "C" int w4a16_device_status(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return W4_ERR_LAUNCH;
+    const int a = gemm_wait_flag(), b = gemv_wait_flag();
+    if (a < 0 || b < 0) return W4_ERR_LAUNCH;
+    return (a || b) ? W4_ERR_TIMEOUT : W4A16_OK;
 }
 
 extern "C" const char *w4a16_status_string(int status) {

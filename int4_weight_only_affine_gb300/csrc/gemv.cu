@@ -6,26 +6,33 @@
 // keeps independent weight streams in flight, and token selection runs on the
 // device so no logits vector is downloaded.
 //
-// Design (sm_103a):
-//  * A warp owns a tile of 16 output rows.  Lane (g, t) = (lane/4, lane%4)
-//    streams rows g and g+8 of the tile: for every group of 64 codes it loads
-//    words 2t and 2t+1 of each row (8 bytes per row per group; the four lanes
-//    of a row cover the group's 32 contiguous bytes).
-//  * Codes are unpacked in registers straight into the A operand of an
-//    m16n8k16 tensor-core MMA: (word >> 4j) & 0x000F000F places codes j and
-//    j+4 in the two halves of a 32-bit register as binary16 subnormals
-//    q * 2^-24, which are exact.  The B operand holds the activations of up
-//    to 8 (or 16) rows, pre-arranged in shared memory in fragment order so
-//    that the k of each A element matches.  Four MMAs cover one group with
-//    exact products and fp32 accumulation.
-//  * The affine dequantisation is folded per group: with P = sum_{k in g} q x
-//    and X = sum_{k in g} x,  sum_k w x = scale * P + bias * X.  X is
-//    computed once per CTA; the fp32 accumulators get acc_s += scale * (P *
-//    2^-24) and acc_b += bias * X, and y = 2^24 * acc_s + acc_b.
-//  * K is split across the warps of a CTA (partials reduced in shared memory
-//    in fixed order) and, for matrices with few row tiles, across the CTAs of
-//    a thread-block cluster (partials reduced through distributed shared
-//    memory by cluster rank 0, fixed order).  Results are deterministic.
+// Design (sm_103a): one streaming kernel serves both calls.
+//  * Persistent CTAs (at most one per SM), each owning a contiguous range of
+//    16-row tiles and a K-slice of them.  Warp 8 is the producer: one thread
+//    streams each tile's K-chunk (up to 32 groups) into a ring of shared
+//    memory stages with TMA (16 rows x 128 B boxes, 128-byte swizzle) and
+//    the tile's scales and biases with one contiguous bulk copy each; stage
+//    completion is counted on mbarriers (bounded waits).  Up to ~100 KB per
+//    SM are in flight without holding registers.
+//  * Warps 0-7 consume: lane (g, t) reads words 2t, 2t+1 of a group for rows
+//    g and g+8 (conflict-free under the swizzle) and unpacks them straight
+//    into the A operand of an m16n8k16 tensor-core MMA: (word >> 4j) &
+//    0x000F000F places codes j and j+4 in a half pair as binary16 subnormals
+//    q * 2^-24, which are exact.  B holds up to 8 (or 16) activation rows,
+//    pre-arranged in shared memory in fragment order.  Products are exact and
+//    accumulate in fp32.
+//  * The affine step is folded per group: with P = sum_{k in g} q x and
+//    X = sum_{k in g} x,  sum_k w x = scale * P + bias * X; acc_s += scale *
+//    (P * 2^-24), acc_b += bias * X, y = 2^24 * acc_s + acc_b.
+//  * The 8 consumer warps split each tile's K-chunk; their partial sums are
+//    combined in fixed order after one named barrier per tile.  Matrices with
+//    few tiles also split K across a thread-block cluster (2-8 CTAs), whose
+//    partials are combined once at the end through distributed shared memory.
+//    Results are deterministic.
+//  * Programmatic dependent launch: every CTA releases the next kernel at
+//    once; the producer never waits on the previous kernel (weights are
+//    constants), the consumers wait before reading activations and writing
+//    outputs.  Launched without the attribute this is ordinary stream order.
 #include <cooperative_groups.h>
 
 #include <mutex>
@@ -61,12 +68,40 @@ int device_cc() {
     return cache[dev];
 }
 
+// Reads and clears this translation unit's expired-wait record.
+int gemv_wait_flag() {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_wait_expired, sizeof(int)) != cudaSuccess) return -1;
+    if (v) {
+        const int zero = 0;
+        cudaMemcpyToSymbol(g_wait_expired, &zero, sizeof(int));
+    }
+    return v;
+}
+
 namespace {
 
-constexpr int kTileRows = 16;  // output rows per MMA tile
-constexpr int kUnroll = 4;     // groups per load batch (two batches in flight)
+constexpr int kTileRows = 16;                    // output rows per MMA tile
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;  // 256
+constexpr int kThreads = kConsumers + 32;        // + one producer warp
+constexpr int kChunkGroups = 32;                 // groups per stage (8 boxes)
+constexpr int kBoxGroups = 4;                    // 128 bytes of codes per row
+constexpr int kBoxBytes = kTileRows * 128;       // 2 KB per TMA box
+constexpr int kMaxStages = 16;
+constexpr int kMaxSmem = 227 * 1024;
+constexpr int kMaxCandidates = 16384;            // pass-2 keys per activation row
 constexpr uint32_t kNibPair = 0x000F000Fu;
+constexpr uint32_t kNibPairHi = 0x00F000F0u;
 constexpr float kTwo24 = 16777216.0f;
+
+__host__ __device__ inline int pow2_at_least(int v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) & ~(a - 1); }
 
 // ---------------------------------------------------------------------------
 // Activation staging.  For local group gl, fragment half h (MMAs j = 2h and
@@ -74,12 +109,21 @@ constexpr float kTwo24 = 16777216.0f;
 //   xf[(((gl*2 + h)*M + c)*4 + t)*4 ...]  =  {b0(2h), b1(2h), b0(2h+1), b1(2h+1)}
 // with b0(j) = (x[c][k+j], x[c][k+j+4]), b1(j) = (x[c][k+8+j], x[c][k+12+j]),
 // k = 64G + 16t.  xsum[gl*M + c] = sum of the group's 64 activations (fp32).
+// The operands of the MMAs for j = 1 and 3 are stored divided by 16 (exact
+// for |x| >= 2^-10; below that the halving error is at most 2^-25), because
+// their codes are extracted 4 bits higher (see group_mma).
+// Run by `nthreads` threads (a multiple of 32) with thread index `tid`.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t sixteenth(uint32_t h2) {
+    const __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&h2), __float2half2_rn(0.0625f));
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
 __device__ void stage_activations(const uint16_t *__restrict__ x, int M, int K, int g0, int ngl,
-                                  uint32_t *xf, float *xsum) {
+                                  uint32_t *xf, float *xsum, int tid, int nthreads) {
     const int items = ngl * M * 4;
-    for (int base = 0; base < items; base += blockDim.x) {
-        const int it = base + threadIdx.x;
+    for (int base = 0; base < items; base += nthreads) {
+        const int it = base + tid;
         float part = 0.f;
         if (it < items) {
             const int t = it & 3;
@@ -91,12 +135,12 @@ __device__ void stage_activations(const uint16_t *__restrict__ x, int M, int K, 
             uint4 f0, f1;
             f0.x = __byte_perm(lo.x, lo.z, 0x5410);  // (x0, x4)
             f0.y = __byte_perm(hi.x, hi.z, 0x5410);  // (x8, x12)
-            f0.z = __byte_perm(lo.x, lo.z, 0x7632);  // (x1, x5)
-            f0.w = __byte_perm(hi.x, hi.z, 0x7632);  // (x9, x13)
-            f1.x = __byte_perm(lo.y, lo.w, 0x5410);  // (x2, x6)
-            f1.y = __byte_perm(hi.y, hi.w, 0x5410);  // (x10, x14)
-            f1.z = __byte_perm(lo.y, lo.w, 0x7632);  // (x3, x7)
-            f1.w = __byte_perm(hi.y, hi.w, 0x7632);  // (x11, x15)
+            f0.z = sixteenth(__byte_perm(lo.x, lo.z, 0x7632));  // (x1, x5) / 16
+            f0.w = sixteenth(__byte_perm(hi.x, hi.z, 0x7632));  // (x9, x13) / 16
+            f1.x = __byte_perm(lo.y, lo.w, 0x5410);             // (x2, x6)
+            f1.y = __byte_perm(hi.y, hi.w, 0x5410);             // (x10, x14)
+            f1.z = sixteenth(__byte_perm(lo.y, lo.w, 0x7632));  // (x3, x7) / 16
+            f1.w = sixteenth(__byte_perm(hi.y, hi.w, 0x7632));  // (x11, x15) / 16
             reinterpret_cast<uint4 *>(xf)[((gl * 2 + 0) * M + c) * 4 + t] = f0;
             reinterpret_cast<uint4 *>(xf)[((gl * 2 + 1) * M + c) * 4 + t] = f1;
             const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
@@ -122,43 +166,36 @@ struct Acc {
 #pragma unroll
             for (int i = 0; i < 4; ++i) s[n][i] = b[n][i] = 0.f;
     }
+    __device__ __forceinline__ float value(int nt, int i) const { return fmaf(kTwo24, s[nt][i], b[nt][i]); }
 };
 
-// Weight and scale registers of one group for one lane.
-struct GroupRegs {
-    uint2 wa, wb;       // words 2t, 2t+1 of rows g and g+8
-    uint16_t sa, sb;    // scales of rows g, g+8
-    uint16_t ba, bb;    // biases of rows g, g+8
-};
-
-struct RowPtrs {
-    const uint32_t *qa, *qb;   // qweight rows g, g+8 (offset by 2t words)
-    const uint16_t *sa, *sb;   // scale rows
-    const uint16_t *ba, *bb;   // bias rows
-};
-
-__device__ __forceinline__ void load_group(GroupRegs &r, const RowPtrs &p, int G) {
-    r.wa = ld_nc_u64(p.qa + (size_t)G * kWordsPerGroup);
-    r.wb = ld_nc_u64(p.qb + (size_t)G * kWordsPerGroup);
-    r.sa = ld_nc_u16(p.sa + G);
-    r.sb = ld_nc_u16(p.sb + G);
-    r.ba = ld_nc_u16(p.ba + G);
-    r.bb = ld_nc_u16(p.bb + G);
-}
-
-// One group of 64 k for the warp's 16-row tile: 4 MMAs per activation tile.
+// One group (64 k) of the warp's 16-row tile: 4 MMAs per activation tile.
+// wa/wb: words 2t, 2t+1 of rows g and g+8; s*/b*: their scales and biases.
 template <int NT>
-__device__ __forceinline__ void group_step(Acc<NT> &acc, const GroupRegs &r, const uint32_t *xf,
-                                           const float *xsum, int gl, int M, int lg, int lt) {
+__device__ __forceinline__ void group_mma(Acc<NT> &acc, uint2 wa, uint2 wb, float sa, float sb, float ba,
+                                          float bb, const uint32_t *xf, const float *xsum, int gl, int M, int lg,
+                                          int lt) {
+    // Codes j and j+4 of a word as a half pair: even j from (w >> 2j) & 0x000F000F
+    // (q * 2^-24), odd j from (w >> 2(j-1)) & 0x00F000F0 (q * 2^-20, matched by
+    // activations stored / 16): one shift per word.
     uint32_t a0[4], a1[4], a2[4], a3[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        a0[j] = (r.wa.x >> (4 * j)) & kNibPair;  // row g,   cols 2t,2t+1   <- k = 16t+j, +4
-        a1[j] = (r.wb.x >> (4 * j)) & kNibPair;  // row g+8, cols 2t,2t+1
-        a2[j] = (r.wa.y >> (4 * j)) & kNibPair;  // row g,   cols 2t+8,2t+9 <- k = 16t+8+j, +4
-        a3[j] = (r.wb.y >> (4 * j)) & kNibPair;  // row g+8, cols 2t+8,2t+9
-    }
-    const float sa = h2f(r.sa), sb = h2f(r.sb), ba = h2f(r.ba), bb = h2f(r.bb);
+    const uint32_t w8[4] = {wa.x >> 8, wb.x >> 8, wa.y >> 8, wb.y >> 8};
+    a0[0] = wa.x & kNibPair;  // row g,   cols 2t,2t+1   <- k = 16t+j, +4
+    a1[0] = wb.x & kNibPair;  // row g+8, cols 2t,2t+1
+    a2[0] = wa.y & kNibPair;  // row g,   cols 2t+8,2t+9 <- k = 16t+8+j, +4
+    a3[0] = wb.y & kNibPair;  // row g+8, cols 2t+8,2t+9
+    a0[1] = wa.x & kNibPairHi;
+    a1[1] = wb.x & kNibPairHi;
+    a2[1] = wa.y & kNibPairHi;
+    a3[1] = wb.y & kNibPairHi;
+    a0[2] = w8[0] & kNibPair;
+    a1[2] = w8[1] & kNibPair;
+    a2[2] = w8[2] & kNibPair;
+    a3[2] = w8[3] & kNibPair;
+    a0[3] = w8[0] & kNibPairHi;
+    a1[3] = w8[1] & kNibPairHi;
+    a2[3] = w8[2] & kNibPairHi;
+    a3[3] = w8[3] & kNibPairHi;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int c = nt * 8 + lg;
@@ -186,141 +223,9 @@ __device__ __forceinline__ void group_step(Acc<NT> &acc, const GroupRegs &r, con
     }
 }
 
-// Dot products of the warp's 16-row tile with the staged activations over
-// groups [wg0, wg1) (global group indices; xf/xsum hold groups from g0 on).
-// Two batches of kUnroll groups are kept in flight.
-template <int NT>
-__device__ __forceinline__ void tile_dot(Acc<NT> &acc, const RowPtrs &p, int wg0, int wg1, int g0,
-                                         const uint32_t *xf, const float *xsum, int M, int lg, int lt,
-                                         GroupRegs (&bufA)[kUnroll], bool preloaded) {
-    GroupRegs bufB[kUnroll];
-    if (wg0 >= wg1) return;
-    if (!preloaded) {
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) load_group(bufA[u], p, min(wg0 + u, wg1 - 1));
-    }
-    for (int gb = wg0; gb < wg1; gb += 2 * kUnroll) {
-        if (gb + kUnroll < wg1) {
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) load_group(bufB[u], p, min(gb + kUnroll + u, wg1 - 1));
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-            if (gb + u < wg1) group_step<NT>(acc, bufA[u], xf, xsum, gb + u - g0, M, lg, lt);
-        if (gb + 2 * kUnroll < wg1) {
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) load_group(bufA[u], p, min(gb + 2 * kUnroll + u, wg1 - 1));
-        }
-        if (gb + kUnroll < wg1) {
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u)
-                if (gb + kUnroll + u < wg1)
-                    group_step<NT>(acc, bufB[u], xf, xsum, gb + kUnroll + u - g0, M, lg, lt);
-        }
-    }
-}
-
-__device__ __forceinline__ RowPtrs row_ptrs(const uint32_t *qw, const uint16_t *sc, const uint16_t *bi,
-                                            int row0, int N, int K, int lg, int lt) {
-    const int ng = K / kGroup;
-    const int ra = min(row0 + lg, N - 1), rb = min(row0 + lg + 8, N - 1);
-    RowPtrs p;
-    p.qa = qw + (size_t)ra * (K / 8) + 2 * lt;
-    p.qb = qw + (size_t)rb * (K / 8) + 2 * lt;
-    p.sa = sc + (size_t)ra * ng;
-    p.sb = sc + (size_t)rb * ng;
-    p.ba = bi + (size_t)ra * ng;
-    p.bb = bi + (size_t)rb * ng;
-    return p;
-}
-
-// Final value of accumulator element i of activation tile nt.
-template <int NT>
-__device__ __forceinline__ float acc_value(const Acc<NT> &acc, int nt, int i) {
-    return fmaf(kTwo24, acc.s[nt][i], acc.b[nt][i]);
-}
-
 // ---------------------------------------------------------------------------
-// w4_gemv kernel.  grid = (row tiles, C); cluster (1, C, 1) splits K.
-// ---------------------------------------------------------------------------
-template <int NT, int NW>
-__global__ void __launch_bounds__(NW * 32)
-    gemv_kernel(const uint16_t *__restrict__ x, const uint32_t *__restrict__ qw,
-                const uint16_t *__restrict__ sc, const uint16_t *__restrict__ bi,
-                uint16_t *__restrict__ y, int M, int N, int K, int gpc) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    const int ng = K / kGroup;
-    const int C = gridDim.y;
-    const int cr = blockIdx.y;
-    const int g0 = cr * gpc;
-    const int g1 = min(ng, g0 + gpc);
-    const int ngl = max(0, g1 - g0);
-    const int row0 = blockIdx.x * kTileRows;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int lg = lane >> 2, lt = lane & 3;
-
-    uint32_t *xf = reinterpret_cast<uint32_t *>(smem);
-    float *xsum = reinterpret_cast<float *>(smem + (size_t)ngl * M * 128);
-    float *red = xsum + ngl * M;               // [NW][16][M]
-    float *cpart = red + NW * kTileRows * M;   // [16][M]
-
-    const int wg0 = g0 + (ngl * warp) / NW;
-    const int wg1 = g0 + (ngl * (warp + 1)) / NW;
-    const RowPtrs p = row_ptrs(qw, sc, bi, row0, N, K, lg, lt);
-
-    // Start the weight stream before the activations are staged.
-    GroupRegs bufA[kUnroll];
-    if (wg0 < wg1) {
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) load_group(bufA[u], p, min(wg0 + u, wg1 - 1));
-    }
-    stage_activations(x, M, K, g0, ngl, xf, xsum);
-    __syncthreads();
-
-    Acc<NT> acc;
-    acc.zero();
-    tile_dot<NT>(acc, p, wg0, wg1, g0, xf, xsum, M, lg, lt, bufA, true);
-
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int row = lg + ((i & 2) ? 8 : 0);
-            const int col = nt * 8 + 2 * lt + (i & 1);
-            if (col < M) red[(warp * kTileRows + row) * M + col] = acc_value<NT>(acc, nt, i);
-        }
-    __syncthreads();
-
-    const int nout = kTileRows * M;  // up to 256 outputs, more than the CTA's threads
-    if (C == 1) {
-        for (int e = threadIdx.x; e < nout; e += blockDim.x) {
-            float part = 0.f;
-            for (int w = 0; w < NW; ++w) part += red[w * nout + e];
-            const int row = e / M, col = e % M;
-            if (row0 + row < N) y[(size_t)col * N + row0 + row] = __half_as_ushort(__float2half_rn(part));
-        }
-        return;
-    }
-    for (int e = threadIdx.x; e < nout; e += blockDim.x) {
-        float part = 0.f;
-        for (int w = 0; w < NW; ++w) part += red[w * nout + e];
-        cpart[e] = part;
-    }
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();
-    if (cr == 0) {
-        for (int e = threadIdx.x; e < nout; e += blockDim.x) {
-            float tot = 0.f;
-            for (int r = 0; r < C; ++r) tot += cluster.map_shared_rank(cpart, r)[e];
-            const int row = e / M, col = e % M;
-            if (row0 + row < N) y[(size_t)col * N + row0 + row] = __half_as_ushort(__float2half_rn(tot));
-        }
-    }
-    cluster.sync();
-}
-
-// ---------------------------------------------------------------------------
-// Token selection keys: order by (value desc, index asc) as one uint64.
+// Token selection keys: (value desc, index asc) as one uint64 so that larger
+// keys rank first.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint64_t make_key(float v, int idx) {
     const uint32_t u = __float_as_uint(v + 0.0f);  // -0 -> +0
@@ -363,10 +268,10 @@ __device__ uint64_t block_max_u64(uint64_t v, uint64_t *scratch) {
 
 // In-place descending bitonic sort of P (power of two) keys in shared memory.
 __device__ void bitonic_sort_desc(uint64_t *keys, int P) {
-    for (int size = 2; size <= P; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+    for (int size = 2, ls = 1; size <= P; size <<= 1, ++ls) {
+        for (int stride = size >> 1, lst = ls - 1; stride > 0; stride >>= 1, --lst) {
             for (int i = threadIdx.x; i < (P >> 1); i += blockDim.x) {
-                const int lo = 2 * stride * (i / stride) + (i % stride);
+                const int lo = ((i >> lst) << (lst + 1)) | (i & (stride - 1));
                 const int hi = lo + stride;
                 const bool desc = (lo & size) == 0;
                 const uint64_t a = keys[lo], b = keys[hi];
@@ -380,103 +285,356 @@ __device__ void bitonic_sort_desc(uint64_t *keys, int P) {
     }
 }
 
-__host__ __device__ inline int pow2_at_least(int v) {
-    int p = 1;
-    while (p < v) p <<= 1;
-    return p;
-}
 
-__host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~(size_t)15; }
-
-// Shared-memory layout of lm_head pass 1 (byte offsets, 16-byte aligned).
-struct LmSmem {
-    size_t xsum, logits, keys, total;
-};
-
-__host__ __device__ inline LmSmem lm_smem_layout(int ng, int M, int rpc, int k) {
-    LmSmem l;
-    l.xsum = align16((size_t)ng * M * 128);
-    l.logits = align16(l.xsum + (size_t)ng * M * 4);
-    l.keys = align16(l.logits + (size_t)M * rpc * 4);
-    l.total = l.keys + (size_t)pow2_at_least(rpc > k ? rpc : k) * 8;
-    return l;
-}
-
-// ---------------------------------------------------------------------------
-// lm_head pass 1: CTA b computes the logits of rows [b*rpc, (b+1)*rpc) into
-// shared memory and writes its k best keys per activation row to
-// ws[(m*G + b)*k + i].
-// ---------------------------------------------------------------------------
-template <int NT, int NW>
-__global__ void __launch_bounds__(NW * 32)
-    lmhead_pass1(const uint16_t *__restrict__ x, const uint32_t *__restrict__ qw,
-                 const uint16_t *__restrict__ sc, const uint16_t *__restrict__ bi, int M, int N,
-                 int K, int k, int rpc, uint64_t *__restrict__ ws) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    const int ng = K / kGroup;
-    const int G = gridDim.x;
-    const int n0 = blockIdx.x * rpc;
-    const int n1 = min(N, n0 + rpc);
-    const int rows = max(0, n1 - n0);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int lg = lane >> 2, lt = lane & 3;
-    const int P = pow2_at_least(max(rpc, k));
-
-    const LmSmem lay = lm_smem_layout(ng, M, rpc, k);
-    uint32_t *xf = reinterpret_cast<uint32_t *>(smem);
-    float *xsum = reinterpret_cast<float *>(smem + lay.xsum);
-    float *lgt = reinterpret_cast<float *>(smem + lay.logits);     // [M][rpc]
-    uint64_t *keys = reinterpret_cast<uint64_t *>(smem + lay.keys);  // [P]
-
-    const int ntiles = (rows + kTileRows - 1) / kTileRows;
-    GroupRegs bufA[kUnroll];
-    bool preloaded = false;
-    if (warp < ntiles) {
-        const RowPtrs p = row_ptrs(qw, sc, bi, n0 + warp * kTileRows, N, K, lg, lt);
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) load_group(bufA[u], p, min(u, ng - 1));
-        preloaded = true;
-    }
-    stage_activations(x, M, K, 0, ng, xf, xsum);
-    __syncthreads();
-
-    for (int tile = warp; tile < ntiles; tile += NW) {
-        const int row0 = n0 + tile * kTileRows;
-        const RowPtrs p = row_ptrs(qw, sc, bi, row0, N, K, lg, lt);
-        Acc<NT> acc;
-        acc.zero();
-        tile_dot<NT>(acc, p, 0, ng, 0, xf, xsum, M, lg, lt, bufA, preloaded);
-        preloaded = false;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int row = row0 + lg + ((i & 2) ? 8 : 0);
-                const int col = nt * 8 + 2 * lt + (i & 1);
-                if (col < M && row < n1) lgt[col * rpc + (row - n0)] = acc_value<NT>(acc, nt, i);
-            }
-    }
-    __syncthreads();
-
-    for (int m = 0; m < M; ++m) {
-        uint64_t *out = ws + ((size_t)m * G + blockIdx.x) * k;
-        if (k == 1) {
-            uint64_t best = 0ull;
-            for (int i = threadIdx.x; i < rows; i += blockDim.x) {
-                const uint64_t key = make_key(lgt[m * rpc + i], n0 + i);
-                best = key > best ? key : best;
-            }
-            best = block_max_u64(best, keys);
-            if (threadIdx.x == 0) out[0] = best;
-        } else {
-            for (int i = threadIdx.x; i < P; i += blockDim.x)
-                keys[i] = (i < rows) ? make_key(lgt[m * rpc + i], n0 + i) : 0ull;
+// Block-wide top-k of n distinct keys (global or shared memory), written in
+// descending order to out[0..k), zero-padded when n < k.  A radix select over
+// the value word (4 passes of 8 bits) finds the value v of the k-th largest
+// key; every key whose value word is >= v is gathered into `buf` (capacity
+// >= n) and only those are sorted.  hist: 256 words, misc: 4 words of
+// shared memory.  Called by all threads of the block.
+__device__ void block_topk(const uint64_t *keys, int n, int k, uint64_t *out, uint64_t *buf,
+                           uint32_t *hist, uint32_t *misc) {
+    const int tid = threadIdx.x, bd = blockDim.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    uint32_t prefix = 0, mask = 0;
+    if (n > k) {
+        uint32_t need = (uint32_t)k;
+        for (int shift = 24; shift >= 0; shift -= 8) {
+            for (int i = tid; i < 256; i += bd) hist[i] = 0;
             __syncthreads();
-            bitonic_sort_desc(keys, P);
-            for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = keys[i];
+            for (int i = tid; i < n; i += bd) {
+                const uint32_t hi = (uint32_t)(keys[i] >> 32);
+                if ((hi & mask) == prefix) atomicAdd(&hist[(hi >> shift) & 255u], 1u);
+            }
+            __syncthreads();
+            if (warp == 0) {
+                // lane l owns bins 255-8l .. 248-8l, scanned from the top.
+                uint32_t c[8], sum = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    c[j] = hist[255 - 8 * lane - j];
+                    sum += c[j];
+                }
+                uint32_t incl = sum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                const uint32_t excl = incl - sum;
+                if (excl < need && need <= incl) {
+                    uint32_t run = excl;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (run + c[j] >= need) {
+                            misc[0] = 255u - 8u * lane - j;
+                            misc[1] = run;
+                            break;
+                        }
+                        run += c[j];
+                    }
+                }
+            }
+            __syncthreads();
+            need -= misc[1];
+            prefix |= misc[0] << shift;
+            mask |= 255u << shift;
             __syncthreads();
         }
     }
+    if (tid == 0) misc[2] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += bd) {
+        const uint64_t key = keys[i];
+        if ((uint32_t)(key >> 32) >= prefix) buf[atomicAdd(&misc[2], 1u)] = key;
+    }
+    __syncthreads();
+    const int m = (int)misc[2];
+    const int P = pow2_at_least(m > k ? m : k);
+    for (int i = m + tid; i < P; i += bd) buf[i] = 0ull;
+    __syncthreads();
+    bitonic_sort_desc(buf, P);
+    for (int i = tid; i < k; i += bd) out[i] = buf[i];
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// The streaming kernel.
+// ---------------------------------------------------------------------------
+
+// Everything a launch needs besides the weight tensor map.  Byte offsets are
+// relative to the 1024-aligned start of dynamic shared memory.
+struct StreamArgs {
+    const uint16_t *x, *sc, *bi;
+    uint16_t *y;   // w4_gemv: output [M][N]
+    uint64_t *ws;  // lm_head pass 1: candidate keys [M][gridDim.x][k]
+    int M, N, K, k;
+    int C;       // CTAs per cluster splitting K
+    int tiles;   // ceil(N / 16)
+    int stages;  // ring depth
+    int ng;      // groups along K
+    int units;   // 8-group units along K
+    int nq_full; // whole 128-byte quads (4 groups) per row
+    int cq;      // quads per 3-D copy
+    int defer;   // 1: per-warp partials of all tiles kept, combined once at the end
+    uint32_t stage_bytes, w_bytes;
+    uint32_t off_xf, off_xsum, off_red, off_res, off_bar;
+};
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+
+template <int NT, bool LMHEAD>
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
+    stream_kernel(const __grid_constant__ CUtensorMap tm3, const __grid_constant__ CUtensorMap tm2,
+                  const StreamArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sb = smem_raw + (base - raw);
+    pdl_launch_dependents();
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int M = a.M, N = a.N, ng = a.ng, S = a.stages, C = a.C;
+    const int rank = blockIdx.x % C;
+    const int ncl = gridDim.x / C, cl = blockIdx.x / C;
+    const int t0 = (int)((long long)cl * a.tiles / ncl);
+    const int t1 = (int)((long long)(cl + 1) * a.tiles / ncl);
+    const int ntl = t1 - t0;
+    const int gs0 = 8 * (rank * a.units / C);
+    const int gs1 = min(ng, 8 * ((rank + 1) * a.units / C));
+    const int ngl = max(0, gs1 - gs0);
+    const int nch = (ngl + kChunkGroups - 1) / kChunkGroups;
+    const int out16 = kTileRows * M;
+
+    uint32_t *xf = reinterpret_cast<uint32_t *>(sb + a.off_xf);
+    float *xsum = reinterpret_cast<float *>(sb + a.off_xsum);
+    float *red = reinterpret_cast<float *>(sb + a.off_red);  // [2][8][16*M]
+    float *res = reinterpret_cast<float *>(sb + a.off_res);  // [ntl][16*M]
+    const uint32_t bar0 = base + a.off_bar;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sb + a.off_bar + 16 * S);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), kConsumerWarps);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tm3) : "memory");
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ---------------- producer: weights need no dependency wait ----------------
+        if (lane == 0) {
+            uint32_t issued_ph = 0, issued_any = 0;
+            int it = 0;
+            bool ok = true;
+            for (int tl = 0; tl < ntl && ok; ++tl) {
+                const int t = t0 + tl;
+                const bool tail = (t + 1) * kTileRows > N;
+                for (int ch = 0; ch < nch; ++ch, ++it) {
+                    const int s = it % S;
+                    const uint32_t ph = (it / S) & 1;
+                    if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const int cg0 = gs0 + ch * kChunkGroups;
+                    const int len = min(kChunkGroups, gs1 - cg0);
+                    const int q0 = cg0 / kBoxGroups;
+                    const int nbox = (len + kBoxGroups - 1) / kBoxGroups;
+                    const uint32_t sbytes = tail ? 0u : 32u * ng;
+                    const uint32_t st = base + s * a.stage_bytes;
+                    if (q0 + nbox <= a.nq_full) {
+                        // One 3-D copy: cq quads x 16 rows x 128 B, the same swizzled
+                        // image as cq separate 16 x 128 B boxes.
+                        mbar_expect_tx(full_bar(s), a.cq * kBoxBytes + 2 * sbytes);
+                        tma_load_3d(st, &tm3, 0, t * kTileRows, q0, full_bar(s));
+                    } else {
+                        // The chunk holding the ragged end of a row: one box per quad.
+                        mbar_expect_tx(full_bar(s), nbox * kBoxBytes + 2 * sbytes);
+                        for (int b = 0; b < nbox; ++b)
+                            tma_load_2d(st + b * kBoxBytes, &tm2, (q0 + b) * 32, t * kTileRows, full_bar(s));
+                    }
+                    if (!tail) {
+                        bulk_load(st + a.w_bytes, a.sc + (size_t)t * kTileRows * ng, sbytes, full_bar(s));
+                        bulk_load(st + a.w_bytes + sbytes, a.bi + (size_t)t * kTileRows * ng, sbytes, full_bar(s));
+                    }
+                    issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+                    issued_any |= 1u << s;
+                }
+            }
+            // Every copy issued here has landed before the CTA moves on.
+            for (int s = 0; s < S; ++s)
+                if (issued_any & (1u << s)) mbar_wait(full_bar(s), (issued_ph >> s) & 1);
+        }
+    } else {
+        // ---------------- consumers ----------------
+        const int lg = lane >> 2, lt = lane & 3;
+        // Groups of a chunk go to the warps round-robin (warp w takes w, w+8,
+        // w+16, w+24), so a warp always reads the same 16-byte chunk of a box
+        // row: its swizzled offset and the stride between its groups are fixed.
+        const int wsw = ((((warp & 3) << 1) | (lt >> 1)) ^ (lg & 7)) << 4;
+        const int lane_w = lg * 128 + ((lt & 1) << 3) + (warp >> 2) * kBoxBytes + wsw;
+        const int xstride = 8 * 2 * M * 4;  // uint4 words of staged activations per 8 groups
+        pdl_wait();
+        stage_activations(a.x, M, a.K, gs0, ngl, xf, xsum, tid, kConsumers);
+        consumer_sync();
+        int it = 0;
+        for (int tl = 0; tl < ntl; ++tl) {
+            const int t = t0 + tl;
+            const int row0 = t * kTileRows;
+            const bool tail = row0 + kTileRows > N;
+            Acc<NT> acc;
+            acc.zero();
+            for (int ch = 0; ch < nch; ++ch, ++it) {
+                const int s = it % S;
+                const uint32_t ph = (it / S) & 1;
+                const bool ok = mbar_wait(full_bar(s), ph, abort_flag);
+                uint8_t *st = sb + (size_t)s * a.stage_bytes;
+                uint16_t *sp = reinterpret_cast<uint16_t *>(st + a.w_bytes);  // [16][ng] scales, then biases
+                if (tail) {
+                    // The producer copies no scales for the ragged last tile (its rows
+                    // end inside the arrays); fill them here, rows past N repeated.
+                    for (int i = tid; i < 2 * kTileRows * ng; i += kConsumers) {
+                        const int arr = i / (kTileRows * ng), r = (i / ng) % kTileRows, gi = i % ng;
+                        const uint16_t *src = arr ? a.bi : a.sc;
+                        sp[i] = src[(size_t)min(row0 + r, N - 1) * ng + gi];
+                    }
+                    consumer_sync();
+                }
+                if (ok) {
+                    const int cg0 = gs0 + ch * kChunkGroups;
+                    const int len = min(kChunkGroups, gs1 - cg0);
+                    const int cnt = len > warp ? (len - warp + kConsumerWarps - 1) / kConsumerWarps : 0;
+                    const uint8_t *wp = st + lane_w;
+                    const uint16_t *sa = sp + lg * ng + cg0 + warp;
+                    const uint16_t *sbb = sa + 8 * ng;
+                    const uint16_t *ba = sa + kTileRows * ng;
+                    const uint16_t *bb = sbb + kTileRows * ng;
+                    const int gl0 = cg0 - gs0 + warp;
+#pragma unroll
+                    for (int j = 0; j < kChunkGroups / kConsumerWarps; ++j) {
+                        if (j < cnt) {
+                            const uint2 wa = *reinterpret_cast<const uint2 *>(wp + j * 2 * kBoxBytes);
+                            const uint2 wb = *reinterpret_cast<const uint2 *>(wp + j * 2 * kBoxBytes + 8 * 128);
+                            group_mma<NT>(acc, wa, wb, h2f(sa[8 * j]), h2f(sbb[8 * j]), h2f(ba[8 * j]), h2f(bb[8 * j]),
+                                          xf, xsum, gl0 + 8 * j, M, lg, lt);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(s));
+            }
+            if (a.defer) {
+                // Keep this warp's partial; all tiles are combined once at the end.
+                float *mine = red + ((size_t)tl * kConsumerWarps + warp) * out16;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int row = lg + ((i & 2) ? 8 : 0);
+                        const int col = nt * 8 + 2 * lt + (i & 1);
+                        if (col < M) mine[row * M + col] = acc.value(nt, i);
+                    }
+                continue;
+            }
+            // Per-tile reduction over the 8 consumer warps, fixed order.
+            float *mine = red + ((tl & 1) * kConsumerWarps + warp) * out16;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int row = lg + ((i & 2) ? 8 : 0);
+                    const int col = nt * 8 + 2 * lt + (i & 1);
+                    if (col < M) mine[row * M + col] = acc.value(nt, i);
+                }
+            consumer_sync();
+            if (warp == (tl & (kConsumerWarps - 1))) {
+                const float *grp = red + (tl & 1) * kConsumerWarps * out16;
+                for (int e = lane; e < out16; e += 32) {
+                    float v = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kConsumerWarps; ++w) v += grp[w * out16 + e];
+                    if (!LMHEAD && C == 1) {
+                        const int row = e / M, col = e % M;
+                        if (row0 + row < N) a.y[(size_t)col * N + row0 + row] = __half_as_ushort(__float2half_rn(v));
+                    } else {
+                        res[tl * out16 + e] = v;
+                    }
+                }
+            }
+        }
+        if (a.defer) {
+            consumer_sync();
+            for (int i = tid; i < ntl * out16; i += kConsumers) {
+                const int tl = i / out16, e = i % out16;
+                const float *grp = red + (size_t)tl * kConsumerWarps * out16;
+                float v = 0.f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) v += grp[w * out16 + e];
+                if (!LMHEAD && C == 1) {
+                    const int row = e / M, col = e % M, r = (t0 + tl) * kTileRows + row;
+                    if (r < N) a.y[(size_t)col * N + r] = __half_as_ushort(__float2half_rn(v));
+                } else {
+                    res[tl * out16 + e] = v;
+                }
+            }
+        }
+        (void)xstride;
+    }
+    __syncthreads();
+
+    if (!LMHEAD) {
+        if (C > 1) {
+            // Tile tl is finished by rank tl % C, summing the ranks in order.
+            cg::cluster_group cluster = cg::this_cluster();
+            cluster.sync();
+            for (int tl = rank; tl < ntl; tl += C) {
+                const int row0 = (t0 + tl) * kTileRows;
+                for (int e = tid; e < out16; e += kThreads) {
+                    float v = 0.f;
+                    for (int q = 0; q < C; ++q) v += cluster.map_shared_rank(res, q)[tl * out16 + e];
+                    const int row = e / M, col = e % M;
+                    if (row0 + row < N) a.y[(size_t)col * N + row0 + row] = __half_as_ushort(__float2half_rn(v));
+                }
+            }
+            cluster.sync();
+        }
+        return;
+    }
+
+    // ---------------- lm_head pass 1: k best keys of this CTA's rows ----------------
+    const int n0 = t0 * kTileRows;
+    const int rows = min(N, t1 * kTileRows) - n0;
+    const int P = pow2_at_least(rows > a.k ? rows : a.k);
+    uint64_t *keys = reinterpret_cast<uint64_t *>(sb);  // the ring is free now
+    uint64_t *buf = keys + P;
+    uint32_t *hist = reinterpret_cast<uint32_t *>(buf + P);
+    for (int m = 0; m < M; ++m) {
+        uint64_t *out = a.ws + ((size_t)m * gridDim.x + blockIdx.x) * a.k;
+        if (a.k == 1) {
+            uint64_t best = 0ull;
+            for (int i = tid; i < rows; i += kThreads) {
+                const uint64_t key = make_key(res[i * M + m], n0 + i);
+                best = key > best ? key : best;
+            }
+            best = block_max_u64(best, keys);
+            if (tid == 0) out[0] = best;
+        } else {
+            for (int i = tid; i < rows; i += kThreads) keys[i] = make_key(res[i * M + m], n0 + i);
+            __syncthreads();
+            block_topk(keys, rows, a.k, out, buf, hist, hist + 256);
+        }
+    }
+}
+
+const void *stream_kernel_ptr(int M, bool lmhead) {
+    if (lmhead) return M <= 8 ? (const void *)stream_kernel<1, true> : (const void *)stream_kernel<2, true>;
+    return M <= 8 ? (const void *)stream_kernel<1, false> : (const void *)stream_kernel<2, false>;
 }
 
 // lm_head pass 2: one CTA per activation row merges the G*k candidates.
@@ -501,111 +659,24 @@ __global__ void __launch_bounds__(1024)
         }
         return;
     }
-    const int P = pow2_at_least(n);
-    for (int i = threadIdx.x; i < P; i += blockDim.x) keys[i] = (i < n) ? src[i] : 0ull;
-    __syncthreads();
-    bitonic_sort_desc(keys, P);
+    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + (size_t)pow2_at_least(n) * 8);
+    __shared__ uint64_t top[64];
+    block_topk(src, n, k, top, keys, hist, hist + 256);
     for (int i = threadIdx.x; i < k; i += blockDim.x) {
         float v;
         int id;
-        decode_key(keys[i], v, id);
+        decode_key(top[i], v, id);
         idx[(size_t)m * k + i] = id;
         val[(size_t)m * k + i] = v;
     }
 }
 
 // ---------------------------------------------------------------------------
-// Host-side planning.
+// Host-side planning and launch.
 // ---------------------------------------------------------------------------
-constexpr int kGemvWarps = 4;
-constexpr int kLmWarps = 16;
-constexpr int kMaxSmem = 227 * 1024;
-constexpr int kMaxCandidates = 16384;  // pass-2 sort size (keys)
 
-struct GemvPlan {
-    int C;      // CTAs per cluster splitting K
-    int gpc;    // groups per CTA
-    size_t smem;
-};
-
-size_t gemv_smem(int ngl, int M) {
-    return (size_t)ngl * M * 128 + (size_t)ngl * M * 4 + (size_t)kGemvWarps * kTileRows * M * 4 +
-           (size_t)kTileRows * M * 4;
-}
-
-GemvPlan plan_gemv(int M, int N, int K) {
-    const int ng = K / kGroup;
-    const int rt = (N + kTileRows - 1) / kTileRows;
-    const int target = 2 * sm_count();
-    GemvPlan pl{1, ng, 0};
-    int C = 1;
-    while (C < 8 && rt * C < target && ng / (2 * C) >= kGemvWarps) C *= 2;
-    // Keep the staged activations within shared memory.
-    while (C < 8 && gemv_smem((ng + C - 1) / C, M) > (size_t)kMaxSmem / 2) C *= 2;
-    pl.C = C;
-    pl.gpc = (ng + C - 1) / C;
-    pl.smem = gemv_smem(pl.gpc, M);
-    return pl;
-}
-
-// Raise a kernel's dynamic shared-memory limit once per device (and only
-// upwards), so that launches captured into CUDA graphs issue no attribute calls.
-template <typename Kern>
-bool ensure_smem(Kern kern, size_t bytes) {
-    static size_t granted[64] = {0};
-    if (bytes <= 48 * 1024) return true;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-    if (granted[dev] >= bytes) return true;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
-        return false;
-    granted[dev] = bytes;
-    return true;
-}
-
-template <int NT>
-int launch_gemv(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, const uint16_t *bi,
-                uint16_t *y, int M, int N, int K, cudaStream_t st) {
-    const GemvPlan pl = plan_gemv(M, N, K);
-    if (pl.smem > (size_t)kMaxSmem) return W4_ERR_SHAPE;
-    auto kern = gemv_kernel<NT, kGemvWarps>;
-    if (!ensure_smem(kern, pl.smem)) return W4_ERR_LAUNCH;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((N + kTileRows - 1) / kTileRows, pl.C, 1);
-    cfg.blockDim = dim3(kGemvWarps * 32, 1, 1);
-    cfg.dynamicSmemBytes = pl.smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = pl.C;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pl.C > 1 ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, x, qw, sc, bi, y, M, N, K, pl.gpc);
-    return e == cudaSuccess ? W4A16_OK : W4_ERR_LAUNCH;
-}
-
-struct LmPlan {
-    int G, rpc;
-    size_t smem1, smem2;
-};
-
-bool plan_lmhead(int M, int N, int K, int k, int sms, LmPlan &pl) {
-    const int ng = K / kGroup;
-    const int max_rpc = 16384 / M;  // logits buffer <= 64 KB
-    int rpc = (N + sms - 1) / sms;
-    rpc = ((rpc + kTileRows - 1) / kTileRows) * kTileRows;
-    const int min_rpc_cand = (int)(((long long)N * k + kMaxCandidates - 1) / kMaxCandidates);
-    if (rpc < min_rpc_cand) rpc = ((min_rpc_cand + kTileRows - 1) / kTileRows) * kTileRows;
-    if (rpc > max_rpc) return false;
-    pl.rpc = rpc;
-    pl.G = (N + rpc - 1) / rpc;
-    if ((long long)pl.G * k > kMaxCandidates) return false;
-    pl.smem1 = lm_smem_layout(ng, M, rpc, k).total;
-    pl.smem2 = (size_t)(k == 1 ? 32 : pow2_at_least(pl.G * k)) * 8;
-    return pl.smem1 <= (size_t)kMaxSmem && pl.smem2 <= (size_t)kMaxSmem;
-}
+// Pass 2 shared memory: gather buffer for up to n keys + histogram.
+inline size_t lm_pass2_smem(int n, int k) { return k == 1 ? 64 * 8 : (size_t)pow2_at_least(n) * 8 + 260 * 4; }
 
 // Upper bound on the pass-1 grid for a given (N, k), independent of the GPU.
 long long lm_max_blocks(int N, int k) {
@@ -614,24 +685,287 @@ long long lm_max_blocks(int N, int k) {
     return tiles < cap ? tiles : cap;
 }
 
-template <int NT>
-int launch_lmhead(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, const uint16_t *bi, int M,
-                  int N, int K, int k, int32_t *idx, float *val, uint64_t *ws, const LmPlan &pl,
-                  cudaStream_t st) {
-    auto k1 = lmhead_pass1<NT, kLmWarps>;
-    if (!ensure_smem(k1, pl.smem1) || !ensure_smem(lmhead_pass2, pl.smem2)) return W4_ERR_LAUNCH;
-    k1<<<pl.G, kLmWarps * 32, pl.smem1, st>>>(x, qw, sc, bi, M, N, K, k, pl.rpc, ws);
-    if (cudaGetLastError() != cudaSuccess) return W4_ERR_LAUNCH;
-    lmhead_pass2<<<M, 1024, pl.smem2, st>>>(ws, pl.G, k, idx, val);
-    return launch_status();
+struct StreamPlan {
+    StreamArgs a;
+    int grid;
+    size_t smem;
+};
+
+bool layout_stream(StreamPlan &p, int M, bool lmhead, size_t ring_budget, int tpc, int slice_groups) {
+    StreamArgs &a = p.a;
+    const int ng = a.ng;
+    const int wbox = min(kChunkGroups, slice_groups + kBoxGroups - 1) / kBoxGroups;
+    a.w_bytes = (uint32_t)(wbox * kBoxBytes);
+    a.cq = wbox;
+    a.nq_full = a.K / 256;
+    a.stage_bytes = (uint32_t)align_up((size_t)a.w_bytes + 64u * ng, 1024);
+    // As many stages as the byte budget allows: the ring is what keeps HBM busy.
+    const int stages = (int)max((size_t)2, min((size_t)kMaxStages, ring_budget / a.stage_bytes));
+    a.stages = stages;
+    size_t off = (size_t)stages * a.stage_bytes;
+    if (lmhead) {
+        // After the main loop the ring holds the selection keys.
+        const int P = pow2_at_least(max(tpc * kTileRows, a.k));
+        const size_t need = (size_t)2 * P * 8 + 260 * 4;
+        if (off < need) off = align_up(need, 1024);
+    }
+    a.off_xf = (uint32_t)off;
+    off = align_up(off + (size_t)slice_groups * M * 128, 16);
+    a.off_xsum = (uint32_t)off;
+    off = align_up(off + (size_t)slice_groups * M * 4, 16);
+    a.off_red = (uint32_t)off;
+    const size_t red_all = (size_t)tpc * kConsumerWarps * kTileRows * M * 4;
+    a.defer = red_all <= 32 * 1024 ? 1 : 0;
+    off = align_up(off + (a.defer ? red_all : (size_t)2 * kConsumerWarps * kTileRows * M * 4), 16);
+    a.off_res = (uint32_t)off;
+    if (lmhead || a.C > 1) off = align_up(off + (size_t)tpc * kTileRows * M * 4, 16);
+    a.off_bar = (uint32_t)off;
+    off += 16 * stages + 16;
+    p.smem = off + 1024;  // alignment slack
+    return true;
 }
 
-int check_common(const void *x, const uint32_t *qw, const uint16_t *sc, const uint16_t *bi, int M, int N,
-                 int K, int group) {
+// CTAs per SM: two for up to 8 activation rows (16 consumer warps per SM and
+// two rings in flight), one otherwise.
+int ctas_per_sm(int M) { return M <= 8 ? 2 : 1; }
+
+const void *stream_kernel_ptr(int M, bool lmhead);
+bool ensure_smem(const void *kern, size_t bytes);
+
+// Clusters of C CTAs (this kernel, this shared memory) that can be resident
+// at once; cached per (kernel, C, bytes, device).
+int max_active_clusters(const void *kern, int C, size_t smem, int fallback) {
+    struct Entry {
+        const void *kern;
+        int C, dev;
+        size_t smem;
+        int n;
+    };
+    static std::mutex mu;
+    static Entry cache[128];
+    static int n = 0;
+    if (C == 1) return fallback;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fallback;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n; ++i)
+        if (cache[i].kern == kern && cache[i].C == C && cache[i].smem == smem && cache[i].dev == dev)
+            return cache[i].n;
+    int v = 0;
+    if (!ensure_smem(kern, smem)) return fallback;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C * 64, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&v, kern, &cfg) != cudaSuccess || v <= 0) {
+        cudaGetLastError();
+        v = fallback;
+    }
+    if (n < 128) cache[n++] = Entry{kern, C, dev, smem, v};
+    return v;
+}
+
+// Lays out a launch with C CTAs per cluster; false if it does not fit.
+bool plan_with_cluster(StreamPlan &p, int C, int slots, int per_sm, bool lmhead) {
+    StreamArgs &a = p.a;
+    a.C = C;
+    int ncl = min(a.tiles, max(1, slots / C));
+    if (C > 1) {
+        // Size the shared memory first (it does not depend on the cluster
+        // count beyond tiles per cluster), then keep every cluster resident.
+        StreamPlan probe = p;
+        const int tpc0 = (a.tiles + ncl - 1) / ncl;
+        const int slice0 = min(a.ng, 8 * ((a.units + C - 1) / C));
+        layout_stream(probe, a.M, lmhead, (size_t)kMaxSmem / per_sm - (per_sm == 2 ? 24 * 1024 : 0), tpc0,
+                      slice0);
+        const int act = max_active_clusters(stream_kernel_ptr(a.M, lmhead), C, probe.smem, ncl);
+        ncl = min(ncl, max(1, act));
+    }
+    p.grid = ncl * C;
+    const int tpc = (a.tiles + ncl - 1) / ncl;
+    const int slice = min(a.ng, 8 * ((a.units + C - 1) / C));
+    const size_t per_cta = (size_t)kMaxSmem / per_sm;
+    for (size_t budget = per_cta; budget >= 16 * 1024; budget -= 8 * 1024) {
+        layout_stream(p, a.M, lmhead, budget - (per_sm == 2 ? 24 * 1024 : 0), tpc, slice);
+        if (p.smem <= per_cta) return true;
+    }
+    return false;
+}
+
+bool plan_stream(StreamPlan &p, int M, int N, int K, bool lmhead, int k) {
+    StreamArgs &a = p.a;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.k = k;
+    a.ng = K / kGroup;
+    a.units = (a.ng + 7) / 8;
+    a.tiles = (N + kTileRows - 1) / kTileRows;
+    const int per_sm = ctas_per_sm(M);
+    int slots = sm_count() * per_sm;
+    if (lmhead) slots = min(slots, kMaxCandidates / k);
+    // Split K over a cluster only when the tiles alone cannot spread evenly
+    // over the SMs or the activations of a whole row do not fit (cost = work
+    // of the busiest cluster in 16-row x 8-group units; a split must save at
+    // least 10 %).
+    int bestC = 0;
+    long long bestCost = -1;
+    for (int C = 1; C <= (lmhead ? 1 : 8); C *= 2) {
+        if (C > a.units) break;
+        StreamPlan trial = p;
+        if (!plan_with_cluster(trial, C, slots, per_sm, lmhead)) continue;
+        const int ncl = trial.grid / C;
+        const long long cost = (long long)((a.tiles + ncl - 1) / ncl) * ((a.units + C - 1) / C);
+        if (bestCost < 0 || cost * 10 < bestCost * 9) {
+            bestC = C;
+            bestCost = cost;
+        }
+    }
+    if (bestC == 0) return false;
+    return plan_with_cluster(p, bestC, slots, per_sm, lmhead);
+}
+
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device), and
+// only upwards, so that launches captured into CUDA graphs issue no attribute
+// calls.
+bool ensure_smem(const void *kern, size_t bytes) {
+    struct Grant {
+        const void *kern;
+        int dev;
+        size_t bytes;
+    };
+    static std::mutex mu;
+    static Grant grants[64];
+    static int ngrants = 0;
+    if (bytes <= 48 * 1024) return true;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    int slot = -1;
+    for (int i = 0; i < ngrants; ++i)
+        if (grants[i].kern == kern && grants[i].dev == dev) slot = i;
+    if (slot >= 0 && grants[slot].bytes >= bytes) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess) {
+        cudaGetLastError();  // leave no stale error for a later launch check
+        return false;
+    }
+    if (slot < 0 && ngrants < 64) slot = ngrants++;
+    if (slot >= 0) grants[slot] = Grant{kern, dev, bytes};
+    return true;
+}
+
+template <int NT, bool LM>
+int launch_stream(const StreamPlan &p, const uint32_t *qw, bool overlap, cudaStream_t st) {
+    CUtensorMap tm3, tm2;
+    const uint64_t KW = (uint64_t)p.a.K / 8;
+    if (!make_map_2d(&tm2, CU_TENSOR_MAP_DATA_TYPE_UINT32, qw, KW, (uint64_t)p.a.N, KW * 4, 32, kTileRows,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+        return W4_ERR_DEVICE;
+    if (p.a.nq_full > 0) {
+        if (!make_map_3d(&tm3, CU_TENSOR_MAP_DATA_TYPE_UINT32, qw, 32, (uint64_t)p.a.N, (uint64_t)p.a.nq_full, KW * 4,
+                         128, 32, kTileRows, (uint32_t)p.a.cq, CU_TENSOR_MAP_SWIZZLE_128B))
+            return W4_ERR_DEVICE;
+    } else {
+        tm3 = tm2;  // never used: every chunk takes the 2-D path
+    }
+    auto kern = stream_kernel<NT, LM>;
+    if (!ensure_smem(reinterpret_cast<const void *>(kern), p.smem)) return W4_ERR_LAUNCH;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (p.a.C > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = p.a.C;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (overlap) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tm3, tm2, p.a);
+    return e == cudaSuccess ? W4A16_OK : W4_ERR_LAUNCH;
+}
+
+int check_common(const void *x, const uint32_t *qw, const uint16_t *sc, const uint16_t *bi, int M, int N, int K,
+                 int group) {
     if (!x || !qw || !sc || !bi) return W4_ERR_NULL;
     if (group != kGroup) return W4_ERR_GROUP;
     if (M < 1 || M > 16 || N < 1 || K < kGroup || K % kGroup != 0) return W4_ERR_SHAPE;
     if (!aligned16(x) || !aligned16(qw) || !aligned16(sc) || !aligned16(bi)) return W4_ERR_ALIGN;
+    return W4A16_OK;
+}
+
+int gemv_impl(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, const uint16_t *bi, uint16_t *y, int M,
+              int N, int K, int group, unsigned flags, void *stream) {
+    int st = check_common(x, qw, sc, bi, M, N, K, group);
+    if (st != W4A16_OK) return st;
+    if (!y) return W4_ERR_NULL;
+    if (!aligned16(y)) return W4_ERR_ALIGN;
+    if (flags & ~(unsigned)W4A16_OVERLAP_PREVIOUS) return W4_ERR_SHAPE;
+    StreamPlan p;
+    if (!plan_stream(p, M, N, K, false, 1)) return W4_ERR_SHAPE;
+    p.a.x = x;
+    p.a.sc = sc;
+    p.a.bi = bi;
+    p.a.y = y;
+    p.a.ws = nullptr;
+    const bool ov = (flags & W4A16_OVERLAP_PREVIOUS) != 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return M <= 8 ? launch_stream<1, false>(p, qw, ov, s) : launch_stream<2, false>(p, qw, ov, s);
+}
+
+int lmhead_impl(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, const uint16_t *bi, int M, int N, int K,
+                int group, int k, int32_t *idx, float *val, uint64_t *ws, size_t ws_bytes, unsigned flags,
+                void *stream) {
+    StreamPlan p;
+    if (!plan_stream(p, M, N, K, true, k)) return W4_ERR_SHAPE;
+    const int G = p.grid;
+    if ((long long)G > lm_max_blocks(N, k)) return W4_ERR_SHAPE;
+    if (ws_bytes < (size_t)M * G * k * sizeof(uint64_t)) return W4_ERR_WORKSPACE;
+    const size_t smem2 = lm_pass2_smem(G * k, k);
+    if (smem2 > (size_t)kMaxSmem) return W4_ERR_SHAPE;
+    p.a.x = x;
+    p.a.sc = sc;
+    p.a.bi = bi;
+    p.a.y = nullptr;
+    p.a.ws = ws;
+    const bool ov = (flags & W4A16_OVERLAP_PREVIOUS) != 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int st = M <= 8 ? launch_stream<1, true>(p, qw, ov, s) : launch_stream<2, true>(p, qw, ov, s);
+    if (st != W4A16_OK) return st;
+    if (!ensure_smem(reinterpret_cast<const void *>(lmhead_pass2), smem2)) return W4_ERR_LAUNCH;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(M, 1, 1);
+    cfg.blockDim = dim3(1024, 1, 1);
+    cfg.dynamicSmemBytes = smem2;
+    cfg.stream = s;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, lmhead_pass2, (const uint64_t *)ws, G, k, idx, val);
+    return e == cudaSuccess ? W4A16_OK : W4_ERR_LAUNCH;
+}
+
+int lmhead_checks(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, const uint16_t *bi, int M, int N, int K,
+                  int group, int k, int32_t *idx, float *val) {
+    int st = check_common(x, qw, sc, bi, M, N, K, group);
+    if (st != W4A16_OK) return st;
+    if (!idx || !val) return W4_ERR_NULL;
+    if (k < 1 || k > 64 || k > N || (long long)N * k > 16777216LL) return W4_ERR_SHAPE;
+    if (!aligned16(idx) || !aligned16(val)) return W4_ERR_ALIGN;
     return W4A16_OK;
 }
 
@@ -640,17 +974,14 @@ int check_common(const void *x, const uint32_t *qw, const uint16_t *sc, const ui
 
 using namespace w4a16;
 
-extern "C" int w4_gemv(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
-                       const uint16_t *biases, uint16_t *y, int M, int N, int K, int group,
-                       void *stream) {
-    int st = check_common(x, qweight, scales, biases, M, N, K, group);
-    if (st != W4A16_OK) return st;
-    if (!y) return W4_ERR_NULL;
-    if (!aligned16(y)) return W4_ERR_ALIGN;
-    if (gemv_smem((K / kGroup + 7) / 8, M) > (size_t)kMaxSmem) return W4_ERR_SHAPE;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return M <= 8 ? launch_gemv<1>(x, qweight, scales, biases, y, M, N, K, s)
-                  : launch_gemv<2>(x, qweight, scales, biases, y, M, N, K, s);
+extern "C" int w4_gemv(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales, const uint16_t *biases,
+                       uint16_t *y, int M, int N, int K, int group, void *stream) {
+    return gemv_impl(x, qweight, scales, biases, y, M, N, K, group, 0u, stream);
+}
+
+extern "C" int w4_gemv_ex(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales, const uint16_t *biases,
+                          uint16_t *y, int M, int N, int K, int group, unsigned flags, void *stream) {
+    return gemv_impl(x, qweight, scales, biases, y, M, N, K, group, flags, stream);
 }
 
 extern "C" size_t lm_head_workspace_bytes(int M, int N, int k) {
@@ -660,24 +991,27 @@ extern "C" size_t lm_head_workspace_bytes(int M, int N, int k) {
 }
 
 extern "C" int lm_head_argmax_topk(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
-                                   const uint16_t *biases, int M, int N, int K, int group, int k,
-                                   int32_t *idx, float *val, void *workspace, size_t workspace_bytes,
-                                   void *stream) {
-    int st = check_common(x, qweight, scales, biases, M, N, K, group);
+                                   const uint16_t *biases, int M, int N, int K, int group, int k, int32_t *idx,
+                                   float *val, void *workspace, size_t workspace_bytes, void *stream) {
+    int st = lmhead_checks(x, qweight, scales, biases, M, N, K, group, k, idx, val);
     if (st != W4A16_OK) return st;
-    if (!idx || !val) return W4_ERR_NULL;
-    if (k < 1 || k > 64 || k > N || (long long)N * k > 16777216LL) return W4_ERR_SHAPE;
-    if (!aligned16(idx) || !aligned16(val)) return W4_ERR_ALIGN;
-    const size_t need = lm_head_workspace_bytes(M, N, k);
-    if (!workspace || workspace_bytes < need) return W4_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < lm_head_workspace_bytes(M, N, k)) return W4_ERR_WORKSPACE;
     if (!aligned16(workspace)) return W4_ERR_ALIGN;
-    LmPlan pl;
-    if (!plan_lmhead(M, N, K, k, sm_count(), pl)) return W4_ERR_SHAPE;
-    if ((long long)pl.G > lm_max_blocks(N, k)) return W4_ERR_SHAPE;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    uint64_t *ws = reinterpret_cast<uint64_t *>(workspace);
-    return M <= 8 ? launch_lmhead<1>(x, qweight, scales, biases, M, N, K, k, idx, val, ws, pl, s)
-                  : launch_lmhead<2>(x, qweight, scales, biases, M, N, K, k, idx, val, ws, pl, s);
+    return lmhead_impl(x, qweight, scales, biases, M, N, K, group, k, idx, val,
+                       reinterpret_cast<uint64_t *>(workspace), workspace_bytes, 0u, stream);
+}
+
+extern "C" int lm_head_argmax_topk_ex(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                                      const uint16_t *biases, int M, int N, int K, int group, int k, int32_t *idx,
+                                      float *val, void *workspace, size_t workspace_bytes, unsigned flags,
+                                      void *stream) {
+    int st = lmhead_checks(x, qweight, scales, biases, M, N, K, group, k, idx, val);
+    if (st != W4A16_OK) return st;
+    if (flags & ~(unsigned)W4A16_OVERLAP_PREVIOUS) return W4_ERR_SHAPE;
+    if (!workspace || workspace_bytes < lm_head_workspace_bytes(M, N, k)) return W4_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return W4_ERR_ALIGN;
+    return lmhead_impl(x, qweight, scales, biases, M, N, K, group, k, idx, val,
+                       reinterpret_cast<uint64_t *>(workspace), workspace_bytes, flags, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -716,24 +1050,15 @@ void *noalloc_scratch() {
 }  // namespace
 }  // namespace w4a16
 
-extern "C" int lm_head_argmax_topk_noalloc(const uint16_t *x, const uint32_t *qweight,
-                                           const uint16_t *scales, const uint16_t *biases, int M, int N,
-                                           int K, int group, int k, int32_t *idx, float *val,
-                                           void *stream) {
-    int st = check_common(x, qweight, scales, biases, M, N, K, group);
+extern "C" int lm_head_argmax_topk_noalloc(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                                           const uint16_t *biases, int M, int N, int K, int group, int k,
+                                           int32_t *idx, float *val, void *stream) {
+    int st = lmhead_checks(x, qweight, scales, biases, M, N, K, group, k, idx, val);
     if (st != W4A16_OK) return st;
-    if (!idx || !val) return W4_ERR_NULL;
-    if (k < 1 || k > 64 || k > N || (long long)N * k > 16777216LL) return W4_ERR_SHAPE;
-    if (!aligned16(idx) || !aligned16(val)) return W4_ERR_ALIGN;
     const size_t need = lm_head_workspace_bytes(M, N, k);
     if (need == 0 || need > kNoAllocScratchBytes) return W4_ERR_WORKSPACE;
     void *scratch = noalloc_scratch();
     if (!scratch) return W4_ERR_DEVICE;
-    LmPlan pl;
-    if (!plan_lmhead(M, N, K, k, sm_count(), pl)) return W4_ERR_SHAPE;
-    if ((long long)pl.G > lm_max_blocks(N, k)) return W4_ERR_SHAPE;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    uint64_t *ws = reinterpret_cast<uint64_t *>(scratch);
-    return M <= 8 ? launch_lmhead<1>(x, qweight, scales, biases, M, N, K, k, idx, val, ws, pl, s)
-                  : launch_lmhead<2>(x, qweight, scales, biases, M, N, K, k, idx, val, ws, pl, s);
+    return lmhead_impl(x, qweight, scales, biases, M, N, K, group, k, idx, val,
+                       reinterpret_cast<uint64_t *>(scratch), kNoAllocScratchBytes, 0u, stream);
 }
