@@ -249,6 +249,238 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair variant (cta_group::2): a cluster of two CTAs computes a 256 x 256
+// tile.  Each CTA loads its own 128 rows of X and its own 128 columns of W16
+// (half the operand bytes per SM of the single-CTA tile); the leader CTA
+// issues tcgen05.mma.cta_group::2 (M=256, N=256, K=16), which reads A and B
+// from both CTAs' shared memory and accumulates rows 0-127 in the leader's
+// TMEM and rows 128-255 in the peer's.  Both CTAs' copies complete on the
+// leader's stage barrier; commits are multicast to both CTAs; both CTAs'
+// epilogue warps release an accumulator by arriving on the leader's barrier.
+// ---------------------------------------------------------------------------
+constexpr int ST2 = 6;
+constexpr int A2_TILE = 128 * BK * 2;      // 16 KB: this CTA's 128 rows
+constexpr int B2_HALF = BK * 128 * 2;      // 16 KB: this CTA's 128 columns
+constexpr int STAGE2_BYTES = A2_TILE + B2_HALF;
+constexpr size_t SMEM2_BYTES = 1024 + (size_t)ST2 * STAGE2_BYTES + 256;
+constexpr uint32_t kInstrDesc2 = (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (1u << 16) |
+                                 ((uint32_t)(256 >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                                 uint32_t leader_bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3}], [%4];" ::"r"(dst),
+        "l"(map), "r"(c0), "r"(c1), "r"(leader_bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_f16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(kInstrDesc2), "r"(accum));
+}
+
+// Arrive on the barrier at this shared-memory offset in both CTAs of the pair
+// once the preceding MMAs of this thread have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"((uint16_t)3)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm2_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+                 uint16_t *__restrict__ y, int M, int N, int K) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t bar0 = base + ST2 * STAGE2_BYTES;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (ST2 + s); };
+    auto accf_bar = [&](int a) { return bar0 + 8u * (2 * ST2 + a); };
+    auto acce_bar = [&](int a) { return bar0 + 8u * (2 * ST2 + 2 + a); };
+    const uint32_t done_bar = bar0 + 8u * (2 * ST2 + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + ST2 * STAGE2_BYTES + 8 * (2 * ST2 + 5));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    const int tiles_m = (M + 255) / 256, tiles_n = (N + BN - 1) / BN;
+    const int ntiles = tiles_m * tiles_n;
+    const int nk = (K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ST2; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(accf_bar(a), 1);
+            mbar_init(acce_bar(a), 8);  // 4 epilogue warps in each CTA of the pair
+        }
+        mbar_init(done_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tma_a) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tma_b) : "memory");
+    }
+    if (warp == 1) {
+        // One warp of each CTA of the pair allocates collectively.
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         (uint32_t)__cvta_generic_to_shared(tmem_slot)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // both CTAs' barriers exist before any remote signal
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer (both CTAs) ----------------
+            uint32_t issued_ph = 0, issued_any = 0;
+            int it = 0;
+            bool ok = true;
+            for (int t = pair; t < ntiles && ok; t += npairs) {
+                const int m0 = (t % tiles_m) * 256 + 128 * (int)rank;
+                const int n0 = (t / tiles_m) * BN + 128 * (int)rank;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % ST2;
+                    const uint32_t ph = (it / ST2) & 1;
+                    if (!mbar_wait(empty_bar(s), ph ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (rank == 0) mbar_expect_tx(full_bar(s), 2 * STAGE2_BYTES);
+                    const uint32_t lbar = map_to_rank(full_bar(s), 0);
+                    const uint32_t sa = base + s * STAGE2_BYTES;
+                    const uint32_t sb = sa + A2_TILE;
+                    tma_load_2d_pair(sa, &tma_a, kb * BK, m0, lbar);
+                    tma_load_2d_pair(sb, &tma_b, n0, kb * BK, lbar);
+                    tma_load_2d_pair(sb + B_BOX, &tma_b, n0 + 64, kb * BK, lbar);
+                    issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+                    issued_any |= 1u << s;
+                }
+            }
+            // The leader's stage barriers count both CTAs' copies: the leader
+            // drains them; the final cluster barrier holds the peer until then.
+            if (rank == 0)
+                for (int s = 0; s < ST2; ++s)
+                    if (issued_any & (1u << s)) mbar_wait(full_bar(s), (issued_ph >> s) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            if (rank == 0) {
+                // ---------------- MMA issuer (leader CTA) ----------------
+                int it = 0, tc = 0;
+                bool ok = true;
+                for (int t = pair; t < ntiles && ok; t += npairs, ++tc) {
+                    const int acc = tc & 1;
+                    const uint32_t aph = (tc >> 1) & 1;
+                    if (!mbar_wait(acce_bar(acc), aph ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t dst = tmem + acc * BN;
+                    for (int kb = 0; kb < nk; ++kb, ++it) {
+                        const int s = it % ST2;
+                        const uint32_t ph = (it / ST2) & 1;
+                        if (!mbar_wait(full_bar(s), ph)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sa = base + s * STAGE2_BYTES;
+                        const uint32_t sb = sa + A2_TILE;
+#pragma unroll
+                        for (int ks = 0; ks < BK / 16; ++ks) {
+                            const uint64_t ad = smem_desc(sa + ks * 32, 16, 1024);
+                            const uint64_t bd = smem_desc(sb + ks * 2048, B_BOX, 1024);
+                            mma_f16_pair(dst, ad, bd, (kb | ks) != 0);
+                        }
+                        mma_commit_pair(empty_bar(s));
+                    }
+                    if (!ok) break;
+                    mma_commit_pair(accf_bar(acc));
+                }
+                mma_commit_pair(done_bar);
+            }
+            mbar_wait(done_bar, 0);
+        }
+    } else {
+        // ---------------- epilogue: warps 2..5 of both CTAs ----------------
+        const int quad = warp & 3;
+        int tc = 0;
+        for (int t = pair; t < ntiles; t += npairs, ++tc) {
+            const int m0 = (t % tiles_m) * 256 + 128 * (int)rank, n0 = (t / tiles_m) * BN;
+            const int acc = tc & 1;
+            const uint32_t aph = (tc >> 1) & 1;
+            if (!mbar_wait(accf_bar(acc), aph)) break;
+            tc_fence_after();
+            const int row = m0 + quad * 32 + lane;
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + acc * BN + c * 32, r);
+                if (c == BN / 32 - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote(map_to_rank(acce_bar(acc), 0));
+                }
+                if (row < M) {
+                    uint16_t *dst = y + (size_t)row * N + n0 + c * 32;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        if (n0 + c * 32 + 8 * v < N) {
+                            uint4 o;
+                            o.x = pack_half2(r[8 * v + 0], r[8 * v + 1]);
+                            o.y = pack_half2(r[8 * v + 2], r[8 * v + 3]);
+                            o.z = pack_half2(r[8 * v + 4], r[8 * v + 5]);
+                            o.w = pack_half2(r[8 * v + 6], r[8 * v + 7]);
+                            *reinterpret_cast<uint4 *>(dst + 8 * v) = o;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+    }
+}
+
 bool make_map(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
               uint32_t box_outer) {
     return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ptr, inner, outer, inner * 2, box_inner, box_outer,
@@ -269,6 +501,8 @@ extern "C" int f16_gemm(const uint16_t *x16, const uint16_t *w16, uint16_t *y, i
     CUtensorMap ta, tb;
     if (!make_map(&ta, x16, (uint64_t)K, (uint64_t)M, BK, BM)) return W4_ERR_DEVICE;
     if (!make_map(&tb, w16, (uint64_t)N, (uint64_t)K, 64, BK)) return W4_ERR_DEVICE;
+    // The pair kernel loads 128-row A boxes (one per CTA) and the same B boxes.
+    CUtensorMap ta2 = ta, tb2 = tb;
     static bool attr_set[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -278,10 +512,38 @@ extern "C" int f16_gemm(const uint16_t *x16, const uint16_t *w16, uint16_t *y, i
             return W4_ERR_LAUNCH;
         attr_set[dev] = true;
     }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (M > BM) {
+        // CTA pairs: 256 x 256 tiles, half the operand traffic per SM.
+        static bool attr2_set[64] = {false};
+        if (dev >= 0 && dev < 64 && !attr2_set[dev]) {
+            if (cudaFuncSetAttribute(gemm2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)SMEM2_BYTES) != cudaSuccess)
+                return W4_ERR_LAUNCH;
+            attr2_set[dev] = true;
+        }
+        const int tiles = ((M + 255) / 256) * ((N + BN - 1) / BN);
+        int pairs = sm_count() / 2;
+        if (pairs > tiles) pairs = tiles;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * pairs, 1, 1);
+        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = SMEM2_BYTES;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm2_kernel, ta2, tb2, y, M, N, K);
+        return e == cudaSuccess ? W4A16_OK : W4_ERR_LAUNCH;
+    }
     const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     int grid = sm_count();
     if (grid > tiles) grid = tiles;
-    gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(ta, tb, y, M, N, K);
+    gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, y, M, N, K);
     return launch_status();
 }
 
