@@ -94,6 +94,42 @@ W4A16_API int w4_gemv_ex(const uint16_t *x, const uint32_t *qweight, const uint1
             unsigned flags, void *stream);
 
 /*
+ * w4_gemv_seq - a list of GEMVs in one persistent launch (decode projection
+ * list).
+ *   ("The inference engine - Mojo 1.0 on Metal", "Appendix: the remaining
+ *   gap": the per-token floor of some 250 small launches binds decode.)
+ *   Runs ops[0..nops) in order, each exactly as w4_gemv would (same format,
+ *   same results).  An operation with wait_prev != 0 reads activations that
+ *   earlier operations of the list write: it starts only after all of them
+ *   are complete and visible.  Weights are streamed without waiting, so they
+ *   must not be written by the operations of the list.
+ *   M       1..16 activation rows, shared by all operations.
+ *   Each operation: N >= 1, K a multiple of 256, pointers 16-byte aligned.
+ *   workspace  device buffer of w4_gemv_seq_workspace_bytes() bytes, 16-byte
+ *              aligned (a completion counter, reset by each launch).
+ *   flags   0.
+ *   Long lists run as several launches of up to 96 operations; a launch is
+ *   cooperative (one CTA per SM) and waits inside it are bounded (2 s; an
+ *   expiry is reported by w4a16_device_status).
+ * Errors: as w4_gemv, plus W4_ERR_WORKSPACE.
+ */
+typedef struct {
+    const uint16_t *x;        /* binary16 [M][K] */
+    const uint32_t *qweight;  /* [N][K/8] */
+    const uint16_t *scales;   /* binary16 [N][K/64] */
+    const uint16_t *biases;   /* binary16 [N][K/64] */
+    uint16_t *y;              /* binary16 [M][N] */
+    int N, K;
+    int wait_prev;            /* nonzero: x is written by an earlier operation */
+    int reserved;             /* set to 0 */
+} w4_gemv_op;
+
+W4A16_API size_t w4_gemv_seq_workspace_bytes(void);
+
+W4A16_API int w4_gemv_seq(const w4_gemv_op *ops, int nops, int M, void *workspace,
+            size_t workspace_bytes, unsigned flags, void *stream);
+
+/*
  * lm_head_argmax_topk - LM-head GEMV fused with token selection.
  *   ("The inference engine - Mojo 1.0 on Metal", "Crossing Mojo 1.0" and
  *   "What's inside the engine today": greedy / top-k selection on the GPU so

@@ -17,7 +17,7 @@ import os
 
 import torch
 
-__all__ = ["OVERLAP_PREVIOUS", "w4_gemv", "lm_head_argmax_topk", "lm_head_workspace_bytes", "w4_dequant_f16",
+__all__ = ["OVERLAP_PREVIOUS", "w4_gemv", "w4_gemv_seq", "GemvOp", "lm_head_argmax_topk", "lm_head_workspace_bytes", "w4_dequant_f16",
            "f16_gemm", "device_status", "W4A16Error", "LIB_PATH", "lib"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -44,6 +44,9 @@ def _load() -> ctypes.CDLL:
     L.lm_head_argmax_topk.argtypes = [P, P, P, P, I, I, I, I, I, P, P, P, Z, P]
     L.w4_gemv_ex.argtypes = [P, P, P, P, P, I, I, I, I, ctypes.c_uint, P]
     L.lm_head_argmax_topk_ex.argtypes = [P, P, P, P, I, I, I, I, I, P, P, P, Z, ctypes.c_uint, P]
+    L.w4_gemv_seq.argtypes = [P, I, I, P, Z, ctypes.c_uint, P]
+    L.w4_gemv_seq_workspace_bytes.argtypes = []
+    L.w4_gemv_seq_workspace_bytes.restype = Z
     L.lm_head_workspace_bytes.argtypes = [I, I, I]
     L.lm_head_workspace_bytes.restype = Z
     L.w4_dequant_f16.argtypes = [P, P, P, P, I, I, I, P]
@@ -51,8 +54,8 @@ def _load() -> ctypes.CDLL:
     L.w4a16_status_string.argtypes = [I]
     L.w4a16_status_string.restype = ctypes.c_char_p
     L.w4a16_device_status.argtypes = []
-    for f in ("w4_gemv", "w4_gemv_ex", "lm_head_argmax_topk", "lm_head_argmax_topk_ex", "w4_dequant_f16",
-              "f16_gemm", "w4a16_device_status"):
+    for f in ("w4_gemv", "w4_gemv_ex", "w4_gemv_seq", "lm_head_argmax_topk", "lm_head_argmax_topk_ex",
+              "w4_dequant_f16", "f16_gemm", "w4a16_device_status"):
         getattr(L, f).restype = I
     return L
 
@@ -108,6 +111,41 @@ def w4_gemv(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, biases
                                      _dev(scales, "scales", _H), _dev(biases, "biases", _H),
                                      _dev(y, "y", _H), M, N, K, group, flags, _stream(stream)))
     return y
+
+
+class GemvOp(ctypes.Structure):
+    """One operation of w4_gemv_seq (mirror of the C struct w4_gemv_op)."""
+    _fields_ = [("x", ctypes.c_void_p), ("qweight", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("biases", ctypes.c_void_p), ("y", ctypes.c_void_p), ("N", ctypes.c_int), ("K", ctypes.c_int),
+                ("wait_prev", ctypes.c_int), ("reserved", ctypes.c_int)]
+
+
+def w4_gemv_seq(ops, workspace: torch.Tensor | None = None, group: int = 64, stream=None):
+    """Run a list of GEMVs in one persistent launch.
+
+    ops: sequence of (x, qweight, scales, biases, y, wait_prev) with torch
+    tensors; wait_prev = True when x is written by an earlier operation of the
+    list.  All x share the same number of rows M.  Returns the list of y."""
+    if group != 64:
+        raise ValueError("group must be 64")
+    arr = (GemvOp * len(ops))()
+    M = None
+    for i, (x, qw, s, b, y, wait) in enumerate(ops):
+        N, K = _weight_dims(qw, s, b, group)
+        x2 = x.reshape(-1, K) if x.dim() != 2 else x
+        if M is None:
+            M = x2.shape[0]
+        elif x2.shape[0] != M:
+            raise ValueError("all operations must have the same number of activation rows")
+        arr[i] = GemvOp(_dev(x2, "x", _H), _dev(qw, "qweight", _QW), _dev(s, "scales", _H),
+                        _dev(b, "biases", _H), _dev(y, "y", _H), N, K, 1 if wait else 0, 0)
+    if workspace is None:
+        workspace = torch.empty(int(lib.w4_gemv_seq_workspace_bytes()), dtype=torch.uint8,
+                                device=ops[0][0].device)
+    _check("w4_gemv_seq", lib.w4_gemv_seq(ctypes.cast(arr, ctypes.c_void_p), len(ops), M,
+                                          _dev(workspace, "workspace", (torch.uint8,)), workspace.numel(),
+                                          0, _stream(stream)))
+    return [op[4] for op in ops]
 
 
 def lm_head_workspace_bytes(M: int, N: int, k: int) -> int:

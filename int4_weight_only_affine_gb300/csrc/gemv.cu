@@ -120,7 +120,7 @@ __device__ __forceinline__ uint32_t sixteenth(uint32_t h2) {
 }
 
 __device__ void stage_activations(const uint16_t *__restrict__ x, int M, int K, int g0, int ngl,
-                                  uint32_t *xf, float *xsum, int tid, int nthreads) {
+                                  uint32_t *xf, float *xsum, int tid, int nthreads, bool coherent = false) {
     const int items = ngl * M * 4;
     for (int base = 0; base < items; base += nthreads) {
         const int it = base + tid;
@@ -131,7 +131,10 @@ __device__ void stage_activations(const uint16_t *__restrict__ x, int M, int K, 
             const int gl = (it >> 2) / M;
             const uint4 *src =
                 reinterpret_cast<const uint4 *>(x + (size_t)c * K + (size_t)(g0 + gl) * kGroup + 16 * t);
-            const uint4 lo = __ldg(src), hi = __ldg(src + 1);
+            // Activations written earlier in the same kernel must bypass the
+            // non-coherent read-only path.
+            const uint4 lo = coherent ? __ldcg(src) : __ldg(src);
+            const uint4 hi = coherent ? __ldcg(src + 1) : __ldg(src + 1);
             uint4 f0, f1;
             f0.x = __byte_perm(lo.x, lo.z, 0x5410);  // (x0, x4)
             f0.y = __byte_perm(hi.x, hi.z, 0x5410);  // (x8, x12)
@@ -632,6 +635,218 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Projection-list kernel: a sequence of GEMVs in one persistent launch.
+//
+// "The inference engine - Mojo 1.0 on Metal", "Appendix: the remaining gap":
+// the per-token floor of some 250 small launches is the binding constraint of
+// decode.  Here one cooperative, persistent launch (one CTA per SM) runs a
+// whole list of GEMVs.  The producer warp streams the weights of operation
+// after operation into the ring without ever waiting for results (weights
+// are constants), so HBM stays busy across operation boundaries; the 16
+// consumer warps wait, where an operation's activations depend on earlier
+// outputs, until every CTA has published the earlier operations (a counter
+// in the caller's workspace, bounded spin), then stage the activations with
+// coherent loads and compute as the streaming kernel does.  Each operation's
+// tiles are split over the CTAs; outputs are combined in fixed order.
+// ---------------------------------------------------------------------------
+constexpr int kSeqMaxOps = 96;  // operations per launch (tensor maps travel as kernel parameters)
+constexpr int kSeqWarps = 16;
+constexpr int kSeqConsumers = kSeqWarps * 32;
+constexpr int kSeqThreads = kSeqConsumers + 32;
+
+struct SeqOp {
+    const uint16_t *x, *sc, *bi;
+    uint16_t *y;
+    int N, K, wait_prev, cq;
+};
+
+struct SeqParams {
+    CUtensorMap maps[kSeqMaxOps];  // 3-D code maps, one per operation
+    SeqOp ops[kSeqMaxOps];
+    unsigned *done;                // (operation, CTA) completions so far
+    int nops, M, stages;
+    uint32_t stage_bytes, w_bytes;
+    uint32_t off_xf, off_xsum, off_red, off_bar;
+};
+
+__device__ __forceinline__ void seq_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSeqConsumers) : "memory"); }
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_constant__ SeqParams P) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sb = smem_raw + (base - raw);
+    pdl_launch_dependents();
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int M = P.M, S = P.stages, G = gridDim.x, blk = blockIdx.x;
+    const int out16 = kTileRows * M;
+    uint32_t *xf = reinterpret_cast<uint32_t *>(sb + P.off_xf);
+    float *xsum = reinterpret_cast<float *>(sb + P.off_xsum);
+    float *red = reinterpret_cast<float *>(sb + P.off_red);
+    const uint32_t bar0 = base + P.off_bar;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sb + P.off_bar + 16 * S);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), kSeqWarps);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == kSeqWarps) {
+        // ---------------- producer: streams every operation's weights ----------------
+        if (lane == 0) {
+            uint32_t issued_ph = 0, issued_any = 0;
+            int it = 0;
+            bool ok = true;
+            for (int op = 0; op < P.nops && ok; ++op) {
+                const SeqOp &o = P.ops[op];
+                const int T = (o.N + kTileRows - 1) / kTileRows;
+                const int t0 = (int)((long long)blk * T / G), t1 = (int)((long long)(blk + 1) * T / G);
+                const int ng = o.K / kGroup, nch = (ng + kChunkGroups - 1) / kChunkGroups;
+                for (int t = t0; t < t1 && ok; ++t) {
+                    const bool tail = (t + 1) * kTileRows > o.N;
+                    const uint32_t sbytes = tail ? 0u : 32u * ng;
+                    for (int ch = 0; ch < nch; ++ch, ++it) {
+                        const int s = it % S;
+                        const uint32_t ph = (it / S) & 1;
+                        if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t st = base + s * P.stage_bytes;
+                        mbar_expect_tx(full_bar(s), o.cq * kBoxBytes + 2 * sbytes);
+                        tma_load_3d(st, &P.maps[op], 0, t * kTileRows, ch * (kChunkGroups / kBoxGroups), full_bar(s));
+                        if (!tail) {
+                            bulk_load(st + P.w_bytes, o.sc + (size_t)t * kTileRows * ng, sbytes, full_bar(s));
+                            bulk_load(st + P.w_bytes + sbytes, o.bi + (size_t)t * kTileRows * ng, sbytes, full_bar(s));
+                        }
+                        issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+                        issued_any |= 1u << s;
+                    }
+                }
+            }
+            for (int s = 0; s < S; ++s)
+                if (issued_any & (1u << s)) mbar_wait(full_bar(s), (issued_ph >> s) & 1);
+        }
+    } else {
+        // ---------------- consumers ----------------
+        const int lg = lane >> 2, lt = lane & 3;
+        // Warp w takes groups w and w+16 of a chunk: a fixed 16-byte chunk of
+        // a box row (swizzled offset) and a fixed stride of 4 boxes.
+        const int wsw = ((((warp & 3) << 1) | (lt >> 1)) ^ (lg & 7)) << 4;
+        const int lane_w = lg * 128 + ((lt & 1) << 3) + (warp >> 2) * kBoxBytes + wsw;
+        pdl_wait();
+        int it = 0;
+        for (int op = 0; op < P.nops; ++op) {
+            const SeqOp &o = P.ops[op];
+            const int N = o.N, ng = o.K / kGroup, nch = (ng + kChunkGroups - 1) / kChunkGroups;
+            const int T = (N + kTileRows - 1) / kTileRows;
+            const int t0 = (int)((long long)blk * T / G), t1 = (int)((long long)(blk + 1) * T / G);
+            const int ntl = t1 - t0;
+            if (o.wait_prev && op > 0 && tid == 0) {
+                // Every CTA has published operations 0..op-1.
+                const unsigned target = (unsigned)op * (unsigned)G;
+                const uint64_t t_start = global_ns();
+                while (ld_acquire_u32(P.done) < target) {
+                    if (*abort_flag) break;
+                    if (global_ns() - t_start > kWaitNs) {
+                        atomicExch(&g_wait_expired, 1);
+                        *abort_flag = 1;
+                        break;
+                    }
+                }
+            }
+            seq_sync();  // also ends every use of the previous operation's activations
+            stage_activations(o.x, M, o.K, 0, ng, xf, xsum, tid, kSeqConsumers, true);
+            seq_sync();
+            for (int tl = 0; tl < ntl; ++tl) {
+                const int row0 = (t0 + tl) * kTileRows;
+                const bool tail = row0 + kTileRows > N;
+                Acc<NT> acc;
+                acc.zero();
+                for (int ch = 0; ch < nch; ++ch, ++it) {
+                    const int s = it % S;
+                    const uint32_t ph = (it / S) & 1;
+                    const bool ok = mbar_wait(full_bar(s), ph, abort_flag);
+                    uint8_t *st = sb + (size_t)s * P.stage_bytes;
+                    uint16_t *sp = reinterpret_cast<uint16_t *>(st + P.w_bytes);
+                    if (tail) {
+                        for (int i = tid; i < 2 * kTileRows * ng; i += kSeqConsumers) {
+                            const int arr = i / (kTileRows * ng), r = (i / ng) % kTileRows, gi = i % ng;
+                            const uint16_t *src = arr ? o.bi : o.sc;
+                            sp[i] = src[(size_t)min(row0 + r, N - 1) * ng + gi];
+                        }
+                        seq_sync();
+                    }
+                    if (ok) {
+                        const int cg0 = ch * kChunkGroups;
+                        const int len = min(kChunkGroups, ng - cg0);
+                        const int cnt = len > warp ? (len - warp + kSeqWarps - 1) / kSeqWarps : 0;
+                        const uint8_t *wp = st + lane_w;
+                        const uint16_t *sa = sp + lg * ng + cg0 + warp;
+                        const uint16_t *sbb = sa + 8 * ng;
+                        const uint16_t *ba = sa + kTileRows * ng;
+                        const uint16_t *bb = sbb + kTileRows * ng;
+#pragma unroll
+                        for (int j = 0; j < kChunkGroups / kSeqWarps; ++j) {
+                            if (j < cnt) {
+                                const uint2 wa = *reinterpret_cast<const uint2 *>(wp + j * 4 * kBoxBytes);
+                                const uint2 wb = *reinterpret_cast<const uint2 *>(wp + j * 4 * kBoxBytes + 8 * 128);
+                                group_mma<NT>(acc, wa, wb, h2f(sa[16 * j]), h2f(sbb[16 * j]), h2f(ba[16 * j]),
+                                              h2f(bb[16 * j]), xf, xsum, cg0 + warp + 16 * j, M, lg, lt);
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty_bar(s));
+                }
+                float *mine = red + ((size_t)tl * kSeqWarps + warp) * out16;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int row = lg + ((i & 2) ? 8 : 0);
+                        const int col = nt * 8 + 2 * lt + (i & 1);
+                        if (col < M) mine[row * M + col] = acc.value(nt, i);
+                    }
+            }
+            seq_sync();
+            for (int i = tid; i < ntl * out16; i += kSeqConsumers) {
+                const int tl = i / out16, e = i % out16;
+                const float *grp = red + (size_t)tl * kSeqWarps * out16;
+                float v = 0.f;
+#pragma unroll
+                for (int w = 0; w < kSeqWarps; ++w) v += grp[w * out16 + e];
+                const int row = e / M, col = e % M, r = (t0 + tl) * kTileRows + row;
+                if (r < N) o.y[(size_t)col * N + r] = __half_as_ushort(__float2half_rn(v));
+            }
+            // Publish: the CTA barrier orders every thread's stores before the
+            // signalling thread's GPU-scope fence and counter increment.
+            seq_sync();
+            if (tid == 0) {
+                __threadfence();
+                atomicAdd(P.done, 1u);
+            }
+        }
+    }
+    __syncthreads();
+}
+
 const void *stream_kernel_ptr(int M, bool lmhead) {
     if (lmhead) return M <= 8 ? (const void *)stream_kernel<1, true> : (const void *)stream_kernel<2, true>;
     return M <= 8 ? (const void *)stream_kernel<1, false> : (const void *)stream_kernel<2, false>;
@@ -969,6 +1184,79 @@ int lmhead_checks(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, con
     return W4A16_OK;
 }
 
+// Shared-memory layout of one sequence launch; false if it cannot fit.
+bool plan_seq(SeqParams &P, size_t &smem, int ng_max, int ntl_max) {
+    const int M = P.M;
+    P.w_bytes = (uint32_t)(kChunkGroups / kBoxGroups) * kBoxBytes;
+    P.stage_bytes = (uint32_t)align_up((size_t)P.w_bytes + 64u * ng_max, 1024);
+    const size_t fixed = align_up((size_t)ng_max * M * 128, 16) + align_up((size_t)ng_max * M * 4, 16) +
+                         align_up((size_t)ntl_max * kSeqWarps * kTileRows * M * 4, 16) + 16 * kMaxStages + 16 + 1024;
+    if (fixed + 2 * (size_t)P.stage_bytes > (size_t)kMaxSmem) return false;
+    P.stages = (int)min((size_t)kMaxStages, ((size_t)kMaxSmem - fixed) / P.stage_bytes);
+    size_t off = (size_t)P.stages * P.stage_bytes;
+    P.off_xf = (uint32_t)off;
+    off = align_up(off + (size_t)ng_max * M * 128, 16);
+    P.off_xsum = (uint32_t)off;
+    off = align_up(off + (size_t)ng_max * M * 4, 16);
+    P.off_red = (uint32_t)off;
+    off = align_up(off + (size_t)ntl_max * kSeqWarps * kTileRows * M * 4, 16);
+    P.off_bar = (uint32_t)off;
+    off += 16 * P.stages + 16;
+    smem = off + 1024;
+    return smem <= (size_t)kMaxSmem;
+}
+
+int seq_launch(const w4_gemv_op *ops, int nops, int M, unsigned *done, cudaStream_t st) {
+    static SeqParams P;  // large: kept off the stack (calls are host-serialised per process)
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    const int G = sm_count();
+    int ng_max = 1, ntl_max = 1;
+    for (int i = 0; i < nops; ++i) {
+        const w4_gemv_op &o = ops[i];
+        SeqOp &d = P.ops[i];
+        d.x = o.x;
+        d.sc = o.scales;
+        d.bi = o.biases;
+        d.y = o.y;
+        d.N = o.N;
+        d.K = o.K;
+        d.wait_prev = o.wait_prev;
+        const int nq = o.K / 256;
+        d.cq = min(kChunkGroups / kBoxGroups, nq);
+        ng_max = max(ng_max, o.K / kGroup);
+        ntl_max = max(ntl_max, ((o.N + kTileRows - 1) / kTileRows + G - 1) / G);
+        const uint64_t KW = (uint64_t)o.K / 8;
+        if (!make_map_3d(&P.maps[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, o.qweight, 32, (uint64_t)o.N, (uint64_t)nq,
+                         KW * 4, 128, 32, kTileRows, (uint32_t)d.cq, CU_TENSOR_MAP_SWIZZLE_128B))
+            return W4_ERR_DEVICE;
+    }
+    P.nops = nops;
+    P.M = M;
+    P.done = done;
+    size_t smem = 0;
+    if (!plan_seq(P, smem, ng_max, ntl_max)) return W4_ERR_SHAPE;
+    const void *kern = M <= 8 ? (const void *)seq_kernel<1> : (const void *)seq_kernel<2>;
+    if (!ensure_smem(kern, smem)) return W4_ERR_LAUNCH;
+    if (cudaMemsetAsync(done, 0, sizeof(unsigned), st) != cudaSuccess) return W4_ERR_LAUNCH;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G, 1, 1);
+    cfg.blockDim = dim3(kSeqThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: the waits cannot starve
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = M <= 8 ? cudaLaunchKernelEx(&cfg, seq_kernel<1>, P) : cudaLaunchKernelEx(&cfg, seq_kernel<2>, P);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return W4_ERR_LAUNCH;
+    }
+    return W4A16_OK;
+}
+
 }  // namespace
 }  // namespace w4a16
 
@@ -1012,6 +1300,31 @@ extern "C" int lm_head_argmax_topk_ex(const uint16_t *x, const uint32_t *qweight
     if (!aligned16(workspace)) return W4_ERR_ALIGN;
     return lmhead_impl(x, qweight, scales, biases, M, N, K, group, k, idx, val,
                        reinterpret_cast<uint64_t *>(workspace), workspace_bytes, flags, stream);
+}
+
+extern "C" size_t w4_gemv_seq_workspace_bytes(void) { return 16; }
+
+extern "C" int w4_gemv_seq(const w4_gemv_op *ops, int nops, int M, void *workspace, size_t workspace_bytes,
+                           unsigned flags, void *stream) {
+    if (!ops || !workspace) return ops ? W4_ERR_WORKSPACE : W4_ERR_NULL;
+    if (workspace_bytes < w4_gemv_seq_workspace_bytes()) return W4_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return W4_ERR_ALIGN;
+    if (nops < 1 || M < 1 || M > 16 || flags != 0) return W4_ERR_SHAPE;
+    for (int i = 0; i < nops; ++i) {
+        const w4_gemv_op &o = ops[i];
+        int st = check_common(o.x, o.qweight, o.scales, o.biases, M, o.N, o.K, kGroup);
+        if (st != W4A16_OK) return st;
+        if (!o.y) return W4_ERR_NULL;
+        if (!aligned16(o.y)) return W4_ERR_ALIGN;
+        if (o.K % 256 != 0) return W4_ERR_SHAPE;  // whole 128-byte quads per row
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (int first = 0; first < nops; first += kSeqMaxOps) {
+        const int n = min(kSeqMaxOps, nops - first);
+        const int st = seq_launch(ops + first, n, M, reinterpret_cast<unsigned *>(workspace), s);
+        if (st != W4A16_OK) return st;
+    }
+    return W4A16_OK;
 }
 
 // ---------------------------------------------------------------------------
