@@ -103,6 +103,12 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
     return false;
 }
 
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA / bulk copy) accesses of the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
 }

@@ -173,11 +173,12 @@ struct Acc {
 };
 
 // One group (64 k) of the warp's 16-row tile: 4 MMAs per activation tile.
-// wa/wb: words 2t, 2t+1 of rows g and g+8; s*/b*: their scales and biases.
-template <int NT>
+// wa/wb: words 2t, 2t+1 of rows g and g+8; s*/b*: their scales and biases;
+// xg: the group's staged activation fragments, xs: its activation sums.
+// M1: a single activation row (only column 0 of the MMA result is used).
+template <int NT, bool M1>
 __device__ __forceinline__ void group_mma(Acc<NT> &acc, uint2 wa, uint2 wb, float sa, float sb, float ba,
-                                          float bb, const uint32_t *xf, const float *xsum, int gl, int M, int lg,
-                                          int lt) {
+                                          float bb, const uint4 *xg, const float *xs, int M, int lg, int lt) {
     // Codes j and j+4 of a word as a half pair: even j from (w >> 2j) & 0x000F000F
     // (q * 2^-24), odd j from (w >> 2(j-1)) & 0x00F000F0 (q * 2^-20, matched by
     // activations stored / 16): one shift per word.
@@ -203,26 +204,93 @@ __device__ __forceinline__ void group_mma(Acc<NT> &acc, uint2 wa, uint2 wb, floa
     for (int nt = 0; nt < NT; ++nt) {
         const int c = nt * 8 + lg;
         uint4 f0 = make_uint4(0, 0, 0, 0), f1 = make_uint4(0, 0, 0, 0);
-        if (c < M) {
-            f0 = reinterpret_cast<const uint4 *>(xf)[((gl * 2 + 0) * M + c) * 4 + lt];
-            f1 = reinterpret_cast<const uint4 *>(xf)[((gl * 2 + 1) * M + c) * 4 + lt];
+        if (M1 ? lg == 0 : c < M) {
+            f0 = xg[(0 * M + c) * 4 + lt];
+            f1 = xg[(1 * M + c) * 4 + lt];
         }
         float d[4] = {0.f, 0.f, 0.f, 0.f};
         mma_16816(d, a0[0], a1[0], a2[0], a3[0], f0.x, f0.y);
         mma_16816(d, a0[1], a1[1], a2[1], a3[1], f0.z, f0.w);
         mma_16816(d, a0[2], a1[2], a2[2], a3[2], f1.x, f1.y);
         mma_16816(d, a0[3], a1[3], a2[3], a3[3], f1.z, f1.w);
-        const int c0 = nt * 8 + 2 * lt;
-        const float X0 = (c0 < M) ? xsum[gl * M + c0] : 0.f;
-        const float X1 = (c0 + 1 < M) ? xsum[gl * M + c0 + 1] : 0.f;
-        acc.s[nt][0] = fmaf(sa, d[0], acc.s[nt][0]);
-        acc.s[nt][1] = fmaf(sa, d[1], acc.s[nt][1]);
-        acc.s[nt][2] = fmaf(sb, d[2], acc.s[nt][2]);
-        acc.s[nt][3] = fmaf(sb, d[3], acc.s[nt][3]);
-        acc.b[nt][0] = fmaf(ba, X0, acc.b[nt][0]);
-        acc.b[nt][1] = fmaf(ba, X1, acc.b[nt][1]);
-        acc.b[nt][2] = fmaf(bb, X0, acc.b[nt][2]);
-        acc.b[nt][3] = fmaf(bb, X1, acc.b[nt][3]);
+        if (M1) {
+            // Column 0 lives in d[0] (row g) and d[2] (row g+8) of lanes t = 0.
+            const float X0 = xs[0];
+            acc.s[nt][0] = fmaf(sa, d[0], acc.s[nt][0]);
+            acc.s[nt][2] = fmaf(sb, d[2], acc.s[nt][2]);
+            acc.b[nt][0] = fmaf(ba, X0, acc.b[nt][0]);
+            acc.b[nt][2] = fmaf(bb, X0, acc.b[nt][2]);
+        } else {
+            const int c0 = nt * 8 + 2 * lt;
+            const float X0 = (c0 < M) ? xs[c0] : 0.f;
+            const float X1 = (c0 + 1 < M) ? xs[c0 + 1] : 0.f;
+            acc.s[nt][0] = fmaf(sa, d[0], acc.s[nt][0]);
+            acc.s[nt][1] = fmaf(sa, d[1], acc.s[nt][1]);
+            acc.s[nt][2] = fmaf(sb, d[2], acc.s[nt][2]);
+            acc.s[nt][3] = fmaf(sb, d[3], acc.s[nt][3]);
+            acc.b[nt][0] = fmaf(ba, X0, acc.b[nt][0]);
+            acc.b[nt][1] = fmaf(ba, X1, acc.b[nt][1]);
+            acc.b[nt][2] = fmaf(bb, X0, acc.b[nt][2]);
+            acc.b[nt][3] = fmaf(bb, X1, acc.b[nt][3]);
+        }
+    }
+}
+
+// Shared-memory byte offsets, within a stage, of the words a lane reads for
+// group j (0..3) of box `box`: row g, 16-byte chunk 2j + t/2 under the
+// 128-byte swizzle (chunk index XOR row % 8), word pair t % 2.  Row g+8 is
+// 1024 bytes further with the same swizzle phase.
+__device__ __forceinline__ void box_offsets(int (&off)[4], int box, int lg, int lt) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        off[j] = box * kBoxBytes + lg * 128 + ((((2 * j) | (lt >> 1)) ^ (lg & 7)) << 4) + ((lt & 1) << 3);
+}
+
+__device__ __forceinline__ void unpack4h(uint2 v, float (&f)[4]) {
+    const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
+    const float2 hi = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
+    f[0] = lo.x;
+    f[1] = lo.y;
+    f[2] = hi.x;
+    f[3] = hi.y;
+}
+
+// The warp's box of a stage: n (1..4) consecutive groups of a 16-row tile.
+// st: the stage; sp: the tile's scales [16][ng] (biases follow);
+// g: the box's first group (index into a scale row); xg: staged activations
+// of that group; xs: its activation sums.  FULL: n == 4 and ng % 4 == 0, so
+// a lane's four scales of a row are one aligned 8-byte word.
+template <int NT, bool M1, bool FULL>
+__device__ __forceinline__ void box_mma(Acc<NT> &acc, const uint8_t *st, const int (&off)[4], const uint16_t *sp,
+                                        int ng, int g, int n, const uint4 *xg, const float *xs, int M, int lg,
+                                        int lt) {
+    const uint16_t *sa = sp + lg * ng + g;  // scales of row g; row g+8 is 8 rows on
+    const uint16_t *ba = sa + kTileRows * ng;
+    float fsa[4], fsb[4], fba[4], fbb[4];
+    if (FULL) {
+        unpack4h(*reinterpret_cast<const uint2 *>(sa), fsa);
+        unpack4h(*reinterpret_cast<const uint2 *>(sa + 8 * ng), fsb);
+        unpack4h(*reinterpret_cast<const uint2 *>(ba), fba);
+        unpack4h(*reinterpret_cast<const uint2 *>(ba + 8 * ng), fbb);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int jj = j < n ? j : 0;
+            fsa[j] = h2f(sa[jj]);
+            fsb[j] = h2f(sa[8 * ng + jj]);
+            fba[j] = h2f(ba[jj]);
+            fbb[j] = h2f(ba[8 * ng + jj]);
+        }
+    }
+    const int xstep = 2 * M * 4;  // uint4 words of staged activations per group
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (FULL || j < n) {
+            const uint2 wa = *reinterpret_cast<const uint2 *>(st + off[j]);
+            const uint2 wb = *reinterpret_cast<const uint2 *>(st + off[j] + 8 * 128);
+            group_mma<NT, M1>(acc, wa, wb, fsa[j], fsb[j], fba[j], fbb[j], xg + j * (M1 ? 8 : xstep),
+                              xs + j * (M1 ? 1 : M), M, lg, lt);
+        }
     }
 }
 
@@ -386,7 +454,7 @@ struct StreamArgs {
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
 
-template <int NT, bool LMHEAD>
+template <int NT, bool LMHEAD, bool M1>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
     stream_kernel(const __grid_constant__ CUtensorMap tm3, const __grid_constant__ CUtensorMap tm2,
                   const StreamArgs a) {
@@ -477,28 +545,25 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
     } else {
         // ---------------- consumers ----------------
         const int lg = lane >> 2, lt = lane & 3;
-        // Groups of a chunk go to the warps round-robin (warp w takes w, w+8,
-        // w+16, w+24), so a warp always reads the same 16-byte chunk of a box
-        // row: its swizzled offset and the stride between its groups are fixed.
-        const int wsw = ((((warp & 3) << 1) | (lt >> 1)) ^ (lg & 7)) << 4;
-        const int lane_w = lg * 128 + ((lt & 1) << 3) + (warp >> 2) * kBoxBytes + wsw;
-        const int xstride = 8 * 2 * M * 4;  // uint4 words of staged activations per 8 groups
+        // Warp w takes box w of every stage: groups 4w .. 4w+3 of the chunk.
+        int off[4];
+        box_offsets(off, warp, lg, lt);
+        const bool vec = (ng & 3) == 0;
         pdl_wait();
         stage_activations(a.x, M, a.K, gs0, ngl, xf, xsum, tid, kConsumers);
         consumer_sync();
-        int it = 0;
+        int s = 0;
+        uint32_t ph = 0;
         for (int tl = 0; tl < ntl; ++tl) {
             const int t = t0 + tl;
             const int row0 = t * kTileRows;
             const bool tail = row0 + kTileRows > N;
             Acc<NT> acc;
             acc.zero();
-            for (int ch = 0; ch < nch; ++ch, ++it) {
-                const int s = it % S;
-                const uint32_t ph = (it / S) & 1;
+            for (int ch = 0; ch < nch; ++ch) {
                 const bool ok = mbar_wait(full_bar(s), ph, abort_flag);
-                uint8_t *st = sb + (size_t)s * a.stage_bytes;
-                uint16_t *sp = reinterpret_cast<uint16_t *>(st + a.w_bytes);  // [16][ng] scales, then biases
+                const uint8_t *st = sb + (size_t)s * a.stage_bytes;
+                uint16_t *sp = reinterpret_cast<uint16_t *>(sb + (size_t)s * a.stage_bytes + a.w_bytes);
                 if (tail) {
                     // The producer copies no scales for the ragged last tile (its rows
                     // end inside the arrays); fill them here, rows past N repeated.
@@ -507,30 +572,25 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
                         const uint16_t *src = arr ? a.bi : a.sc;
                         sp[i] = src[(size_t)min(row0 + r, N - 1) * ng + gi];
                     }
+                    fence_proxy_async_smem();  // a later bulk copy reuses these bytes
                     consumer_sync();
                 }
                 if (ok) {
-                    const int cg0 = gs0 + ch * kChunkGroups;
-                    const int len = min(kChunkGroups, gs1 - cg0);
-                    const int cnt = len > warp ? (len - warp + kConsumerWarps - 1) / kConsumerWarps : 0;
-                    const uint8_t *wp = st + lane_w;
-                    const uint16_t *sa = sp + lg * ng + cg0 + warp;
-                    const uint16_t *sbb = sa + 8 * ng;
-                    const uint16_t *ba = sa + kTileRows * ng;
-                    const uint16_t *bb = sbb + kTileRows * ng;
-                    const int gl0 = cg0 - gs0 + warp;
-#pragma unroll
-                    for (int j = 0; j < kChunkGroups / kConsumerWarps; ++j) {
-                        if (j < cnt) {
-                            const uint2 wa = *reinterpret_cast<const uint2 *>(wp + j * 2 * kBoxBytes);
-                            const uint2 wb = *reinterpret_cast<const uint2 *>(wp + j * 2 * kBoxBytes + 8 * 128);
-                            group_mma<NT>(acc, wa, wb, h2f(sa[8 * j]), h2f(sbb[8 * j]), h2f(ba[8 * j]), h2f(bb[8 * j]),
-                                          xf, xsum, gl0 + 8 * j, M, lg, lt);
-                        }
-                    }
+                    const int g = gs0 + ch * kChunkGroups + kBoxGroups * warp;
+                    const int n = min(kBoxGroups, gs1 - g);
+                    const int gl = g - gs0;
+                    const uint4 *xg = reinterpret_cast<const uint4 *>(xf) + (size_t)gl * 2 * M * 4;
+                    if (n == kBoxGroups && vec)
+                        box_mma<NT, M1, true>(acc, st, off, sp, ng, g, n, xg, xsum + gl * M, M, lg, lt);
+                    else if (n > 0)
+                        box_mma<NT, M1, false>(acc, st, off, sp, ng, g, n, xg, xsum + gl * M, M, lg, lt);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_bar(s));
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1;
+                }
             }
             if (a.defer) {
                 // Keep this warp's partial; all tiles are combined once at the end.
@@ -587,7 +647,6 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
                 }
             }
         }
-        (void)xstride;
     }
     __syncthreads();
 
@@ -652,6 +711,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
 // ---------------------------------------------------------------------------
 constexpr int kSeqMaxOps = 96;  // operations per launch (tensor maps travel as kernel parameters)
 constexpr int kSeqWarps = 16;
+constexpr int kSeqTeamWarps = 8;  // consumer warps per tile team
 constexpr int kSeqConsumers = kSeqWarps * 32;
 constexpr int kSeqThreads = kSeqConsumers + 32;
 
@@ -671,6 +731,10 @@ struct SeqParams {
 };
 
 __device__ __forceinline__ void seq_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSeqConsumers) : "memory"); }
+// Named barrier of one 8-warp team (ids 2 and 3).
+__device__ __forceinline__ void team_sync(int team) {
+    asm volatile("bar.sync %0, %1;" ::"r"(2 + team), "n"(kSeqTeamWarps * 32) : "memory");
+}
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
     unsigned v;
@@ -678,7 +742,7 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
     return v;
 }
 
-template <int NT>
+template <int NT, bool M1>
 __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_constant__ SeqParams P) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
@@ -700,7 +764,7 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), kSeqWarps);
+            mbar_init(empty_bar(s), kSeqTeamWarps);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -744,14 +808,14 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
                 if (issued_any & (1u << s)) mbar_wait(full_bar(s), (issued_ph >> s) & 1);
         }
     } else {
-        // ---------------- consumers ----------------
+        // ---------------- consumers: two teams of 8 warps, alternate tiles ----------------
         const int lg = lane >> 2, lt = lane & 3;
-        // Warp w takes groups w and w+16 of a chunk: a fixed 16-byte chunk of
-        // a box row (swizzled offset) and a fixed stride of 4 boxes.
-        const int wsw = ((((warp & 3) << 1) | (lt >> 1)) ^ (lg & 7)) << 4;
-        const int lane_w = lg * 128 + ((lt & 1) << 3) + (warp >> 2) * kBoxBytes + wsw;
+        const int team = warp / kSeqTeamWarps, tw = warp % kSeqTeamWarps;
+        // Warp tw of a team takes box tw of every stage (groups 4tw .. 4tw+3).
+        int off[4];
+        box_offsets(off, tw, lg, lt);
         pdl_wait();
-        int it = 0;
+        int base_it = 0;  // stages consumed by all earlier operations
         for (int op = 0; op < P.nops; ++op) {
             const SeqOp &o = P.ops[op];
             const int N = o.N, ng = o.K / kGroup, nch = (ng + kChunkGroups - 1) / kChunkGroups;
@@ -774,48 +838,48 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
             seq_sync();  // also ends every use of the previous operation's activations
             stage_activations(o.x, M, o.K, 0, ng, xf, xsum, tid, kSeqConsumers, true);
             seq_sync();
-            for (int tl = 0; tl < ntl; ++tl) {
+            for (int tl = team; tl < ntl; tl += 2) {
                 const int row0 = (t0 + tl) * kTileRows;
                 const bool tail = row0 + kTileRows > N;
                 Acc<NT> acc;
                 acc.zero();
-                for (int ch = 0; ch < nch; ++ch, ++it) {
-                    const int s = it % S;
-                    const uint32_t ph = (it / S) & 1;
+                // Stage index of this tile's first chunk: every earlier operation's
+                // stages, then nch per earlier tile of this operation.
+                const int it0 = base_it + tl * nch;
+                int s = it0 % S;
+                uint32_t ph = (it0 / S) & 1;
+                for (int ch = 0; ch < nch; ++ch) {
                     const bool ok = mbar_wait(full_bar(s), ph, abort_flag);
-                    uint8_t *st = sb + (size_t)s * P.stage_bytes;
-                    uint16_t *sp = reinterpret_cast<uint16_t *>(st + P.w_bytes);
+                    const uint8_t *st = sb + (size_t)s * P.stage_bytes;
+                    uint16_t *sp = reinterpret_cast<uint16_t *>(sb + (size_t)s * P.stage_bytes + P.w_bytes);
                     if (tail) {
-                        for (int i = tid; i < 2 * kTileRows * ng; i += kSeqConsumers) {
+                        // Only the last tile of the operation is ragged; its team
+                        // fills the scales the producer could not copy.
+                        for (int i = tw * 32 + lane; i < 2 * kTileRows * ng; i += kSeqTeamWarps * 32) {
                             const int arr = i / (kTileRows * ng), r = (i / ng) % kTileRows, gi = i % ng;
                             const uint16_t *src = arr ? o.bi : o.sc;
                             sp[i] = src[(size_t)min(row0 + r, N - 1) * ng + gi];
                         }
-                        seq_sync();
+                        fence_proxy_async_smem();  // a later bulk copy reuses these bytes
+                        team_sync(team);
                     }
                     if (ok) {
-                        const int cg0 = ch * kChunkGroups;
-                        const int len = min(kChunkGroups, ng - cg0);
-                        const int cnt = len > warp ? (len - warp + kSeqWarps - 1) / kSeqWarps : 0;
-                        const uint8_t *wp = st + lane_w;
-                        const uint16_t *sa = sp + lg * ng + cg0 + warp;
-                        const uint16_t *sbb = sa + 8 * ng;
-                        const uint16_t *ba = sa + kTileRows * ng;
-                        const uint16_t *bb = sbb + kTileRows * ng;
-#pragma unroll
-                        for (int j = 0; j < kChunkGroups / kSeqWarps; ++j) {
-                            if (j < cnt) {
-                                const uint2 wa = *reinterpret_cast<const uint2 *>(wp + j * 4 * kBoxBytes);
-                                const uint2 wb = *reinterpret_cast<const uint2 *>(wp + j * 4 * kBoxBytes + 8 * 128);
-                                group_mma<NT>(acc, wa, wb, h2f(sa[16 * j]), h2f(sbb[16 * j]), h2f(ba[16 * j]),
-                                              h2f(bb[16 * j]), xf, xsum, cg0 + warp + 16 * j, M, lg, lt);
-                            }
-                        }
+                        const int g = ch * kChunkGroups + kBoxGroups * tw;
+                        const int n = min(kBoxGroups, ng - g);
+                        const uint4 *xg = reinterpret_cast<const uint4 *>(xf) + (size_t)g * 2 * M * 4;
+                        if (n == kBoxGroups)  // ng % 4 == 0 holds for every operation here
+                            box_mma<NT, M1, true>(acc, st, off, sp, ng, g, n, xg, xsum + g * M, M, lg, lt);
+                        else if (n > 0)
+                            box_mma<NT, M1, false>(acc, st, off, sp, ng, g, n, xg, xsum + g * M, M, lg, lt);
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(empty_bar(s));
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1;
+                    }
                 }
-                float *mine = red + ((size_t)tl * kSeqWarps + warp) * out16;
+                float *mine = red + ((size_t)tl * kSeqTeamWarps + tw) * out16;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -825,13 +889,14 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
                         if (col < M) mine[row * M + col] = acc.value(nt, i);
                     }
             }
+            base_it += ntl * nch;
             seq_sync();
             for (int i = tid; i < ntl * out16; i += kSeqConsumers) {
                 const int tl = i / out16, e = i % out16;
-                const float *grp = red + (size_t)tl * kSeqWarps * out16;
+                const float *grp = red + (size_t)tl * kSeqTeamWarps * out16;
                 float v = 0.f;
 #pragma unroll
-                for (int w = 0; w < kSeqWarps; ++w) v += grp[w * out16 + e];
+                for (int w = 0; w < kSeqTeamWarps; ++w) v += grp[w * out16 + e];
                 const int row = e / M, col = e % M, r = (t0 + tl) * kTileRows + row;
                 if (r < N) o.y[(size_t)col * N + r] = __half_as_ushort(__float2half_rn(v));
             }
@@ -848,8 +913,11 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
 }
 
 const void *stream_kernel_ptr(int M, bool lmhead) {
-    if (lmhead) return M <= 8 ? (const void *)stream_kernel<1, true> : (const void *)stream_kernel<2, true>;
-    return M <= 8 ? (const void *)stream_kernel<1, false> : (const void *)stream_kernel<2, false>;
+    if (lmhead)
+        return M == 1 ? (const void *)stream_kernel<1, true, true>
+                      : M <= 8 ? (const void *)stream_kernel<1, true, false> : (const void *)stream_kernel<2, true, false>;
+    return M == 1 ? (const void *)stream_kernel<1, false, true>
+                  : M <= 8 ? (const void *)stream_kernel<1, false, false> : (const void *)stream_kernel<2, false, false>;
 }
 
 // lm_head pass 2: one CTA per activation row merges the G*k candidates.
@@ -1076,7 +1144,7 @@ bool ensure_smem(const void *kern, size_t bytes) {
     return true;
 }
 
-template <int NT, bool LM>
+template <int NT, bool LM, bool M1>
 int launch_stream(const StreamPlan &p, const uint32_t *qw, bool overlap, cudaStream_t st) {
     CUtensorMap tm3, tm2;
     const uint64_t KW = (uint64_t)p.a.K / 8;
@@ -1090,7 +1158,7 @@ int launch_stream(const StreamPlan &p, const uint32_t *qw, bool overlap, cudaStr
     } else {
         tm3 = tm2;  // never used: every chunk takes the 2-D path
     }
-    auto kern = stream_kernel<NT, LM>;
+    auto kern = stream_kernel<NT, LM, M1>;
     if (!ensure_smem(reinterpret_cast<const void *>(kern), p.smem)) return W4_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.grid, 1, 1);
@@ -1142,7 +1210,8 @@ int gemv_impl(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, const u
     p.a.ws = nullptr;
     const bool ov = (flags & W4A16_OVERLAP_PREVIOUS) != 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return M <= 8 ? launch_stream<1, false>(p, qw, ov, s) : launch_stream<2, false>(p, qw, ov, s);
+    return M == 1 ? launch_stream<1, false, true>(p, qw, ov, s)
+                  : M <= 8 ? launch_stream<1, false, false>(p, qw, ov, s) : launch_stream<2, false, false>(p, qw, ov, s);
 }
 
 int lmhead_impl(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, const uint16_t *bi, int M, int N, int K,
@@ -1162,7 +1231,8 @@ int lmhead_impl(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, const
     p.a.ws = ws;
     const bool ov = (flags & W4A16_OVERLAP_PREVIOUS) != 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int st = M <= 8 ? launch_stream<1, true>(p, qw, ov, s) : launch_stream<2, true>(p, qw, ov, s);
+    const int st = M == 1 ? launch_stream<1, true, true>(p, qw, ov, s)
+                   : M <= 8 ? launch_stream<1, true, false>(p, qw, ov, s) : launch_stream<2, true, false>(p, qw, ov, s);
     if (st != W4A16_OK) return st;
     if (!ensure_smem(reinterpret_cast<const void *>(lmhead_pass2), smem2)) return W4_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
@@ -1190,7 +1260,7 @@ bool plan_seq(SeqParams &P, size_t &smem, int ng_max, int ntl_max) {
     P.w_bytes = (uint32_t)(kChunkGroups / kBoxGroups) * kBoxBytes;
     P.stage_bytes = (uint32_t)align_up((size_t)P.w_bytes + 64u * ng_max, 1024);
     const size_t fixed = align_up((size_t)ng_max * M * 128, 16) + align_up((size_t)ng_max * M * 4, 16) +
-                         align_up((size_t)ntl_max * kSeqWarps * kTileRows * M * 4, 16) + 16 * kMaxStages + 16 + 1024;
+                         align_up((size_t)ntl_max * kSeqTeamWarps * kTileRows * M * 4, 16) + 16 * kMaxStages + 16 + 1024;
     if (fixed + 2 * (size_t)P.stage_bytes > (size_t)kMaxSmem) return false;
     P.stages = (int)min((size_t)kMaxStages, ((size_t)kMaxSmem - fixed) / P.stage_bytes);
     size_t off = (size_t)P.stages * P.stage_bytes;
@@ -1199,7 +1269,7 @@ bool plan_seq(SeqParams &P, size_t &smem, int ng_max, int ntl_max) {
     P.off_xsum = (uint32_t)off;
     off = align_up(off + (size_t)ng_max * M * 4, 16);
     P.off_red = (uint32_t)off;
-    off = align_up(off + (size_t)ntl_max * kSeqWarps * kTileRows * M * 4, 16);
+    off = align_up(off + (size_t)ntl_max * kSeqTeamWarps * kTileRows * M * 4, 16);
     P.off_bar = (uint32_t)off;
     off += 16 * P.stages + 16;
     smem = off + 1024;
@@ -1236,7 +1306,8 @@ int seq_launch(const w4_gemv_op *ops, int nops, int M, unsigned *done, cudaStrea
     P.done = done;
     size_t smem = 0;
     if (!plan_seq(P, smem, ng_max, ntl_max)) return W4_ERR_SHAPE;
-    const void *kern = M <= 8 ? (const void *)seq_kernel<1> : (const void *)seq_kernel<2>;
+    const void *kern = M == 1 ? (const void *)seq_kernel<1, true>
+                       : M <= 8 ? (const void *)seq_kernel<1, false> : (const void *)seq_kernel<2, false>;
     if (!ensure_smem(kern, smem)) return W4_ERR_LAUNCH;
     if (cudaMemsetAsync(done, 0, sizeof(unsigned), st) != cudaSuccess) return W4_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
@@ -1249,7 +1320,9 @@ int seq_launch(const w4_gemv_op *ops, int nops, int M, unsigned *done, cudaStrea
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = M <= 8 ? cudaLaunchKernelEx(&cfg, seq_kernel<1>, P) : cudaLaunchKernelEx(&cfg, seq_kernel<2>, P);
+    const cudaError_t e = M == 1  ? cudaLaunchKernelEx(&cfg, seq_kernel<1, true>, P)
+                          : M <= 8 ? cudaLaunchKernelEx(&cfg, seq_kernel<1, false>, P)
+                                   : cudaLaunchKernelEx(&cfg, seq_kernel<2, false>, P);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return W4_ERR_LAUNCH;
