@@ -100,13 +100,24 @@ W4A16_API int w4_gemv_ex(const uint16_t *x, const uint32_t *qweight, const uint1
  *   gap": the per-token floor of some 250 small launches binds decode.)
  *   Runs ops[0..nops) in order, each exactly as w4_gemv would (same format,
  *   same results).  An operation with wait_prev != 0 reads activations that
- *   earlier operations of the list write: it starts only after all of them
- *   are complete and visible.  Weights are streamed without waiting, so they
+ *   earlier operations of the list write: it starts only after they are
+ *   complete and visible.  Weights are streamed without waiting, so they
  *   must not be written by the operations of the list.
  *   M       1..16 activation rows, shared by all operations.
  *   Each operation: N >= 1, K a multiple of 256, pointers 16-byte aligned.
- *   workspace  device buffer of w4_gemv_seq_workspace_bytes() bytes, 16-byte
- *              aligned (a completion counter, reset by each launch).
+ *   workspace  device buffer, 16-byte aligned, ZERO-FILLED before its first
+ *              use and then passed unchanged to every later call (the library
+ *              keeps its counters consistent: the last CTA of each launch
+ *              resets them and advances an epoch).  With at least
+ *              w4_gemv_seq_workspace_bytes_ex(ops, nops, M) bytes, an operation
+ *              whose x lies inside the output of the latest earlier operation
+ *              that writes any of x reads a tagged copy of that output (each
+ *              word carries a 16-bit (epoch, operation) tag and the reader
+ *              polls the words themselves); other waits, and every wait when
+ *              the workspace holds only w4_gemv_seq_workspace_bytes() bytes,
+ *              use a completion counter.  A workspace is used by one call at
+ *              a time.  After an expired wait its contents are undefined:
+ *              zero it again.
  *   flags   0.
  *   Long lists run as several launches of up to 96 operations; a launch is
  *   cooperative (one CTA per SM) and waits inside it are bounded (2 s; an
@@ -124,7 +135,13 @@ typedef struct {
     int reserved;             /* set to 0 */
 } w4_gemv_op;
 
+/* Minimum workspace (completion counters only). */
 W4A16_API size_t w4_gemv_seq_workspace_bytes(void);
+
+/* Workspace for the tagged activation exchange of this operation list:
+ * the counters plus, per launch of up to 96 operations, one uint32 word per
+ * output element of every operation whose output a later one reads. */
+W4A16_API size_t w4_gemv_seq_workspace_bytes_ex(const w4_gemv_op *ops, int nops, int M);
 
 W4A16_API int w4_gemv_seq(const w4_gemv_op *ops, int nops, int M, void *workspace,
             size_t workspace_bytes, unsigned flags, void *stream);

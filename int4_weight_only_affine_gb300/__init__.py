@@ -17,7 +17,7 @@ import os
 
 import torch
 
-__all__ = ["OVERLAP_PREVIOUS", "w4_gemv", "w4_gemv_seq", "GemvOp", "lm_head_argmax_topk", "lm_head_workspace_bytes", "w4_dequant_f16",
+__all__ = ["OVERLAP_PREVIOUS", "w4_gemv", "w4_gemv_seq", "seq_workspace", "seq_workspace_bytes", "GemvOp", "lm_head_argmax_topk", "lm_head_workspace_bytes", "w4_dequant_f16",
            "f16_gemm", "device_status", "W4A16Error", "LIB_PATH", "lib"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -47,6 +47,8 @@ def _load() -> ctypes.CDLL:
     L.w4_gemv_seq.argtypes = [P, I, I, P, Z, ctypes.c_uint, P]
     L.w4_gemv_seq_workspace_bytes.argtypes = []
     L.w4_gemv_seq_workspace_bytes.restype = Z
+    L.w4_gemv_seq_workspace_bytes_ex.argtypes = [P, I, I]
+    L.w4_gemv_seq_workspace_bytes_ex.restype = Z
     L.lm_head_workspace_bytes.argtypes = [I, I, I]
     L.lm_head_workspace_bytes.restype = Z
     L.w4_dequant_f16.argtypes = [P, P, P, P, I, I, I, P]
@@ -120,12 +122,7 @@ class GemvOp(ctypes.Structure):
                 ("wait_prev", ctypes.c_int), ("reserved", ctypes.c_int)]
 
 
-def w4_gemv_seq(ops, workspace: torch.Tensor | None = None, group: int = 64, stream=None):
-    """Run a list of GEMVs in one persistent launch.
-
-    ops: sequence of (x, qweight, scales, biases, y, wait_prev) with torch
-    tensors; wait_prev = True when x is written by an earlier operation of the
-    list.  All x share the same number of rows M.  Returns the list of y."""
+def _seq_array(ops, group):
     if group != 64:
         raise ValueError("group must be 64")
     arr = (GemvOp * len(ops))()
@@ -139,9 +136,35 @@ def w4_gemv_seq(ops, workspace: torch.Tensor | None = None, group: int = 64, str
             raise ValueError("all operations must have the same number of activation rows")
         arr[i] = GemvOp(_dev(x2, "x", _H), _dev(qw, "qweight", _QW), _dev(s, "scales", _H),
                         _dev(b, "biases", _H), _dev(y, "y", _H), N, K, 1 if wait else 0, 0)
+    return arr, M
+
+
+def seq_workspace_bytes(ops, group: int = 64) -> int:
+    """Workspace bytes for w4_gemv_seq(ops) with the tagged activation exchange
+    (w4_gemv_seq_workspace_bytes_ex); a smaller workspace of at least
+    w4_gemv_seq_workspace_bytes() bytes selects the completion-counter path."""
+    arr, M = _seq_array(ops, group)
+    return int(lib.w4_gemv_seq_workspace_bytes_ex(ctypes.cast(arr, ctypes.c_void_p), len(ops), M))
+
+
+def seq_workspace(ops, group: int = 64) -> torch.Tensor:
+    """A zero-filled workspace for w4_gemv_seq(ops); reuse it for every later
+    call with the same list (its counters reset themselves)."""
+    return torch.zeros(seq_workspace_bytes(ops, group), dtype=torch.uint8, device=ops[0][0].device)
+
+
+def w4_gemv_seq(ops, workspace: torch.Tensor | None = None, group: int = 64, stream=None):
+    """Run a list of GEMVs in one persistent launch.
+
+    ops: sequence of (x, qweight, scales, biases, y, wait_prev) with torch
+    tensors; wait_prev = True when x is written by an earlier operation of the
+    list.  All x share the same number of rows M.  workspace: from
+    seq_workspace(ops) (zero-filled before its first use, then passed
+    unchanged to every call); a fresh one is made when None.  Returns the
+    list of y."""
+    arr, M = _seq_array(ops, group)
     if workspace is None:
-        workspace = torch.empty(int(lib.w4_gemv_seq_workspace_bytes()), dtype=torch.uint8,
-                                device=ops[0][0].device)
+        workspace = seq_workspace(ops, group)
     _check("w4_gemv_seq", lib.w4_gemv_seq(ctypes.cast(arr, ctypes.c_void_p), len(ops), M,
                                           _dev(workspace, "workspace", (torch.uint8,)), workspace.numel(),
                                           0, _stream(stream)))

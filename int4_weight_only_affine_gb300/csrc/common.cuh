@@ -88,8 +88,7 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 // be null) is raised by the first wait that expires and makes every later
 // wait of the CTA give up at once, so the CTA can still reach its barriers
 // and exit.
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort = nullptr) {
-    if (mbar_try(bar, parity)) return true;
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort) {
     const uint64_t t0 = global_ns();
     for (uint32_t spin = 0; spin < kMaxSpins; ++spin) {
         if (mbar_try(bar, parity)) return true;
@@ -101,6 +100,10 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, vol
     atomicExch(&g_wait_expired, 1);
     if (abort) *abort = 1;
     return false;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort = nullptr) {
+    return mbar_try(bar, parity) || mbar_wait_slow(bar, parity, abort);
 }
 
 // Orders this thread's generic-proxy shared-memory writes before later

@@ -35,9 +35,10 @@
 //    outputs.  Launched without the attribute this is ordinary stream order.
 #include <cooperative_groups.h>
 
+#include <algorithm>
 #include <mutex>
 
-#include "common.cuh"
+#include "gemv_tile.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -80,219 +81,6 @@ int gemv_wait_flag() {
 }
 
 namespace {
-
-constexpr int kTileRows = 16;                    // output rows per MMA tile
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = kConsumerWarps * 32;  // 256
-constexpr int kThreads = kConsumers + 32;        // + one producer warp
-constexpr int kChunkGroups = 32;                 // groups per stage (8 boxes)
-constexpr int kBoxGroups = 4;                    // 128 bytes of codes per row
-constexpr int kBoxBytes = kTileRows * 128;       // 2 KB per TMA box
-constexpr int kMaxStages = 16;
-constexpr int kMaxSmem = 227 * 1024;
-constexpr int kMaxCandidates = 16384;            // pass-2 keys per activation row
-constexpr uint32_t kNibPair = 0x000F000Fu;
-constexpr uint32_t kNibPairHi = 0x00F000F0u;
-constexpr float kTwo24 = 16777216.0f;
-
-__host__ __device__ inline int pow2_at_least(int v) {
-    int p = 1;
-    while (p < v) p <<= 1;
-    return p;
-}
-
-__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) & ~(a - 1); }
-
-// ---------------------------------------------------------------------------
-// Activation staging.  For local group gl, fragment half h (MMAs j = 2h and
-// 2h+1), activation row c and lane quad t, four words are stored at
-//   xf[(((gl*2 + h)*M + c)*4 + t)*4 ...]  =  {b0(2h), b1(2h), b0(2h+1), b1(2h+1)}
-// with b0(j) = (x[c][k+j], x[c][k+j+4]), b1(j) = (x[c][k+8+j], x[c][k+12+j]),
-// k = 64G + 16t.  xsum[gl*M + c] = sum of the group's 64 activations (fp32).
-// The operands of the MMAs for j = 1 and 3 are stored divided by 16 (exact
-// for |x| >= 2^-10; below that the halving error is at most 2^-25), because
-// their codes are extracted 4 bits higher (see group_mma).
-// Run by `nthreads` threads (a multiple of 32) with thread index `tid`.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t sixteenth(uint32_t h2) {
-    const __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&h2), __float2half2_rn(0.0625f));
-    return *reinterpret_cast<const uint32_t *>(&v);
-}
-
-__device__ void stage_activations(const uint16_t *__restrict__ x, int M, int K, int g0, int ngl,
-                                  uint32_t *xf, float *xsum, int tid, int nthreads, bool coherent = false) {
-    const int items = ngl * M * 4;
-    for (int base = 0; base < items; base += nthreads) {
-        const int it = base + tid;
-        float part = 0.f;
-        if (it < items) {
-            const int t = it & 3;
-            const int c = (it >> 2) % M;
-            const int gl = (it >> 2) / M;
-            const uint4 *src =
-                reinterpret_cast<const uint4 *>(x + (size_t)c * K + (size_t)(g0 + gl) * kGroup + 16 * t);
-            // Activations written earlier in the same kernel must bypass the
-            // non-coherent read-only path.
-            const uint4 lo = coherent ? __ldcg(src) : __ldg(src);
-            const uint4 hi = coherent ? __ldcg(src + 1) : __ldg(src + 1);
-            uint4 f0, f1;
-            f0.x = __byte_perm(lo.x, lo.z, 0x5410);  // (x0, x4)
-            f0.y = __byte_perm(hi.x, hi.z, 0x5410);  // (x8, x12)
-            f0.z = sixteenth(__byte_perm(lo.x, lo.z, 0x7632));  // (x1, x5) / 16
-            f0.w = sixteenth(__byte_perm(hi.x, hi.z, 0x7632));  // (x9, x13) / 16
-            f1.x = __byte_perm(lo.y, lo.w, 0x5410);             // (x2, x6)
-            f1.y = __byte_perm(hi.y, hi.w, 0x5410);             // (x10, x14)
-            f1.z = sixteenth(__byte_perm(lo.y, lo.w, 0x7632));  // (x3, x7) / 16
-            f1.w = sixteenth(__byte_perm(hi.y, hi.w, 0x7632));  // (x11, x15) / 16
-            reinterpret_cast<uint4 *>(xf)[((gl * 2 + 0) * M + c) * 4 + t] = f0;
-            reinterpret_cast<uint4 *>(xf)[((gl * 2 + 1) * M + c) * 4 + t] = f1;
-            const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                part += h2f((uint16_t)(w[i] & 0xFFFFu));
-                part += h2f((uint16_t)(w[i] >> 16));
-            }
-        }
-        part += __shfl_xor_sync(0xffffffffu, part, 1);
-        part += __shfl_xor_sync(0xffffffffu, part, 2);
-        if (it < items && (it & 3) == 0) xsum[it >> 2] = part;
-    }
-}
-
-template <int NT>
-struct Acc {
-    float s[NT][4];
-    float b[NT][4];
-    __device__ __forceinline__ void zero() {
-#pragma unroll
-        for (int n = 0; n < NT; ++n)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) s[n][i] = b[n][i] = 0.f;
-    }
-    __device__ __forceinline__ float value(int nt, int i) const { return fmaf(kTwo24, s[nt][i], b[nt][i]); }
-};
-
-// One group (64 k) of the warp's 16-row tile: 4 MMAs per activation tile.
-// wa/wb: words 2t, 2t+1 of rows g and g+8; s*/b*: their scales and biases;
-// xg: the group's staged activation fragments, xs: its activation sums.
-// M1: a single activation row (only column 0 of the MMA result is used).
-template <int NT, bool M1>
-__device__ __forceinline__ void group_mma(Acc<NT> &acc, uint2 wa, uint2 wb, float sa, float sb, float ba,
-                                          float bb, const uint4 *xg, const float *xs, int M, int lg, int lt) {
-    // Codes j and j+4 of a word as a half pair: even j from (w >> 2j) & 0x000F000F
-    // (q * 2^-24), odd j from (w >> 2(j-1)) & 0x00F000F0 (q * 2^-20, matched by
-    // activations stored / 16): one shift per word.
-    uint32_t a0[4], a1[4], a2[4], a3[4];
-    const uint32_t w8[4] = {wa.x >> 8, wb.x >> 8, wa.y >> 8, wb.y >> 8};
-    a0[0] = wa.x & kNibPair;  // row g,   cols 2t,2t+1   <- k = 16t+j, +4
-    a1[0] = wb.x & kNibPair;  // row g+8, cols 2t,2t+1
-    a2[0] = wa.y & kNibPair;  // row g,   cols 2t+8,2t+9 <- k = 16t+8+j, +4
-    a3[0] = wb.y & kNibPair;  // row g+8, cols 2t+8,2t+9
-    a0[1] = wa.x & kNibPairHi;
-    a1[1] = wb.x & kNibPairHi;
-    a2[1] = wa.y & kNibPairHi;
-    a3[1] = wb.y & kNibPairHi;
-    a0[2] = w8[0] & kNibPair;
-    a1[2] = w8[1] & kNibPair;
-    a2[2] = w8[2] & kNibPair;
-    a3[2] = w8[3] & kNibPair;
-    a0[3] = w8[0] & kNibPairHi;
-    a1[3] = w8[1] & kNibPairHi;
-    a2[3] = w8[2] & kNibPairHi;
-    a3[3] = w8[3] & kNibPairHi;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int c = nt * 8 + lg;
-        uint4 f0 = make_uint4(0, 0, 0, 0), f1 = make_uint4(0, 0, 0, 0);
-        if (M1 ? lg == 0 : c < M) {
-            f0 = xg[(0 * M + c) * 4 + lt];
-            f1 = xg[(1 * M + c) * 4 + lt];
-        }
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_16816(d, a0[0], a1[0], a2[0], a3[0], f0.x, f0.y);
-        mma_16816(d, a0[1], a1[1], a2[1], a3[1], f0.z, f0.w);
-        mma_16816(d, a0[2], a1[2], a2[2], a3[2], f1.x, f1.y);
-        mma_16816(d, a0[3], a1[3], a2[3], a3[3], f1.z, f1.w);
-        if (M1) {
-            // Column 0 lives in d[0] (row g) and d[2] (row g+8) of lanes t = 0.
-            const float X0 = xs[0];
-            acc.s[nt][0] = fmaf(sa, d[0], acc.s[nt][0]);
-            acc.s[nt][2] = fmaf(sb, d[2], acc.s[nt][2]);
-            acc.b[nt][0] = fmaf(ba, X0, acc.b[nt][0]);
-            acc.b[nt][2] = fmaf(bb, X0, acc.b[nt][2]);
-        } else {
-            const int c0 = nt * 8 + 2 * lt;
-            const float X0 = (c0 < M) ? xs[c0] : 0.f;
-            const float X1 = (c0 + 1 < M) ? xs[c0 + 1] : 0.f;
-            acc.s[nt][0] = fmaf(sa, d[0], acc.s[nt][0]);
-            acc.s[nt][1] = fmaf(sa, d[1], acc.s[nt][1]);
-            acc.s[nt][2] = fmaf(sb, d[2], acc.s[nt][2]);
-            acc.s[nt][3] = fmaf(sb, d[3], acc.s[nt][3]);
-            acc.b[nt][0] = fmaf(ba, X0, acc.b[nt][0]);
-            acc.b[nt][1] = fmaf(ba, X1, acc.b[nt][1]);
-            acc.b[nt][2] = fmaf(bb, X0, acc.b[nt][2]);
-            acc.b[nt][3] = fmaf(bb, X1, acc.b[nt][3]);
-        }
-    }
-}
-
-// Shared-memory byte offsets, within a stage, of the words a lane reads for
-// group j (0..3) of box `box`: row g, 16-byte chunk 2j + t/2 under the
-// 128-byte swizzle (chunk index XOR row % 8), word pair t % 2.  Row g+8 is
-// 1024 bytes further with the same swizzle phase.
-__device__ __forceinline__ void box_offsets(int (&off)[4], int box, int lg, int lt) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        off[j] = box * kBoxBytes + lg * 128 + ((((2 * j) | (lt >> 1)) ^ (lg & 7)) << 4) + ((lt & 1) << 3);
-}
-
-__device__ __forceinline__ void unpack4h(uint2 v, float (&f)[4]) {
-    const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&v.x));
-    const float2 hi = __half22float2(*reinterpret_cast<const __half2 *>(&v.y));
-    f[0] = lo.x;
-    f[1] = lo.y;
-    f[2] = hi.x;
-    f[3] = hi.y;
-}
-
-// The warp's box of a stage: n (1..4) consecutive groups of a 16-row tile.
-// st: the stage; sp: the tile's scales [16][ng] (biases follow);
-// g: the box's first group (index into a scale row); xg: staged activations
-// of that group; xs: its activation sums.  FULL: n == 4 and ng % 4 == 0, so
-// a lane's four scales of a row are one aligned 8-byte word.
-template <int NT, bool M1, bool FULL>
-__device__ __forceinline__ void box_mma(Acc<NT> &acc, const uint8_t *st, const int (&off)[4], const uint16_t *sp,
-                                        int ng, int g, int n, const uint4 *xg, const float *xs, int M, int lg,
-                                        int lt) {
-    const uint16_t *sa = sp + lg * ng + g;  // scales of row g; row g+8 is 8 rows on
-    const uint16_t *ba = sa + kTileRows * ng;
-    float fsa[4], fsb[4], fba[4], fbb[4];
-    if (FULL) {
-        unpack4h(*reinterpret_cast<const uint2 *>(sa), fsa);
-        unpack4h(*reinterpret_cast<const uint2 *>(sa + 8 * ng), fsb);
-        unpack4h(*reinterpret_cast<const uint2 *>(ba), fba);
-        unpack4h(*reinterpret_cast<const uint2 *>(ba + 8 * ng), fbb);
-    } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int jj = j < n ? j : 0;
-            fsa[j] = h2f(sa[jj]);
-            fsb[j] = h2f(sa[8 * ng + jj]);
-            fba[j] = h2f(ba[jj]);
-            fbb[j] = h2f(ba[8 * ng + jj]);
-        }
-    }
-    const int xstep = 2 * M * 4;  // uint4 words of staged activations per group
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        if (FULL || j < n) {
-            const uint2 wa = *reinterpret_cast<const uint2 *>(st + off[j]);
-            const uint2 wb = *reinterpret_cast<const uint2 *>(st + off[j] + 8 * 128);
-            group_mma<NT, M1>(acc, wa, wb, fsa[j], fsb[j], fba[j], fbb[j], xg + j * (M1 ? 8 : xstep),
-                              xs + j * (M1 ? 1 : M), M, lg, lt);
-        }
-    }
-}
 
 // ---------------------------------------------------------------------------
 // Token selection keys: (value desc, index asc) as one uint64 so that larger
@@ -548,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
         // Warp w takes box w of every stage: groups 4w .. 4w+3 of the chunk.
         int off[4];
         box_offsets(off, warp, lg, lt);
+        const int xoff = lane_xoff(M, lg, lt), xd1 = lane_xd1(M, lg);
         const bool vec = (ng & 3) == 0;
         pdl_wait();
         stage_activations(a.x, M, a.K, gs0, ngl, xf, xsum, tid, kConsumers);
@@ -579,11 +368,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
                     const int g = gs0 + ch * kChunkGroups + kBoxGroups * warp;
                     const int n = min(kBoxGroups, gs1 - g);
                     const int gl = g - gs0;
-                    const uint4 *xg = reinterpret_cast<const uint4 *>(xf) + (size_t)gl * 2 * M * 4;
+                    const uint4 *xl = reinterpret_cast<const uint4 *>(xf) + (size_t)gl * 2 * M * 4 + xoff;
                     if (n == kBoxGroups && vec)
-                        box_mma<NT, M1, true>(acc, st, off, sp, ng, g, n, xg, xsum + gl * M, M, lg, lt);
+                        box_mma<NT, M1, true>(acc, st, off, sp, ng, g, n, xl, xd1, xsum + gl * M, M, lg, lt);
                     else if (n > 0)
-                        box_mma<NT, M1, false>(acc, st, off, sp, ng, g, n, xg, xsum + gl * M, M, lg, lt);
+                        box_mma<NT, M1, false>(acc, st, off, sp, ng, g, n, xl, xd1, xsum + gl * M, M, lg, lt);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_bar(s));
@@ -710,6 +499,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
 // tiles are split over the CTAs; outputs are combined in fixed order.
 // ---------------------------------------------------------------------------
 constexpr int kSeqMaxOps = 96;  // operations per launch (tensor maps travel as kernel parameters)
+constexpr size_t kSeqCounterBytes = 16;  // workspace head: completion counter, epoch, finished CTAs
 constexpr int kSeqWarps = 16;
 constexpr int kSeqTeamWarps = 8;  // consumer warps per tile team
 constexpr int kSeqConsumers = kSeqWarps * 32;
@@ -718,17 +508,28 @@ constexpr int kSeqThreads = kSeqConsumers + 32;
 struct SeqOp {
     const uint16_t *x, *sc, *bi;
     uint16_t *y;
+    const uint32_t *xt;  // tagged copy of x written earlier in this launch, or null
+    uint32_t *yt;        // tagged copy of y for later operations, or null
     int N, K, wait_prev, cq;
+    int src;             // operation (of this launch) that writes xt
 };
 
 struct SeqParams {
     CUtensorMap maps[kSeqMaxOps];  // 3-D code maps, one per operation
     SeqOp ops[kSeqMaxOps];
-    unsigned *done;                // (operation, CTA) completions so far
+    unsigned *ws;                  // [0] (operation, CTA) completions, [1] launch epoch, [2] CTAs finished
     int nops, M, stages;
+    int publish;                   // 1: some operation waits on the completion counter
     uint32_t stage_bytes, w_bytes;
     uint32_t off_xf, off_xsum, off_red, off_bar;
 };
+
+// 16-bit tag (1..65535) of the words operation `op` writes in the launch of
+// epoch `epoch`: distinct for the operations of a launch and from those of the
+// previous launch as long as nops < 65535.
+__device__ __forceinline__ uint32_t seq_tag(unsigned epoch, int nops, int op) {
+    return (uint32_t)(((unsigned long long)epoch * (unsigned)nops + (unsigned)op) % 65535ull) + 1u;
+}
 
 __device__ __forceinline__ void seq_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSeqConsumers) : "memory"); }
 // Named barrier of one 8-warp team (ids 2 and 3).
@@ -814,6 +615,12 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
         // Warp tw of a team takes box tw of every stage (groups 4tw .. 4tw+3).
         int off[4];
         box_offsets(off, tw, lg, lt);
+        const int xoff = lane_xoff(M, lg, lt), xd1 = lane_xd1(M, lg);
+        // The workspace epoch counts completed launches; (epoch, operation)
+        // names the 16-bit tag of every tagged word an operation writes, so a
+        // word left by an earlier launch never matches.
+        unsigned epoch;
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(epoch) : "l"(P.ws + 1) : "memory");
         pdl_wait();
         int base_it = 0;  // stages consumed by all earlier operations
         for (int op = 0; op < P.nops; ++op) {
@@ -822,11 +629,11 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
             const int T = (N + kTileRows - 1) / kTileRows;
             const int t0 = (int)((long long)blk * T / G), t1 = (int)((long long)(blk + 1) * T / G);
             const int ntl = t1 - t0;
-            if (o.wait_prev && op > 0 && tid == 0) {
+            if (o.wait_prev && op > 0 && !o.xt && tid == 0) {
                 // Every CTA has published operations 0..op-1.
                 const unsigned target = (unsigned)op * (unsigned)G;
                 const uint64_t t_start = global_ns();
-                while (ld_acquire_u32(P.done) < target) {
+                while (ld_acquire_u32(P.ws) < target) {
                     if (*abort_flag) break;
                     if (global_ns() - t_start > kWaitNs) {
                         atomicExch(&g_wait_expired, 1);
@@ -836,7 +643,14 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
                 }
             }
             seq_sync();  // also ends every use of the previous operation's activations
-            stage_activations(o.x, M, o.K, 0, ng, xf, xsum, tid, kSeqConsumers, true);
+            if (o.xt) {
+                // Activations produced by an earlier operation of this launch: poll
+                // the tagged words themselves (one L2 round trip, no counter).
+                stage_activations_t<true>(nullptr, o.xt, seq_tag(epoch, P.nops, o.src), M, o.K, 0, ng, xf, xsum,
+                                          tid, kSeqConsumers, true, abort_flag);
+            } else {
+                stage_activations(o.x, M, o.K, 0, ng, xf, xsum, tid, kSeqConsumers, true);
+            }
             seq_sync();
             for (int tl = team; tl < ntl; tl += 2) {
                 const int row0 = (t0 + tl) * kTileRows;
@@ -866,11 +680,11 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
                     if (ok) {
                         const int g = ch * kChunkGroups + kBoxGroups * tw;
                         const int n = min(kBoxGroups, ng - g);
-                        const uint4 *xg = reinterpret_cast<const uint4 *>(xf) + (size_t)g * 2 * M * 4;
+                        const uint4 *xl = reinterpret_cast<const uint4 *>(xf) + (size_t)g * 2 * M * 4 + xoff;
                         if (n == kBoxGroups)  // ng % 4 == 0 holds for every operation here
-                            box_mma<NT, M1, true>(acc, st, off, sp, ng, g, n, xg, xsum + g * M, M, lg, lt);
+                            box_mma<NT, M1, true>(acc, st, off, sp, ng, g, n, xl, xd1, xsum + g * M, M, lg, lt);
                         else if (n > 0)
-                            box_mma<NT, M1, false>(acc, st, off, sp, ng, g, n, xg, xsum + g * M, M, lg, lt);
+                            box_mma<NT, M1, false>(acc, st, off, sp, ng, g, n, xl, xd1, xsum + g * M, M, lg, lt);
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(empty_bar(s));
@@ -898,14 +712,32 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
 #pragma unroll
                 for (int w = 0; w < kSeqTeamWarps; ++w) v += grp[w * out16 + e];
                 const int row = e / M, col = e % M, r = (t0 + tl) * kTileRows + row;
-                if (r < N) o.y[(size_t)col * N + r] = __half_as_ushort(__float2half_rn(v));
+                if (r < N) {
+                    const uint16_t h = __half_as_ushort(__float2half_rn(v));
+                    o.y[(size_t)col * N + r] = h;
+                    if (o.yt) {
+                        const uint32_t w = (seq_tag(epoch, P.nops, op) << 16) | h;
+                        asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(o.yt + (size_t)col * N + r), "r"(w)
+                                     : "memory");
+                    }
+                }
             }
             // Publish: the CTA barrier orders every thread's stores before the
-            // signalling thread's GPU-scope fence and counter increment.
-            seq_sync();
-            if (tid == 0) {
+            // signalling thread's release increment (cumulative at gpu scope).
+            if (P.publish) {
+                seq_sync();
+                if (tid == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(P.ws) : "memory");
+            }
+        }
+        if (tid == 0) {
+            // The last CTA to finish resets the counters and advances the epoch
+            // for the next launch on this workspace.
+            __threadfence();
+            if (atomicAdd(P.ws + 2, 1u) == (unsigned)G - 1u) {
                 __threadfence();
-                atomicAdd(P.done, 1u);
+                P.ws[0] = 0u;
+                P.ws[2] = 0u;
+                P.ws[1] = epoch + 1u;
             }
         }
     }
@@ -1276,11 +1108,57 @@ bool plan_seq(SeqParams &P, size_t &smem, int ng_max, int ntl_max) {
     return smem <= (size_t)kMaxSmem;
 }
 
-int seq_launch(const w4_gemv_op *ops, int nops, int M, unsigned *done, cudaStream_t st) {
+// Which activations of a launch's operations come from an earlier operation
+// of the same launch: for operation c with wait_prev, the latest earlier
+// operation whose output range overlaps x; when x lies inside that output,
+// c reads its tagged copy (src[c] = that operation), otherwise it falls back to
+// the completion counter (src[c] = -1).  tagged[i]: operation i's output is
+// read this way.  Returns the tagged-copy bytes the launch needs.
+size_t seq_sources(const w4_gemv_op *ops, int nops, int M, int *src, bool *tagged) {
+    for (int i = 0; i < nops; ++i) {
+        src[i] = -1;
+        tagged[i] = false;
+    }
+    for (int c = 1; c < nops; ++c) {
+        if (!ops[c].wait_prev) continue;
+        const uintptr_t x0 = reinterpret_cast<uintptr_t>(ops[c].x);
+        const uintptr_t x1 = x0 + (uintptr_t)M * ops[c].K * 2;
+        for (int i = c - 1; i >= 0; --i) {
+            const uintptr_t y0 = reinterpret_cast<uintptr_t>(ops[i].y);
+            const uintptr_t y1 = y0 + (uintptr_t)M * ops[i].N * 2;
+            if (x1 <= y0 || y1 <= x0) continue;  // disjoint
+            if (x0 >= y0 && x1 <= y1 && (x0 - y0) % 2 == 0) {
+                src[c] = i;
+                tagged[i] = true;
+            }
+            break;
+        }
+    }
+    size_t bytes = 0;
+    for (int i = 0; i < nops; ++i)
+        if (tagged[i]) bytes += align_up((size_t)M * ops[i].N * 4, 16);
+    return bytes;
+}
+
+int seq_launch(const w4_gemv_op *ops, int nops, int M, unsigned *ws, uint8_t *tagbuf, size_t tag_bytes,
+               cudaStream_t st) {
     static SeqParams P;  // large: kept off the stack (calls are host-serialised per process)
+    static int src[kSeqMaxOps];
+    static bool tagged[kSeqMaxOps];
     static std::mutex mu;
     std::lock_guard<std::mutex> lock(mu);
     const int G = sm_count();
+    // Tagged exchange when the workspace has room for it, else the counter.
+    const bool use_tags = tagbuf && seq_sources(ops, nops, M, src, tagged) <= tag_bytes;
+    uint32_t *yts[kSeqMaxOps];
+    size_t toff = 0;
+    for (int i = 0; i < nops; ++i) {
+        yts[i] = nullptr;
+        if (use_tags && tagged[i]) {
+            yts[i] = reinterpret_cast<uint32_t *>(tagbuf + toff);
+            toff += align_up((size_t)M * ops[i].N * 4, 16);
+        }
+    }
     int ng_max = 1, ntl_max = 1;
     for (int i = 0; i < nops; ++i) {
         const w4_gemv_op &o = ops[i];
@@ -1292,6 +1170,9 @@ int seq_launch(const w4_gemv_op *ops, int nops, int M, unsigned *done, cudaStrea
         d.N = o.N;
         d.K = o.K;
         d.wait_prev = o.wait_prev;
+        d.yt = yts[i];
+        d.src = use_tags ? src[i] : -1;
+        d.xt = d.src >= 0 ? yts[d.src] + (reinterpret_cast<const uint16_t *>(o.x) - ops[d.src].y) : nullptr;
         const int nq = o.K / 256;
         d.cq = min(kChunkGroups / kBoxGroups, nq);
         ng_max = max(ng_max, o.K / kGroup);
@@ -1303,13 +1184,15 @@ int seq_launch(const w4_gemv_op *ops, int nops, int M, unsigned *done, cudaStrea
     }
     P.nops = nops;
     P.M = M;
-    P.done = done;
+    P.ws = ws;
+    P.publish = 0;
+    for (int i = 1; i < nops; ++i)
+        if (P.ops[i].wait_prev && !P.ops[i].xt) P.publish = 1;
     size_t smem = 0;
     if (!plan_seq(P, smem, ng_max, ntl_max)) return W4_ERR_SHAPE;
     const void *kern = M == 1 ? (const void *)seq_kernel<1, true>
                        : M <= 8 ? (const void *)seq_kernel<1, false> : (const void *)seq_kernel<2, false>;
     if (!ensure_smem(kern, smem)) return W4_ERR_LAUNCH;
-    if (cudaMemsetAsync(done, 0, sizeof(unsigned), st) != cudaSuccess) return W4_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G, 1, 1);
     cfg.blockDim = dim3(kSeqThreads, 1, 1);
@@ -1375,7 +1258,21 @@ extern "C" int lm_head_argmax_topk_ex(const uint16_t *x, const uint32_t *qweight
                        reinterpret_cast<uint64_t *>(workspace), workspace_bytes, flags, stream);
 }
 
-extern "C" size_t w4_gemv_seq_workspace_bytes(void) { return 16; }
+extern "C" size_t w4_gemv_seq_workspace_bytes(void) { return kSeqCounterBytes; }
+
+extern "C" size_t w4_gemv_seq_workspace_bytes_ex(const w4_gemv_op *ops, int nops, int M) {
+    if (!ops || nops < 1 || M < 1 || M > 16) return kSeqCounterBytes;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    static int src[kSeqMaxOps];
+    static bool tagged[kSeqMaxOps];
+    size_t most = 0;
+    for (int first = 0; first < nops; first += kSeqMaxOps) {
+        const int n = min(kSeqMaxOps, nops - first);
+        most = std::max(most, seq_sources(ops + first, n, M, src, tagged));
+    }
+    return kSeqCounterBytes + most;
+}
 
 extern "C" int w4_gemv_seq(const w4_gemv_op *ops, int nops, int M, void *workspace, size_t workspace_bytes,
                            unsigned flags, void *stream) {
@@ -1394,7 +1291,10 @@ extern "C" int w4_gemv_seq(const w4_gemv_op *ops, int nops, int M, void *workspa
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     for (int first = 0; first < nops; first += kSeqMaxOps) {
         const int n = min(kSeqMaxOps, nops - first);
-        const int st = seq_launch(ops + first, n, M, reinterpret_cast<unsigned *>(workspace), s);
+        uint8_t *ws8 = reinterpret_cast<uint8_t *>(workspace);
+        const int st = seq_launch(ops + first, n, M, reinterpret_cast<unsigned *>(workspace),
+                                  workspace_bytes > kSeqCounterBytes ? ws8 + kSeqCounterBytes : nullptr,
+                                  workspace_bytes - kSeqCounterBytes, s);
         if (st != W4A16_OK) return st;
     }
     return W4A16_OK;

@@ -111,3 +111,46 @@ def test_status_strings(lib):
         s = L.w4a16_status_string(code)
         assert s and s != b"unknown status", name
     assert L.w4a16_status_string(999) == b"unknown status"
+
+
+class _Op(ctypes.Structure):
+    """Mirror of w4_gemv_op (the C struct of include/w4a16.h)."""
+    _fields_ = [("x", ctypes.c_void_p), ("qweight", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("biases", ctypes.c_void_p), ("y", ctypes.c_void_p), ("N", ctypes.c_int), ("K", ctypes.c_int),
+                ("wait_prev", ctypes.c_int), ("reserved", ctypes.c_int)]
+
+
+def _seq_bytes(lib, ops, M):
+    lib.w4_gemv_seq_workspace_bytes_ex.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
+    lib.w4_gemv_seq_workspace_bytes_ex.restype = ctypes.c_size_t
+    arr = (_Op * len(ops))(*ops)
+    return lib.w4_gemv_seq_workspace_bytes_ex(ctypes.cast(arr, ctypes.c_void_p), len(ops), M)
+
+
+def test_seq_workspace_sizes_follow_the_producer_of_each_input(lib):
+    """Host-only: the tagged-exchange workspace holds one uint32 per output
+    element of each operation whose output a later waiting operation reads
+    (x inside that output: whole, prefix or interior), on top of the 16-byte
+    counter head.  Addresses are never dereferenced."""
+    lib.w4_gemv_seq_workspace_bytes.restype = ctypes.c_size_t
+    head = lib.w4_gemv_seq_workspace_bytes()
+    assert head == 16
+    W = 0x7000_0000
+    a, b, c, d = 0x1000_0000, 0x2000_0000, 0x3000_0000, 0x4000_0000
+    M = 2
+    # op1 reads all of op0's output, op2 reads a prefix of op1's, op3 reads an
+    # unrelated buffer (counter path), op4 does not wait.
+    ops = [_Op(a, W, W, W, b, 2560, 2048, 0, 0),
+           _Op(b, W, W, W, c, 1024, 2560, 1, 0),
+           _Op(c, W, W, W, d, 256, 512, 1, 0),
+           _Op(a, W, W, W, d + 0x10_0000, 256, 2048, 1, 0),
+           _Op(d, W, W, W, d + 0x20_0000, 256, 256, 0, 0)]
+    want = head + M * 2560 * 4 + M * 1024 * 4
+    assert _seq_bytes(lib, ops, M) == want
+    # x straddling the end of the producer's output: counter path, no tagged copy
+    ops2 = [_Op(a, W, W, W, b, 256, 256, 0, 0), _Op(b + 256, W, W, W, c, 256, 256, 1, 0)]
+    assert _seq_bytes(lib, ops2, M) == head
+    # a later writer of the same range shadows the earlier one
+    ops3 = [_Op(a, W, W, W, b, 512, 256, 0, 0), _Op(a, W, W, W, b, 256, 256, 0, 0),
+            _Op(b, W, W, W, c, 256, 256, 1, 0)]
+    assert _seq_bytes(lib, ops3, 1) == head + 256 * 4

@@ -60,6 +60,66 @@ def test_seq_chain_matches_oracle(w4, M):
         assert ok, f"op {i}: worst err/tol = {worst}"
 
 
+@pytest.mark.parametrize("mode", ["tagged", "counter"])
+def test_seq_chain_repeated_calls_share_a_workspace(w4, mode):
+    """Three calls on one workspace: the tagged exchange (words carry an
+    (epoch, operation) tag) and the completion-counter fallback (a 16-byte
+    workspace) give the oracle's results every time, so each launch resets
+    the counters and a word left by the previous launch is never taken."""
+    import torch
+    M = 2
+    plan = [(1024, 2048, False), (2048, 1024, True), (1024, 1536, True), (1536, 512, True)]
+    mats = [synth.make_linear(1300 + i, N, K) + (N, K) for i, (K, N, _) in enumerate(plan)]
+    chain = [c for _, _, c in plan]
+    outs, ads, xs = _oracle_chain(M, synth.make_x(78, M, plan[0][0]), mats, chain)
+    ys = [torch.empty((M, N), dtype=torch.float16, device="cuda") for _, N, _ in plan]
+    ops = [((ys[i - 1] if c else to_dev(xs[i])), to_dev(qw), to_dev(s), to_dev(b), ys[i], c)
+           for i, ((qw, s, b, N, K), c) in enumerate(zip(mats, chain))]
+    if mode == "tagged":
+        ws = w4.seq_workspace(ops)
+        assert ws.numel() == 16 + 4 * M * (2048 + 1024 + 1536)
+    else:
+        ws = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    for call in range(3):
+        for y in ys:
+            y.fill_(float("nan"))
+        w4.w4_gemv_seq(ops, workspace=ws)
+        torch.cuda.synchronize()
+        assert w4.device_status() == 0
+        for i in range(len(plan)):
+            ok, worst = within_tol(ys[i].cpu().numpy(), outs[i], ads[i])
+            assert ok, f"call {call} op {i}: worst err/tol = {worst}"
+    head = ws[:12].cpu().numpy().view(np.uint32)
+    assert head[0] == 0 and head[2] == 0 and head[1] == 3  # counters reset, epoch advanced once per launch
+
+
+def test_seq_reads_a_prefix_of_the_previous_output(w4):
+    """M = 1: an operation whose x is the first K elements of the previous
+    output (K < N), as a projection reading part of a fused q|k|v output."""
+    import torch
+    M = 1
+    plan = [(2048, 2560), (2048, 1024), (512, 768)]
+    mats = [synth.make_linear(1400 + i, N, K) + (N, K) for i, (K, N) in enumerate(plan)]
+    x0 = synth.make_x(79, M, 2048)
+    y0, ad0 = oracle.gemv(x0, *mats[0][:3], 2560, 2048, threads=16)
+    x1 = oracle.double_to_half_array(y0.ravel()[:2048]).reshape(1, 2048).view(np.float16)
+    y1, ad1 = oracle.gemv(x1, *mats[1][:3], 1024, 2048, threads=16)
+    x2 = oracle.double_to_half_array(y1.ravel()[:512]).reshape(1, 512).view(np.float16)
+    y2, ad2 = oracle.gemv(x2, *mats[2][:3], 768, 512, threads=16)
+    ys = [torch.empty((M, N), dtype=torch.float16, device="cuda") for _, N in plan]
+    ops = [(to_dev(x0), *[to_dev(a) for a in mats[0][:3]], ys[0], False),
+           (ys[0][:, :2048], *[to_dev(a) for a in mats[1][:3]], ys[1], True),
+           (ys[1][:, :512], *[to_dev(a) for a in mats[2][:3]], ys[2], True)]
+    ws = w4.seq_workspace(ops)
+    assert ws.numel() == 16 + 4 * (2560 + 1024)
+    w4.w4_gemv_seq(ops, workspace=ws)
+    torch.cuda.synchronize()
+    assert w4.device_status() == 0
+    for y, yo, ad in ((ys[0], y0, ad0), (ys[1], y1, ad1), (ys[2], y2, ad2)):
+        ok, worst = within_tol(y.cpu().numpy(), yo, ad)
+        assert ok, worst
+
+
 def test_seq_long_list_crosses_launches(w4):
     """More operations than one launch carries (96): every even op reads the
     previous op's output, including op 96, whose producer ran in the previous
