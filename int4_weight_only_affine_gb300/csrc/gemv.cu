@@ -125,95 +125,76 @@ __device__ uint64_t block_max_u64(uint64_t v, uint64_t *scratch) {
     return v;
 }
 
-// In-place descending bitonic sort of P (power of two) keys in shared memory.
-__device__ void bitonic_sort_desc(uint64_t *keys, int P) {
-    for (int size = 2, ls = 1; size <= P; size <<= 1, ++ls) {
-        for (int stride = size >> 1, lst = ls - 1; stride > 0; stride >>= 1, --lst) {
-            for (int i = threadIdx.x; i < (P >> 1); i += blockDim.x) {
-                const int lo = ((i >> lst) << (lst + 1)) | (i & (stride - 1));
-                const int hi = lo + stride;
-                const bool desc = (lo & size) == 0;
-                const uint64_t a = keys[lo], b = keys[hi];
-                if ((a < b) == desc) {
-                    keys[lo] = b;
-                    keys[hi] = a;
-                }
-            }
-            __syncthreads();
-        }
+// ---------------------------------------------------------------------------
+// Warp-level top-64 of 64-bit keys.  A warp holds a list of 64 keys sorted
+// descending, element i = 32*r + lane in register v[r].  A bitonic network
+// (compare-exchange stages over shuffles) sorts a chunk of 64 keys, and two
+// sorted lists merge into the 64 largest of their union: the elementwise
+// maximum of one list and the other reversed is a bitonic sequence holding
+// the 64 largest, which six more stages sort.  No block barrier is involved.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+__device__ __forceinline__ uint64_t umin64(uint64_t a, uint64_t b) { return a < b ? a : b; }
+
+// Two keys of a lane: list elements lane (a) and 32 + lane (b).
+struct Key2 {
+    uint64_t a, b;
+};
+
+// One compare-exchange stage: pairs (i, i ^ stride) ordered descending when
+// (i & size) == 0, ascending otherwise (the lower index keeps the larger key
+// in a descending block).
+__device__ __forceinline__ Key2 bitonic_stage64(Key2 v, int size, int stride, int lane) {
+    if (stride == 32) {  // only in the last block (size 64): descending
+        return Key2{umax64(v.a, v.b), umin64(v.a, v.b)};
     }
+    const uint64_t oa = __shfl_xor_sync(0xffffffffu, v.a, stride);
+    const uint64_t ob = __shfl_xor_sync(0xffffffffu, v.b, stride);
+    const bool lower = (lane & stride) == 0;
+    const bool keep_a = lower == ((lane & size) == 0);         // element lane
+    const bool keep_b = lower == (((32 + lane) & size) == 0);  // element 32 + lane
+    return Key2{keep_a ? umax64(v.a, oa) : umin64(v.a, oa), keep_b ? umax64(v.b, ob) : umin64(v.b, ob)};
 }
 
+// The network runs as loops in out-of-line functions: a single compact copy
+// of the code serves every call site.
+__device__ __noinline__ Key2 warp_sort64(Key2 v, int lane) {
+#pragma unroll 1
+    for (int size = 2; size <= 64; size <<= 1)
+#pragma unroll 1
+        for (int stride = size >> 1; stride > 0; stride >>= 1) v = bitonic_stage64(v, size, stride, lane);
+    return v;
+}
 
-// Block-wide top-k of n distinct keys (global or shared memory), written in
-// descending order to out[0..k), zero-padded when n < k.  A radix select over
-// the value word (4 passes of 8 bits) finds the value v of the k-th largest
-// key; every key whose value word is >= v is gathered into `buf` (capacity
-// >= n) and only those are sorted.  hist: 256 words, misc: 4 words of
-// shared memory.  Called by all threads of the block.
-__device__ void block_topk(const uint64_t *keys, int n, int k, uint64_t *out, uint64_t *buf,
-                           uint32_t *hist, uint32_t *misc) {
-    const int tid = threadIdx.x, bd = blockDim.x;
-    const int warp = tid >> 5, lane = tid & 31;
-    uint32_t prefix = 0, mask = 0;
-    if (n > k) {
-        uint32_t need = (uint32_t)k;
-        for (int shift = 24; shift >= 0; shift -= 8) {
-            for (int i = tid; i < 256; i += bd) hist[i] = 0;
-            __syncthreads();
-            for (int i = tid; i < n; i += bd) {
-                const uint32_t hi = (uint32_t)(keys[i] >> 32);
-                if ((hi & mask) == prefix) atomicAdd(&hist[(hi >> shift) & 255u], 1u);
-            }
-            __syncthreads();
-            if (warp == 0) {
-                // lane l owns bins 255-8l .. 248-8l, scanned from the top.
-                uint32_t c[8], sum = 0;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    c[j] = hist[255 - 8 * lane - j];
-                    sum += c[j];
-                }
-                uint32_t incl = sum;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += v;
-                }
-                const uint32_t excl = incl - sum;
-                if (excl < need && need <= incl) {
-                    uint32_t run = excl;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (run + c[j] >= need) {
-                            misc[0] = 255u - 8u * lane - j;
-                            misc[1] = run;
-                            break;
-                        }
-                        run += c[j];
-                    }
-                }
-            }
-            __syncthreads();
-            need -= misc[1];
-            prefix |= misc[0] << shift;
-            mask |= 255u << shift;
-            __syncthreads();
+// The 64 largest of run and c (both sorted descending), sorted descending.
+__device__ __noinline__ Key2 warp_merge64(Key2 run, Key2 c, int lane) {
+    const uint64_t ra = __shfl_sync(0xffffffffu, c.b, 31 - lane);  // c[63 - i] for i = lane
+    const uint64_t rb = __shfl_sync(0xffffffffu, c.a, 31 - lane);  // c[63 - i] for i = 32 + lane
+    Key2 v{umax64(run.a, ra), umax64(run.b, rb)};
+#pragma unroll 1
+    for (int stride = 32; stride > 0; stride >>= 1) v = bitonic_stage64(v, 64, stride, lane);
+    return v;
+}
+
+// The 64 largest of run and an unsorted chunk c.
+__device__ __forceinline__ Key2 warp_insert64(Key2 run, Key2 c, int lane) {
+    return warp_merge64(run, warp_sort64(c, lane), lane);
+}
+
+// Combines the sorted lists of nw warps (lists[w][64] in shared memory) into
+// lists[0] with a pairwise tree; called by every thread of the block.
+__device__ void block_merge_lists(uint64_t (*lists)[64], int nw) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int span = 1; span < nw; span <<= 1) {
+        __syncthreads();
+        // A sorted list that starts with 0 is empty: nothing to merge.
+        if ((warp % (2 * span)) == 0 && warp + span < nw && lists[warp + span][0] != 0ull) {
+            const Key2 run = warp_merge64(Key2{lists[warp][lane], lists[warp][32 + lane]},
+                                          Key2{lists[warp + span][lane], lists[warp + span][32 + lane]}, lane);
+            lists[warp][lane] = run.a;
+            lists[warp][32 + lane] = run.b;
         }
     }
-    if (tid == 0) misc[2] = 0;
-    __syncthreads();
-    for (int i = tid; i < n; i += bd) {
-        const uint64_t key = keys[i];
-        if ((uint32_t)(key >> 32) >= prefix) buf[atomicAdd(&misc[2], 1u)] = key;
-    }
-    __syncthreads();
-    const int m = (int)misc[2];
-    const int P = pow2_at_least(m > k ? m : k);
-    for (int i = m + tid; i < P; i += bd) buf[i] = 0ull;
-    __syncthreads();
-    bitonic_sort_desc(buf, P);
-    for (int i = tid; i < k; i += bd) out[i] = buf[i];
     __syncthreads();
 }
 
@@ -459,26 +440,32 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
     }
 
     // ---------------- lm_head pass 1: k best keys of this CTA's rows ----------------
+    // The keys of this CTA's rows, best first, padded with 0 (below every key).
     const int n0 = t0 * kTileRows;
     const int rows = min(N, t1 * kTileRows) - n0;
-    const int P = pow2_at_least(rows > a.k ? rows : a.k);
-    uint64_t *keys = reinterpret_cast<uint64_t *>(sb);  // the ring is free now
-    uint64_t *buf = keys + P;
-    uint32_t *hist = reinterpret_cast<uint32_t *>(buf + P);
+    uint64_t(*lists)[64] = reinterpret_cast<uint64_t(*)[64]>(sb);  // the ring is free now
+    constexpr int kWarps = kThreads / 32;
     for (int m = 0; m < M; ++m) {
         uint64_t *out = a.ws + ((size_t)m * gridDim.x + blockIdx.x) * a.k;
         if (a.k == 1) {
             uint64_t best = 0ull;
-            for (int i = tid; i < rows; i += kThreads) {
-                const uint64_t key = make_key(res[i * M + m], n0 + i);
-                best = key > best ? key : best;
-            }
-            best = block_max_u64(best, keys);
+            for (int i = tid; i < rows; i += kThreads) best = umax64(best, make_key(res[i * M + m], n0 + i));
+            best = block_max_u64(best, reinterpret_cast<uint64_t *>(sb));
             if (tid == 0) out[0] = best;
         } else {
-            for (int i = tid; i < rows; i += kThreads) keys[i] = make_key(res[i * M + m], n0 + i);
+            // Each warp keeps the best 64 of its 64-row chunks; a tree merges them.
+            Key2 run{0ull, 0ull};
+            for (int c0 = warp * 64; c0 < rows; c0 += kWarps * 64) {
+                const int i = c0 + lane, j = c0 + 32 + lane;
+                const Key2 c{i < rows ? make_key(res[i * M + m], n0 + i) : 0ull,
+                             j < rows ? make_key(res[j * M + m], n0 + j) : 0ull};
+                run = warp_insert64(run, c, lane);
+            }
+            lists[warp][lane] = run.a;
+            lists[warp][32 + lane] = run.b;
+            block_merge_lists(lists, kWarps);
+            for (int i = tid; i < a.k; i += kThreads) out[i] = lists[0][i];
             __syncthreads();
-            block_topk(keys, rows, a.k, out, buf, hist, hist + 256);
         }
     }
 }
@@ -752,20 +739,55 @@ const void *stream_kernel_ptr(int M, bool lmhead) {
                   : M <= 8 ? (const void *)stream_kernel<1, false, false> : (const void *)stream_kernel<2, false, false>;
 }
 
-// lm_head pass 2: one CTA per activation row merges the G*k candidates.
-__global__ void __launch_bounds__(1024)
+// lm_head pass 2: one CTA per activation row merges the G*k candidates
+// (G sorted lists of k keys).  Two lower bounds of the overall k-th key:
+// the largest of the lists' k-th keys (its own list holds k keys above it)
+// and the k-th largest of a subset of the lists' first keys (the best two
+// that each lane of one warp sees; k lists each hold one key above it).  Only keys >= the larger bound T can be selected; for logits
+// spread like independent samples about k of them remain.  They are
+// compacted into shared memory (an overflow goes straight into the warps'
+// running lists, so any input is handled), every warp keeps the best 64 of
+// its chunks, and a tree merges the warps' lists.  Launched as a programmatic
+// dependent of pass 1; it waits for pass 1's results first.
+// Keys are distinct (the index is part of the key), so the rank of a key
+// among a set is the number of larger keys: small sets (the lists' first
+// keys, the survivors) are ranked by counting in shared memory.
+// Number of keys in s[0..n) larger than key (shared memory, 8 loads in flight).
+__device__ __forceinline__ int rank_of(uint64_t key, const uint64_t *s, int n) {
+    int r = 0, j = 0;
+    for (; j + 8 <= n; j += 8) {
+        int c = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) c += s[j + u] > key;
+        r += c;
+    }
+    for (; j < n; ++j) r += s[j] > key;
+    return r;
+}
+
+constexpr int kPass2Threads = 1024;
+constexpr int kSurvivorCap = 2048;
+constexpr int kMaxPerThread = kMaxCandidates / kPass2Threads;  // candidates per row <= 16384
+static_assert(kSurvivorCap >= kPass2Threads, "the survivor buffer first holds one first key per thread");
+
+__global__ void __launch_bounds__(kPass2Threads)
     lmhead_pass2(const uint64_t *__restrict__ ws, int G, int k, int32_t *__restrict__ idx,
                  float *__restrict__ val) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint64_t *keys = reinterpret_cast<uint64_t *>(smem);
+    __shared__ uint64_t lists[kPass2Threads / 32][64];
+    __shared__ uint64_t buf[kSurvivorCap];
+    __shared__ uint64_t scratch[kPass2Threads / 32];
+    __shared__ unsigned nbuf;
+    pdl_wait();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int kWarps = kPass2Threads / 32;
     const int m = blockIdx.x;
     const int n = G * k;
     const uint64_t *src = ws + (size_t)m * n;
     if (k == 1) {
         uint64_t best = 0ull;
-        for (int i = threadIdx.x; i < n; i += blockDim.x) best = src[i] > best ? src[i] : best;
-        best = block_max_u64(best, keys);
-        if (threadIdx.x == 0) {
+        for (int i = tid; i < n; i += kPass2Threads) best = umax64(best, src[i]);
+        best = block_max_u64(best, scratch);
+        if (tid == 0) {
             float v;
             int id;
             decode_key(best, v, id);
@@ -774,13 +796,91 @@ __global__ void __launch_bounds__(1024)
         }
         return;
     }
-    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + (size_t)pow2_at_least(n) * 8);
-    __shared__ uint64_t top[64];
-    block_topk(src, n, k, top, keys, hist, hist + 256);
-    for (int i = threadIdx.x; i < k; i += blockDim.x) {
+    // Every load is issued before any result is used: the candidates (at
+    // most 16 per thread), the first key of list tid, and the k-th keys.
+    uint64_t v[kMaxPerThread];
+#pragma unroll
+    for (int j = 0; j < kMaxPerThread; ++j) {
+        const int i = tid + j * kPass2Threads;
+        v[j] = i < n ? src[i] : 0ull;
+    }
+    const uint64_t fk = tid < G ? src[(size_t)tid * k] : 0ull;  // first key of list tid
+    uint64_t t = 0ull;
+    for (int c = tid; c < G; c += kPass2Threads) t = umax64(t, src[(size_t)c * k + k - 1]);
+    uint64_t T = block_max_u64(t, scratch);
+    if (G >= k) {
+        // The k-th largest first key: k lists each hold a key at least that
+        // large.  Keys are distinct, so counting the larger ones gives every
+        // key its exact rank.
+        buf[tid] = fk;
+        if (tid == 0) scratch[0] = 0ull;
+        __syncthreads();
+        if (G <= kPass2Threads) {
+            if (tid < G && rank_of(fk, buf, G) == k - 1) scratch[0] = fk;
+        } else if (warp == 0) {
+            // Many lists: a looser bound, the k-th largest of the best two
+            // first keys each lane sees.
+            uint64_t f0 = 0ull, f1 = 0ull;
+            for (int c = lane; c < G; c += 32) {
+                const uint64_t f = c < kPass2Threads ? buf[c] : src[(size_t)c * k];
+                f1 = umax64(f1, umin64(f0, f));
+                f0 = umax64(f0, f);
+            }
+            const Key2 best = warp_sort64(Key2{f0, f1}, lane);
+            const uint64_t kth = __shfl_sync(0xffffffffu, (k - 1) < 32 ? best.a : best.b, (k - 1) & 31);
+            if (lane == 0) scratch[0] = kth;
+        }
+        __syncthreads();
+        T = umax64(T, scratch[0]);
+        __syncthreads();
+    }
+    if (tid == 0) nbuf = 0u;
+    __syncthreads();
+    // Compact the keys >= T (one reservation per warp and register).
+    Key2 run{0ull, 0ull};
+#pragma unroll
+    for (int j = 0; j < kMaxPerThread; ++j) {
+        const uint64_t key = v[j] >= T ? v[j] : 0ull;
+        const unsigned bal = __ballot_sync(0xffffffffu, key != 0ull);
+        if (bal == 0u) continue;
+        unsigned slot = 0;
+        if (lane == 0) slot = atomicAdd(&nbuf, (unsigned)__popc(bal));
+        slot = __shfl_sync(0xffffffffu, slot, 0);
+        if (slot + __popc(bal) <= (unsigned)kSurvivorCap) {
+            if (key) buf[slot + __popc(bal & ((1u << lane) - 1u))] = key;
+        } else {
+            // No room: keep them in this warp's list, and zero the reserved
+            // slots that fall inside the buffer.
+            if (slot + lane < (unsigned)kSurvivorCap && lane < __popc(bal)) buf[slot + lane] = 0ull;
+            run = warp_insert64(run, Key2{key, 0ull}, lane);
+        }
+    }
+    __syncthreads();
+    if (nbuf <= (unsigned)kSurvivorCap) {
+        // Every survivor is in buf: rank by counting, write the best k.
+        const int nb = (int)nbuf;
+        for (int i = tid; i < nb; i += kPass2Threads) {
+            const uint64_t key = buf[i];
+            const int r = rank_of(key, buf, nb);
+            if (r < k) {
+                float v;
+                int id;
+                decode_key(key, v, id);
+                idx[(size_t)m * k + r] = id;
+                val[(size_t)m * k + r] = v;
+            }
+        }
+        return;
+    }
+    for (int c0 = warp * 64; c0 < kSurvivorCap; c0 += kWarps * 64)
+        run = warp_insert64(run, Key2{buf[c0 + lane], buf[c0 + 32 + lane]}, lane);
+    lists[warp][lane] = run.a;
+    lists[warp][32 + lane] = run.b;
+    block_merge_lists(lists, kWarps);
+    for (int i = tid; i < k; i += kPass2Threads) {
         float v;
         int id;
-        decode_key(top[i], v, id);
+        decode_key(lists[0][i], v, id);
         idx[(size_t)m * k + i] = id;
         val[(size_t)m * k + i] = v;
     }
@@ -790,8 +890,6 @@ __global__ void __launch_bounds__(1024)
 // Host-side planning and launch.
 // ---------------------------------------------------------------------------
 
-// Pass 2 shared memory: gather buffer for up to n keys + histogram.
-inline size_t lm_pass2_smem(int n, int k) { return k == 1 ? 64 * 8 : (size_t)pow2_at_least(n) * 8 + 260 * 4; }
 
 // Upper bound on the pass-1 grid for a given (N, k), independent of the GPU.
 long long lm_max_blocks(int N, int k) {
@@ -820,8 +918,7 @@ bool layout_stream(StreamPlan &p, int M, bool lmhead, size_t ring_budget, int tp
     size_t off = (size_t)stages * a.stage_bytes;
     if (lmhead) {
         // After the main loop the ring holds the selection keys.
-        const int P = pow2_at_least(max(tpc * kTileRows, a.k));
-        const size_t need = (size_t)2 * P * 8 + 260 * 4;
+        const size_t need = (size_t)(kThreads / 32) * 64 * 8;  // per-warp lists of the selection
         if (off < need) off = align_up(need, 1024);
     }
     a.off_xf = (uint32_t)off;
@@ -1054,8 +1151,6 @@ int lmhead_impl(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, const
     const int G = p.grid;
     if ((long long)G > lm_max_blocks(N, k)) return W4_ERR_SHAPE;
     if (ws_bytes < (size_t)M * G * k * sizeof(uint64_t)) return W4_ERR_WORKSPACE;
-    const size_t smem2 = lm_pass2_smem(G * k, k);
-    if (smem2 > (size_t)kMaxSmem) return W4_ERR_SHAPE;
     p.a.x = x;
     p.a.sc = sc;
     p.a.bi = bi;
@@ -1066,12 +1161,18 @@ int lmhead_impl(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, const
     const int st = M == 1 ? launch_stream<1, true, true>(p, qw, ov, s)
                    : M <= 8 ? launch_stream<1, true, false>(p, qw, ov, s) : launch_stream<2, true, false>(p, qw, ov, s);
     if (st != W4A16_OK) return st;
-    if (!ensure_smem(reinterpret_cast<const void *>(lmhead_pass2), smem2)) return W4_ERR_LAUNCH;
+    // Pass 2 is launched as a programmatic dependent: its launch overlaps pass 1
+    // and it waits (griddepcontrol.wait) for pass 1's results.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(M, 1, 1);
-    cfg.blockDim = dim3(1024, 1, 1);
-    cfg.dynamicSmemBytes = smem2;
+    cfg.blockDim = dim3(kPass2Threads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, lmhead_pass2, (const uint64_t *)ws, G, k, idx, val);
     return e == cudaSuccess ? W4A16_OK : W4_ERR_LAUNCH;
 }
