@@ -5,11 +5,16 @@ as four row blocks: q|k|v, o, gate|up, down, i.e. the 7 projections with the
 blocks that share an input stored contiguously):
   prefill  - w4_dequant_f16 of all 144 weight blocks into the transposed half
              scratch, then f16_gemm at M = 1570 for each block;
-  decode   - one token at M = 1: 144 w4_gemv in layer order (each allowed to
-             stream its weights while the previous kernel finishes), then the
-             lm_head GEMV fused with top-50 selection;
-  batched  - the same projection set at M = 16 activation rows, then per-row
-             greedy argmax over the lm_head.
+  decode   - one token at M = 1: the 144 projection GEMVs in layer order as
+             one w4_gemv_seq list (a persistent launch per 96 operations;
+             every operation waits until all earlier ones are complete, as a
+             dependent chain of projections would), then the lm_head GEMV
+             fused with top-50 selection;
+  batched  - the same projection set at M = 16 activation rows (one w4_gemv
+             per block, each streaming its weights while the previous kernel
+             finishes), then per-row greedy argmax over the lm_head;
+  kernels  - the lm_head GEMV + top-50 alone, and the 36 gate|up GEMVs
+             (2048 -> 22016) back to back: per-kernel decode bandwidth.
 Each part is a CUDA graph replayed on one stream; CUDA events time each part.
 The headline `value` is the decode GEMV bandwidth (algorithmic bytes of the
 token's weights / decode time), the first quantity of the metric; the other
@@ -207,6 +212,30 @@ def run_ours(args, rank, world):
           "down": torch.randn((PREFILL_M, 11008), device=dev).half()}
     yp = {n: torch.empty((PREFILL_M, N), dtype=torch.float16, device=dev) for n, K, N, _ in FUSED}
     ov = w4.OVERLAP_PREVIOUS  # weights are constant: stream them while the previous kernel finishes
+    # decode M=1: the projection list, each operation waiting for all earlier ones
+    seq_ops = []
+    for l in range(LAYERS):
+        for name, _, _, _ in FUSED:
+            qw, s, b, N, K = model.layers[l][name]
+            seq_ops.append((xs1[SRC[name]], qw, s, b, ys1[name], len(seq_ops) > 0))
+    seq_ws = w4.seq_workspace(seq_ops)  # zero-filled once; its counters reset themselves
+    ys_gu = torch.empty((1, 2 * 11008), dtype=torch.float16, device=dev)
+
+    def decode_seq():
+        w4.w4_gemv_seq(seq_ops, workspace=seq_ws, stream=stream)
+        qw, s, b, N, K = model.lm
+        w4.lm_head_argmax_topk(xs1["lm"], qw, s, b, k=TOPK, idx=idx1, val=val1, workspace=ws1, stream=stream,
+                               flags=ov)
+
+    def lm_only():
+        qw, s, b, N, K = model.lm
+        w4.lm_head_argmax_topk(xs1["lm"], qw, s, b, k=TOPK, idx=idx1, val=val1, workspace=ws1, stream=stream,
+                               flags=ov)
+
+    def gate_up_only():
+        for l in range(LAYERS):
+            qw, s, b, N, K = model.layers[l]["gate_up"]
+            w4.w4_gemv(xs1["mlp"], qw, s, b, y=ys_gu, stream=stream, flags=ov)
 
     def decode(xs, ys, M, k, idx, val, ws):
         for l in range(LAYERS):
@@ -231,11 +260,15 @@ def run_ours(args, rank, world):
     parts = {
         "dequant": dequant_all,
         "gemm": gemm_all,
-        "decode_m1": lambda: decode(xs1, ys1, 1, TOPK, idx1, val1, ws1),
+        "decode_m1": decode_seq,
         "decode_m16": lambda: decode(xs16, ys16, BATCH_M, 1, idx16, val16, ws16),
+        "lm_head_m1": lm_only,
+        "gate_up_m1": gate_up_only,
     }
     nb = LAYERS * len(FUSED)
-    launches = {"dequant": nb, "gemm": nb, "decode_m1": nb + 2, "decode_m16": nb + 2}
+    n_seq = (nb + 95) // 96
+    launches = {"dequant": nb, "gemm": nb, "decode_m1": n_seq + 2, "decode_m16": nb + 2, "lm_head_m1": 2,
+                "gate_up_m1": LAYERS}
     # eager warm-up (sets kernel attributes), then capture one graph per part
     with torch.cuda.stream(stream):
         for f in parts.values():
@@ -251,7 +284,7 @@ def run_ours(args, rank, world):
     if w4.device_status() != 0:
         raise RuntimeError("device-side wait expired during warm-up")
 
-    order = ["dequant", "gemm", "decode_m1", "decode_m16"]
+    order = ["dequant", "gemm", "decode_m1", "decode_m16", "lm_head_m1", "gate_up_m1"]
     ev = {n: [] for n in order}
 
     def step(record):
@@ -460,6 +493,8 @@ def main():
     gemm_tflops = PREFILL_FLOPS / (pm["gemm"] / 1e3) / 1e12
     dq_gbs = DEQUANT_BYTES / (pm["dequant"] / 1e3) / 1e9
     m16_gbs = DECODE_BYTES / (pm["decode_m16"] / 1e3) / 1e9
+    lm_gbs = weight_bytes(LM_N, LM_K) / (pm["lm_head_m1"] / 1e3) / 1e9
+    gu_gbs = LAYERS * weight_bytes(2 * 11008, 2048) / (pm["gate_up_m1"] / 1e3) / 1e9
     line = {
         "metric": METRIC,
         "value": decode_gbs * world,
@@ -474,8 +509,9 @@ def main():
         "dtype": "f16",
         "data": "synthetic",
         "config": {"workload": "qwen2.5-3b: prefill M=1570 (dequant-once + f16 GEMM), decode M=1 "
-                               "(36 layers x [qkv, o, gate_up, down] GEMVs + lm_head top-50), batched decode "
-                               "M=16 (+ per-row argmax); q/k/v and gate/up stored as fused row blocks",
+                               "(36 layers x [qkv, o, gate_up, down] GEMVs as one dependent projection list "
+                               "+ lm_head top-50), batched decode M=16 (+ per-row argmax); q/k/v and gate/up "
+                               "stored as fused row blocks",
                    "model": "Qwen2.5-3B-shaped projections x36 + lm_head 2048->151936",
                    "global_batch": 1, "seq_len": PREFILL_M, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (1.74 GB of weights per decode pass, 5.5 GB scratch)"},
@@ -486,13 +522,18 @@ def main():
                            "tok_s": BATCH_M * 1e3 / pm["decode_m16"], "frac_hbm": m16_gbs / hbm},
             "dequant": {"ms": pm["dequant"], "GB_s": dq_gbs, "frac_hbm": dq_gbs / hbm},
             "gemm_m1570": {"ms": pm["gemm"], "TFLOP_s": gemm_tflops, "frac_tensor": gemm_tflops / tflops},
+            "lm_head_m1_top50": {"ms": pm["lm_head_m1"], "GB_s": lm_gbs, "frac_hbm": lm_gbs / hbm},
+            "gemv_gate_up_m1_x36": {"ms": pm["gate_up_m1"], "GB_s": gu_gbs, "frac_hbm": gu_gbs / hbm},
         },
         "roofline": {"bound": "tensor", "kernel": "f16_gemm (tcgen05)", "achieved": gemm_tflops,
                      "peak": tflops, "unit": "TFLOP/s", "frac": gemm_tflops / tflops, "traffic": None,
                      "peak_source": f"{peak_src} bf16 dense (fp16 dense taken equal)"},
-        "roofline_decode": {"bound": "hbm", "kernel": "w4_gemv + lm_head (decode token)",
+        "roofline_decode": {"bound": "hbm", "kernel": "w4_gemv_seq + lm_head (decode token, dependent chain)",
                             "achieved": decode_gbs, "peak": hbm, "unit": "GB/s", "frac": decode_gbs / hbm,
                             "traffic": None, "peak_source": f"{peak_src} HBM copy"},
+        "roofline_gemv": {"bound": "hbm", "kernel": "lm_head GEMV 2048->151936 + top-50 (largest decode GEMV)",
+                          "achieved": lm_gbs, "peak": hbm, "unit": "GB/s", "frac": lm_gbs / hbm,
+                          "traffic": None, "peak_source": f"{peak_src} HBM copy"},
         "e2e": {"value": DECODE_BYTES / r["e2e_s"] / 1e9 * world, "unit": "GB/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "note": "decode token through the Python binding: H2D activations, graph replay, D2H top-50"},
