@@ -21,7 +21,7 @@ token's weights / decode time), the first quantity of the metric; the other
 quantities are reported under `parts`.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-       python bench.py --profile gemv|gemm|dequant|lmhead   (small case for ncu)
+       python bench.py --profile gemv|gemm|dequant|lmhead|seq   (small case for ncu)
 Under torchrun (N > 1) every rank runs an independent replica (the path has no
 exchange step) and rank 0 prints one JSON line.
 """
@@ -423,6 +423,22 @@ def profile_case(which, iters=3):
         x = torch.from_numpy(synth.make_x(2, 1, LM_K)).to(dev)
         for _ in range(iters):
             w4.lm_head_argmax_topk(x, *a, k=TOPK)
+    elif which == "seq":
+        # two layers' blocks as one dependent projection list (M = 1)
+        ops = []
+        seeds = {name: p for p, (name, _, _) in enumerate(PROJ)}
+        rows = {name: n for name, _, n in PROJ}
+        for l in range(2):
+            for name, K, N, parts in FUSED:
+                mats = [synth.make_linear(synth.layer_seed(1000, l, seeds[q]), rows[q], K) for q in parts]
+                qw, s, b = (np.concatenate([m[i] for m in mats]) for i in range(3))
+                x = torch.from_numpy(synth.make_x(10 + len(ops), 1, K)).to(dev)
+                y = torch.empty((1, N), dtype=torch.float16, device=dev)
+                ops.append((x, *[torch.from_numpy(np.ascontiguousarray(t)).to(dev) for t in (qw.view(np.int32), s, b)],
+                            y, len(ops) > 0))
+        ws = w4.seq_workspace(ops)
+        for _ in range(iters):
+            w4.w4_gemv_seq(ops, workspace=ws)
     elif which == "gemm":
         x = torch.randn((PREFILL_M, 2048), device=dev).half()
         w = (0.05 * torch.randn((2048, 11008), device=dev)).half()
@@ -441,7 +457,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--profile", default=None, choices=["gemv", "gemm", "dequant", "lmhead"])
+    ap.add_argument("--profile", default=None, choices=["gemv", "gemm", "dequant", "lmhead", "seq"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
