@@ -250,7 +250,8 @@ def run_ours(args, rank, world):
         for l in range(LAYERS):
             for name, _, _, _ in FUSED:
                 qw, s, b, N, K = model.layers[l][name]
-                w4.w4_dequant_f16(qw, s, b, w16=scratch[l][name], stream=stream)
+                # distinct weights into distinct scratch buffers: independent calls
+                w4.w4_dequant_f16(qw, s, b, w16=scratch[l][name], stream=stream, flags=ov)
 
     def gemm_all():
         for l in range(LAYERS):

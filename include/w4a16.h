@@ -221,6 +221,17 @@ W4A16_API int w4_dequant_f16(const uint32_t *qweight, const uint16_t *scales,
                    const uint16_t *biases, uint16_t *w16, int N, int K, int group,
                    void *stream);
 
+/* w4_dequant_f16_ex - w4_dequant_f16 with flags (0 or W4A16_OVERLAP_PREVIOUS).
+ * For this call W4A16_OVERLAP_PREVIOUS states more than for the GEMVs: the
+ * call reads nothing the previous kernel on the stream writes and writes
+ * nothing it reads or writes (e.g. one of many dequantisations of distinct
+ * weights into distinct scratch buffers).  The kernel is then launched as a
+ * programmatic dependent without any wait and may run concurrently with the
+ * previous kernel. */
+W4A16_API int w4_dequant_f16_ex(const uint32_t *qweight, const uint16_t *scales,
+                                const uint16_t *biases, uint16_t *w16, int N, int K,
+                                int group, unsigned flags, void *stream);
+
 /*
  * f16_gemm - dense half GEMM for prefill, y = x16 * w16.
  *   ("The inference engine - Mojo 1.0 on Metal", "Crossing Mojo 1.0": the

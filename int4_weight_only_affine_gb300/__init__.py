@@ -52,12 +52,13 @@ def _load() -> ctypes.CDLL:
     L.lm_head_workspace_bytes.argtypes = [I, I, I]
     L.lm_head_workspace_bytes.restype = Z
     L.w4_dequant_f16.argtypes = [P, P, P, P, I, I, I, P]
+    L.w4_dequant_f16_ex.argtypes = [P, P, P, P, I, I, I, ctypes.c_uint, P]
     L.f16_gemm.argtypes = [P, P, P, I, I, I, P]
     L.w4a16_status_string.argtypes = [I]
     L.w4a16_status_string.restype = ctypes.c_char_p
     L.w4a16_device_status.argtypes = []
     for f in ("w4_gemv", "w4_gemv_ex", "w4_gemv_seq", "lm_head_argmax_topk", "lm_head_argmax_topk_ex",
-              "w4_dequant_f16", "f16_gemm", "w4a16_device_status"):
+              "w4_dequant_f16", "w4_dequant_f16_ex", "f16_gemm", "w4a16_device_status"):
         getattr(L, f).restype = I
     return L
 
@@ -201,15 +202,17 @@ def lm_head_argmax_topk(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Te
 
 
 def w4_dequant_f16(qweight: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
-                   w16: torch.Tensor | None = None, group: int = 64, stream=None) -> torch.Tensor:
-    """Transposed half scratch w16[K][N] = RNE(scale * q + bias)."""
+                   w16: torch.Tensor | None = None, group: int = 64, stream=None, flags: int = 0) -> torch.Tensor:
+    """Transposed half scratch w16[K][N] = RNE(scale * q + bias).  flags:
+    OVERLAP_PREVIOUS when this call shares no memory with the previous kernel
+    (it may then run concurrently with it)."""
     N, K = _weight_dims(qweight, scales, biases, group)
     if w16 is None:
         w16 = torch.empty((K, N), dtype=torch.float16, device=qweight.device)
     _check("w4_dequant_f16",
-           lib.w4_dequant_f16(_dev(qweight, "qweight", _QW), _dev(scales, "scales", _H),
-                              _dev(biases, "biases", _H), _dev(w16, "w16", _H), N, K, group,
-                              _stream(stream)))
+           lib.w4_dequant_f16_ex(_dev(qweight, "qweight", _QW), _dev(scales, "scales", _H),
+                                 _dev(biases, "biases", _H), _dev(w16, "w16", _H), N, K, group, flags,
+                                 _stream(stream)))
     return w16
 
 

@@ -107,7 +107,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy (TMA / bulk copy) accesses of the same bytes.
+// async-proxy (TMA / bulk copy) accesses of the same bytes (e.g. a TMA store
+// of a tile the threads just wrote).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -141,6 +142,25 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
             "r"(dst),
         "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
+}
+
+// 2-D tensor copy shared -> global, tracked by the issuing thread's bulk
+// async-group (commit with bulk_commit_group, wait with bulk_wait_*).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map), "r"(src),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Until at most N of this thread's committed groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Until at most N of this thread's committed groups are incomplete.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Contiguous bulk copy global -> shared (16-byte aligned, size multiple of 16).

@@ -9,11 +9,23 @@
 // exact subtraction of 1024) and one binary16 fused multiply-add rounds the
 // exact scale*q + bias once, to nearest even: the correctly rounded value.
 //
-// The kernel is HBM bound (0.5625 B read + 2 B written per weight).  A CTA
-// handles tiles of 64 rows x 64 k: threads read the codes of two adjacent rows
-// (16-byte row segments; the two warps covering a 32-byte group share it in L1), dequantise them as (row n, row n+1) half
-// pairs, transpose through padded shared memory, and write 128-byte segments
-// of 64 consecutive n for each k.
+// The kernels are HBM bound (0.5625 B read + 2 B written per weight).
+//
+// dequant_tma_kernel (N % 8 == 0): persistent CTAs, two per SM, walk tiles of
+// 64 rows x 256 k.  Thread 0 brings each tile's codes in with one TMA copy
+// (128-byte swizzle, four tiles in flight) and writes each finished tile out
+// with one TMA store of the transposed [256 k][64 n] binary16 block (two
+// output buffers, the store of one overlapping the conversion of the next).
+// Lane l converts rows 2l and 2l+1 as (row, row+1) half pairs over the
+// 32 k of its 16-byte chunk; the chunk index varies with the lane so that the
+// swizzled reads hit every bank, and every output row is 128 bytes, so the
+// pair stores are conflict-free.  Scales and biases are loaded into
+// registers two tiles ahead of their use.
+//
+// dequant_kernel (any N): tiles of 64 rows x 64 k: threads read the codes of
+// two adjacent rows, dequantise them as (row n, row n+1) half pairs,
+// transpose through padded shared memory, and write 128-byte segments of 64
+// consecutive n for each k.
 #include "common.cuh"
 
 namespace w4a16 {
@@ -84,23 +96,210 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+constexpr int kTmaRows = 64;                       // rows of W per tile (= n columns of w16)
+constexpr int kTmaK = 256;                         // k per tile (4 groups, 32 words per row)
+constexpr int kCodeBytes = kTmaRows * kTmaK / 2;   // 8 KB
+constexpr int kOutBytes = kTmaK * kTmaRows * 2;    // 32 KB
+constexpr int kCodeStages = 4;                    // code tiles in flight per CTA
+constexpr int kTmaSmem = kCodeStages * kCodeBytes + 2 * kOutBytes + 2 * 2 * kTmaRows * 4 * 2 + 8 * kCodeStages;
+
+__global__ void __launch_bounds__(kThreads, 2)
+    dequant_tma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_w,
+                       const uint16_t *__restrict__ sc, const uint16_t *__restrict__ bi, int N, int K, int tiles_n,
+                       int ntiles) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *sb = smem_raw + (base - raw);
+    constexpr int kOutOff = kCodeStages * kCodeBytes;
+    const uint32_t codes0 = base, out0 = base + kOutOff;
+    uint16_t *scl = reinterpret_cast<uint16_t *>(sb + kOutOff + 2 * kOutBytes);  // [2][64][4]
+    uint16_t *bia = scl + 2 * kTmaRows * 4;                                     // [2][64][4]
+    const uint32_t bar0 = base + kOutOff + 2 * kOutBytes + 2 * 2 * kTmaRows * 4 * 2;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int ng = K / kGroup;
+    const int G = gridDim.x;
+    // Launched with W4A16_OVERLAP_PREVIOUS the caller guarantees independence
+    // from the previous and the next kernel: release the next one at once
+    // (without the attribute this is ordinary stream order).
+    pdl_launch_dependents();
+    auto tile_n0 = [&](int t) { return (t % tiles_n) * kTmaRows; };
+    auto tile_k0 = [&](int t) { return (t / tiles_n) * kTmaK; };
+    // Thread tid stages the scale and bias of row tid/4, group tid%4 of a tile.
+    auto load_sb = [&](int t, uint16_t &s, uint16_t &b) {
+        const int n = min(tile_n0(t) + tid / 4, N - 1);
+        const int g = min(tile_k0(t) / kGroup + (tid & 3), ng - 1);
+        s = ld_nc_u16(sc + (size_t)n * ng + g);
+        b = ld_nc_u16(bi + (size_t)n * ng + g);
+    };
+
+    if (tid == 0) {
+        for (int i = 0; i < kCodeStages; ++i) mbar_init(bar0 + 8 * i, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int i = 0; i < kCodeStages; ++i) {
+            const int t = blockIdx.x + i * G;
+            if (t < ntiles) {
+                mbar_expect_tx(bar0 + 8 * i, kCodeBytes);
+                tma_load_2d(codes0 + i * kCodeBytes, &map_q, tile_k0(t) / 8, tile_n0(t), bar0 + 8 * i);
+            }
+        }
+    }
+    // Scales: tile 0's into shared memory now; tile i+1's are in registers
+    // (loaded two tiles ahead) and reach shared memory at the end of tile i.
+    uint16_t ps0 = 0, pb0 = 0, ps1 = 0, pb1 = 0;  // register sets for even / odd tiles
+    if (blockIdx.x < ntiles) {
+        uint16_t s, b;
+        load_sb(blockIdx.x, s, b);
+        scl[tid] = s;
+        bia[tid] = b;
+    }
+    if (blockIdx.x + G < ntiles) load_sb(blockIdx.x + G, ps1, pb1);
+    __syncthreads();
+
+    // Lane l: rows 2l, 2l+1; 16-byte chunk c of the 128-byte row (k = 32c..32c+31).
+    const int c = (warp + (lane >> 2)) & 7;
+    const int rowa = 2 * lane, rowb = 2 * lane + 1;
+    const uint32_t offa = rowa * 128 + ((c ^ (rowa & 7)) << 4);
+    const uint32_t offb = rowb * 128 + ((c ^ (rowb & 7)) << 4);
+    const __half2 k1024 = __float2half2_rn(1024.f);
+    bool ok = true;
+    int waited = 0;  // tiles whose codes this thread has waited for
+    for (int i = 0;; ++i) {
+        const int t = blockIdx.x + i * G;
+        if (t >= ntiles) break;
+        const int st = i & 1;              // output and scale buffer
+        const int cst = i % kCodeStages;   // code buffer
+        const int tn = t + G;
+        if (t + 2 * G < ntiles) {  // scales two tiles ahead, into this tile's register set
+            if (st == 0)
+                load_sb(t + 2 * G, ps0, pb0);
+            else
+                load_sb(t + 2 * G, ps1, pb1);
+        }
+        if (ok) {
+            ok = mbar_wait(bar0 + 8 * cst, (i / kCodeStages) & 1);
+            if (ok) waited = i + 1;
+        }
+        if (tid == 0) bulk_wait_group_read<1>();  // the store that last used this output buffer has read it
+        __syncthreads();
+        if (ok) {
+            const uint8_t *cs = sb + cst * kCodeBytes;
+            const uint4 A = *reinterpret_cast<const uint4 *>(cs + offa);
+            const uint4 B = *reinterpret_cast<const uint4 *>(cs + offb);
+            const int gl = c >> 1;  // group of the chunk within the tile
+            const __half2 s2 = __halves2half2(__ushort_as_half(scl[st * 256 + rowa * 4 + gl]),
+                                              __ushort_as_half(scl[st * 256 + rowb * 4 + gl]));
+            const __half2 b2 = __halves2half2(__ushort_as_half(bia[st * 256 + rowa * 4 + gl]),
+                                              __ushort_as_half(bia[st * 256 + rowb * 4 + gl]));
+            uint32_t *out = reinterpret_cast<uint32_t *>(sb + kOutOff + st * kOutBytes);
+            const uint32_t wa[4] = {A.x, A.y, A.z, A.w}, wb[4] = {B.x, B.y, B.z, B.w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const uint32_t lo = __byte_perm(wa[w], wb[w], 0x5410);  // codes 0..3 of (row a, row b)
+                const uint32_t hi = __byte_perm(wa[w], wb[w], 0x7632);  // codes 4..7
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t src = e < 4 ? lo : hi;
+                    const uint32_t v = ((src >> (4 * (e & 3))) & 0x000F000Fu) | 0x64006400u;  // 1024 + q
+                    const __half2 q2 = __hsub2(*reinterpret_cast<const __half2 *>(&v), k1024);  // exact q
+                    const __half2 w2 = __hfma2(q2, s2, b2);                                      // one rounding
+                    const int k = 32 * c + 8 * w + e;
+                    out[k * (kTmaRows / 2) + lane] = *reinterpret_cast<const uint32_t *>(&w2);
+                }
+            }
+        }
+        fence_proxy_async_smem();  // the tile's generic writes before the TMA store reads them
+        __syncthreads();
+        if (tid == 0) {
+            if (ok) {
+                tma_store_2d(&map_w, out0 + st * kOutBytes, tile_n0(t), tile_k0(t));
+                bulk_commit_group();
+            }
+            const int t2 = t + kCodeStages * G;  // refill this code buffer
+            if (ok && t2 < ntiles) {
+                mbar_expect_tx(bar0 + 8 * cst, kCodeBytes);
+                tma_load_2d(codes0 + cst * kCodeBytes, &map_q, tile_k0(t2) / 8, tile_n0(t2), bar0 + 8 * cst);
+            }
+        }
+        if (tn < ntiles) {
+            scl[(st ^ 1) * 256 + tid] = st ? ps0 : ps1;
+            bia[(st ^ 1) * 256 + tid] = st ? pb0 : pb1;
+        }
+    }
+    if (tid == 0) {
+        // After an expired wait: the code copies issued for tiles not waited
+        // for still land before the CTA exits (bounded waits).
+        for (int i = waited; i < waited + kCodeStages; ++i)
+            if (blockIdx.x + i * G < ntiles) mbar_wait(bar0 + 8 * (i % kCodeStages), (i / kCodeStages) & 1);
+        bulk_wait_group<0>();  // every store has landed before the CTA exits
+    }
+}
+
 }  // namespace
 }  // namespace w4a16
 
 using namespace w4a16;
 
-extern "C" int w4_dequant_f16(const uint32_t *qweight, const uint16_t *scales, const uint16_t *biases,
-                              uint16_t *w16, int N, int K, int group, void *stream) {
+static int dequant_impl(const uint32_t *qweight, const uint16_t *scales, const uint16_t *biases, uint16_t *w16,
+                        int N, int K, int group, unsigned flags, void *stream) {
     if (!qweight || !scales || !biases || !w16) return W4_ERR_NULL;
     if (group != kGroup) return W4_ERR_GROUP;
     if (N < 1 || K < kGroup || K % kGroup != 0) return W4_ERR_SHAPE;
     if (!aligned16(qweight) || !aligned16(scales) || !aligned16(biases) || !aligned16(w16))
         return W4_ERR_ALIGN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (N % 8 == 0) {
+        // w16 rows are 16-byte multiples: tensor copies both ways.
+        CUtensorMap mq, mw;
+        const uint64_t KW = (uint64_t)K / 8;
+        if (!make_map_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, KW, (uint64_t)N, KW * 4, 32, kTmaRows,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT16, w16, (uint64_t)N, (uint64_t)K, (uint64_t)N * 2,
+                         kTmaRows, kTmaK, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return W4_ERR_DEVICE;
+        const int tiles_n = (N + kTmaRows - 1) / kTmaRows;
+        const long long ntiles = (long long)tiles_n * ((K + kTmaK - 1) / kTmaK);
+        if (ntiles > 0x7fffffffLL) return W4_ERR_SHAPE;
+        static bool attr_set[64] = {false};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+            if (cudaFuncSetAttribute(dequant_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmem + 1024) !=
+                cudaSuccess)
+                return W4_ERR_LAUNCH;
+            attr_set[dev] = true;
+        }
+        long long grid = (long long)sm_count() * 2;
+        if (grid > ntiles) grid = ntiles;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kTmaSmem + 1024;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = (flags & W4A16_OVERLAP_PREVIOUS) ? 1 : 0;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, dequant_tma_kernel, mq, mw, scales, biases, N, K, tiles_n,
+                                                 (int)ntiles);
+        return e == cudaSuccess ? W4A16_OK : W4_ERR_LAUNCH;
+    }
     const int tiles_n = (N + kTileN - 1) / kTileN;
     const long long ntiles = (long long)tiles_n * (K / kGroup);
     long long grid = (long long)sm_count() * 8;
     if (grid > ntiles) grid = ntiles;
-    dequant_kernel<<<(unsigned)grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        qweight, scales, biases, w16, N, K, ntiles, tiles_n);
+    dequant_kernel<<<(unsigned)grid, kThreads, 0, st>>>(qweight, scales, biases, w16, N, K, ntiles, tiles_n);
     return launch_status();
+}
+
+extern "C" int w4_dequant_f16(const uint32_t *qweight, const uint16_t *scales, const uint16_t *biases,
+                              uint16_t *w16, int N, int K, int group, void *stream) {
+    return dequant_impl(qweight, scales, biases, w16, N, K, group, 0u, stream);
+}
+
+extern "C" int w4_dequant_f16_ex(const uint32_t *qweight, const uint16_t *scales, const uint16_t *biases,
+                                 uint16_t *w16, int N, int K, int group, unsigned flags, void *stream) {
+    if (flags & ~(unsigned)W4A16_OVERLAP_PREVIOUS) return W4_ERR_SHAPE;
+    return dequant_impl(qweight, scales, biases, w16, N, K, group, flags, stream);
 }

@@ -20,7 +20,11 @@ def _dq(w4, qw, s, b):
     return w4.w4_dequant_f16(to_dev(qw), to_dev(s), to_dev(b)).cpu().numpy().view(np.uint16)
 
 
-@pytest.mark.parametrize("N,K", [(1000, 896), (257, 192), (1, 64), (64, 64), (130, 128), (8, 640), (3, 1024)])
+# N % 8 == 0 takes the tensor-copy kernel (tiles of 64 rows x 256 k, ragged in
+# both directions here, several tiles per CTA for the largest), other N the
+# shared-memory transpose kernel.
+@pytest.mark.parametrize("N,K", [(1000, 896), (257, 192), (1, 64), (64, 64), (130, 128), (8, 640), (3, 1024),
+                                 (4104, 2240), (136, 64)])
 def test_dequant_bit_exact_small(w4, N, K):
     qw, s, b = synth.make_linear(10 + N + K, N, K)
     got = _dq(w4, qw, s, b)
@@ -57,3 +61,21 @@ def test_dequant_full_size_sampled(w4, K, N):
     rows = np.unique(np.concatenate([[0, N - 1, N // 2], g.integers(0, N, size=40)])).astype(np.int32)
     want = oracle.dequant_f16_rows(qw, s, b, K, rows)
     assert np.array_equal(got[:, rows].T, want)
+
+
+def test_dequant_independent_calls_overlap(w4):
+    """Back-to-back calls into distinct scratch buffers with OVERLAP_PREVIOUS
+    (each may run concurrently with the previous one) stay bit-exact."""
+    import torch
+    shapes = [(2560, 2048), (2048, 2048), (4104, 2240), (2048, 1024), (1000, 896)]
+    mats = [synth.make_linear(7000 + i, N, K) for i, (N, K) in enumerate(shapes)]
+    dev = [tuple(to_dev(a) for a in m) for m in mats]
+    outs = [w4.w4_dequant_f16(*d, flags=w4.OVERLAP_PREVIOUS) for d in dev]
+    torch.cuda.synchronize()
+    for (N, K), (qw, s, b), o in zip(shapes, mats, outs):
+        if N * K <= 4 * 1024 * 1024:
+            assert np.array_equal(o.cpu().numpy().view(np.uint16), oracle.dequant_f16_t(qw, s, b, N, K))
+        else:
+            rows = np.array([0, 1, N // 3, N - 1], dtype=np.int32)
+            want = oracle.dequant_f16_rows(qw, s, b, K, rows)
+            assert np.array_equal(o.cpu().numpy().view(np.uint16)[:, rows].T, want)
