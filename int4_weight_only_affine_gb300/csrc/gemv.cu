@@ -985,30 +985,36 @@ int max_active_clusters(const void *kern, int C, size_t smem, int fallback) {
 }
 
 // Lays out a launch with C CTAs per cluster; false if it does not fit.
+// The largest layout within the per-CTA share of shared memory (false if
+// none fits).
+bool fit_layout(StreamPlan &p, bool lmhead, int per_sm, int tpc, int slice) {
+    const size_t per_cta = (size_t)kMaxSmem / per_sm;
+    for (size_t budget = per_cta; budget >= 16 * 1024; budget -= 8 * 1024) {
+        layout_stream(p, p.a.M, lmhead, budget - (per_sm == 2 ? 24 * 1024 : 0), tpc, slice);
+        if (p.smem <= per_cta) return true;
+    }
+    return false;
+}
+
 bool plan_with_cluster(StreamPlan &p, int C, int slots, int per_sm, bool lmhead) {
     StreamArgs &a = p.a;
     a.C = C;
     int ncl = min(a.tiles, max(1, slots / C));
+    const int slice = min(a.ng, 8 * ((a.units + C - 1) / C));
+    if (!fit_layout(p, lmhead, per_sm, (a.tiles + ncl - 1) / ncl, slice)) return false;
     if (C > 1) {
-        // Size the shared memory first (it does not depend on the cluster
-        // count beyond tiles per cluster), then keep every cluster resident.
-        StreamPlan probe = p;
-        const int tpc0 = (a.tiles + ncl - 1) / ncl;
-        const int slice0 = min(a.ng, 8 * ((a.units + C - 1) / C));
-        layout_stream(probe, a.M, lmhead, (size_t)kMaxSmem / per_sm - (per_sm == 2 ? 24 * 1024 : 0), tpc0,
-                      slice0);
-        const int act = max_active_clusters(stream_kernel_ptr(a.M, lmhead), C, probe.smem, ncl);
-        ncl = min(ncl, max(1, act));
+        // Keep every cluster resident: cap the cluster count by the occupancy
+        // of the layout actually launched (fewer clusters mean more tiles per
+        // cluster and possibly a larger layout, so check again).
+        for (int iter = 0; iter < 3; ++iter) {
+            const int act = max_active_clusters(stream_kernel_ptr(a.M, lmhead), C, p.smem, ncl);
+            if (act >= ncl) break;
+            ncl = max(1, act);
+            if (!fit_layout(p, lmhead, per_sm, (a.tiles + ncl - 1) / ncl, slice)) return false;
+        }
     }
     p.grid = ncl * C;
-    const int tpc = (a.tiles + ncl - 1) / ncl;
-    const int slice = min(a.ng, 8 * ((a.units + C - 1) / C));
-    const size_t per_cta = (size_t)kMaxSmem / per_sm;
-    for (size_t budget = per_cta; budget >= 16 * 1024; budget -= 8 * 1024) {
-        layout_stream(p, a.M, lmhead, budget - (per_sm == 2 ? 24 * 1024 : 0), tpc, slice);
-        if (p.smem <= per_cta) return true;
-    }
-    return false;
+    return true;
 }
 
 bool plan_stream(StreamPlan &p, int M, int N, int K, bool lmhead, int k) {
