@@ -34,7 +34,10 @@ def _entries(M, N, n=1500, seed=0):
     g = np.random.default_rng(seed)
     ms = g.integers(0, M, size=n)
     ns = g.integers(0, N, size=n)
-    edge_m = [0, M - 1, min(M - 1, 127), min(M - 1, 128)]
+    # rows at the edges of the 128- and 256-row tiles, including the first row
+    # of a ragged last tile
+    split = (M // 256) * 256
+    edge_m = [0, M - 1, min(M - 1, 127), min(M - 1, 128), max(0, split - 1), min(M - 1, split)]
     edge_n = [0, N - 1, min(N - 1, 255), min(N - 1, 256)]
     ms = np.concatenate([ms, np.repeat(edge_m, len(edge_n))])
     ns = np.concatenate([ns, np.tile(edge_n, len(edge_m))])
@@ -77,3 +80,25 @@ def test_dequant_then_gemm_equals_gemv(w4):
     yv = w4.w4_gemv(tx, tq, ts, tb).cpu().numpy()
     yo, ad = oracle.gemv(x, qw, s, b, N, K, threads=8)
     assert within_tol(yg, yo, ad)[0] and within_tol(yv, yo, ad)[0]
+
+
+def test_gemm_row_tail_keeps_stream_order(w4):
+    """A GEMM reading the previous GEMM's output right after it (no
+    synchronisation, M = 1570 with a ragged 256-row tile) sees all of it:
+    bit-identical to the same chain with a synchronisation in between (the
+    kernels are deterministic)."""
+    import torch
+    M, K, N = 1570, 1024, 1024
+    x = to_dev(synth.make_half_matrix(31, M, K))
+    w1 = to_dev(synth.make_half_matrix(32, K, N, std=0.05))
+    w2 = to_dev(synth.make_half_matrix(33, N, N, std=0.05))
+    y1 = w4.f16_gemm(x, w1)
+    y2 = w4.f16_gemm(y1, w2)
+    torch.cuda.synchronize()
+    z1 = w4.f16_gemm(x, w1)
+    torch.cuda.synchronize()
+    z2 = w4.f16_gemm(z1, w2)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, z1)
+    assert torch.equal(y2, z2)
+    assert w4.device_status() == 0
