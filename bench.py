@@ -363,11 +363,13 @@ def barrier(world):
 
 
 def max_over_ranks(v, world):
+    """The maximum of v over the ranks (NCCL needs a device tensor, gloo a host one)."""
     if world <= 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
