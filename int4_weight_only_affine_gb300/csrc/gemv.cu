@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
         const int xoff = lane_xoff(M, lg, lt), xd1 = lane_xd1(M, lg);
         const bool vec = (ng & 3) == 0;
         pdl_wait();
-        stage_activations(a.x, M, a.K, gs0, ngl, xf, xsum, tid, kConsumers);
+        stage_activations<M1 ? 2 : 4>(a.x, M, a.K, gs0, ngl, xf, xsum, tid, kConsumers);
         consumer_sync();
         int s = 0;
         uint32_t ph = 0;

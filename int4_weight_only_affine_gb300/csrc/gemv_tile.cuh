@@ -127,19 +127,18 @@ __device__ __forceinline__ float item_store(uint4 lo, uint4 hi, int gl, int c, i
 // `xt` of the activations written earlier in the same launch, waiting for
 // the words of tag `tag`; else read x (coherent: bypassing the non-coherent
 // read-only path, for activations written earlier in the same kernel).
-// A thread takes items it and it + nthreads together, so both loads are in
-// flight at once.
-template <bool TAGGED>
+// A thread takes kB items (it, it + nthreads, ...) together, so their loads
+// are in flight at once.
+template <bool TAGGED, int kB = 2>
 __device__ void stage_activations_t(const uint16_t *__restrict__ x, const uint32_t *xt, uint32_t tag, int M, int K,
                                     int g0, int ngl, uint32_t *xf, float *xsum, int tid, int nthreads, bool coherent,
                                     volatile int *abort) {
     const int items = ngl * M * 4;
-    for (int base = 0; base < items; base += 2 * nthreads) {
-        const int ia = base + tid, ib = base + nthreads + tid;
-        uint4 lo[2], hi[2];
+    for (int base = 0; base < items; base += kB * nthreads) {
+        uint4 lo[kB], hi[kB];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int it = u ? ib : ia;
+        for (int u = 0; u < kB; ++u) {
+            const int it = base + u * nthreads + tid;
             if (it < items) {
                 const int t = it & 3, c = (it >> 2) % M, gl = (it >> 2) / M;
                 item_load<TAGGED>(x, xt, tag, (size_t)c * K + (size_t)(g0 + gl) * kGroup + 16 * t, coherent, abort,
@@ -147,8 +146,8 @@ __device__ void stage_activations_t(const uint16_t *__restrict__ x, const uint32
             }
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int it = u ? ib : ia;
+        for (int u = 0; u < kB; ++u) {
+            const int it = base + u * nthreads + tid;
             float part = 0.f;
             if (it < items) part = item_store(lo[u], hi[u], (it >> 2) / M, (it >> 2) % M, it & 3, M, xf);
             part += __shfl_xor_sync(0xffffffffu, part, 1);
@@ -158,10 +157,11 @@ __device__ void stage_activations_t(const uint16_t *__restrict__ x, const uint32
     }
 }
 
+template <int kB = 2>
 __device__ __forceinline__ void stage_activations(const uint16_t *__restrict__ x, int M, int K, int g0, int ngl,
                                                   uint32_t *xf, float *xsum, int tid, int nthreads,
                                                   bool coherent = false) {
-    stage_activations_t<false>(x, nullptr, 0u, M, K, g0, ngl, xf, xsum, tid, nthreads, coherent, nullptr);
+    stage_activations_t<false, kB>(x, nullptr, 0u, M, K, g0, ngl, xf, xsum, tid, nthreads, coherent, nullptr);
 }
 
 template <int NT>
