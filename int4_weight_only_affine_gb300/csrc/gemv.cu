@@ -904,7 +904,10 @@ struct StreamPlan {
     size_t smem;
 };
 
-bool layout_stream(StreamPlan &p, int M, bool lmhead, size_t ring_budget, int tpc, int slice_groups) {
+// force_defer: keep every warp's partial of every tile (no per-tile barrier)
+// even when that takes more than 32 KB.
+bool layout_stream(StreamPlan &p, int M, bool lmhead, size_t ring_budget, int tpc, int slice_groups,
+                   bool force_defer = false) {
     StreamArgs &a = p.a;
     const int ng = a.ng;
     const int wbox = min(kChunkGroups, slice_groups + kBoxGroups - 1) / kBoxGroups;
@@ -927,7 +930,7 @@ bool layout_stream(StreamPlan &p, int M, bool lmhead, size_t ring_budget, int tp
     off = align_up(off + (size_t)slice_groups * M * 4, 16);
     a.off_red = (uint32_t)off;
     const size_t red_all = (size_t)tpc * kConsumerWarps * kTileRows * M * 4;
-    a.defer = red_all <= 32 * 1024 ? 1 : 0;
+    a.defer = (force_defer || red_all <= 32 * 1024) ? 1 : 0;
     off = align_up(off + (a.defer ? red_all : (size_t)2 * kConsumerWarps * kTileRows * M * 4), 16);
     a.off_res = (uint32_t)off;
     if (lmhead || a.C > 1) off = align_up(off + (size_t)tpc * kTileRows * M * 4, 16);
@@ -989,6 +992,15 @@ int max_active_clusters(const void *kern, int C, size_t smem, int fallback) {
 // none fits).
 bool fit_layout(StreamPlan &p, bool lmhead, int per_sm, int tpc, int slice) {
     const size_t per_cta = (size_t)kMaxSmem / per_sm;
+    // First choice: partials of all tiles kept (no per-tile barrier) with a
+    // ring of at least 4 stages; else the largest layout that fits.
+    for (size_t budget = per_cta; budget >= 16 * 1024; budget -= 8 * 1024) {
+        layout_stream(p, p.a.M, lmhead, budget - (per_sm == 2 ? 24 * 1024 : 0), tpc, slice, true);
+        if (p.smem <= per_cta) {
+            if (p.a.stages >= 4) return true;
+            break;
+        }
+    }
     for (size_t budget = per_cta; budget >= 16 * 1024; budget -= 8 * 1024) {
         layout_stream(p, p.a.M, lmhead, budget - (per_sm == 2 ? 24 * 1024 : 0), tpc, slice);
         if (p.smem <= per_cta) return true;
