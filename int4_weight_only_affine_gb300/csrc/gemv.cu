@@ -445,14 +445,19 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
     const int rows = min(N, t1 * kTileRows) - n0;
     uint64_t(*lists)[64] = reinterpret_cast<uint64_t(*)[64]>(sb);  // the ring is free now
     constexpr int kWarps = kThreads / 32;
+    if (a.k == 1) {
+        // Greedy selection: warp w takes activation rows w, w + 9, ...
+        for (int m = warp; m < M; m += kWarps) {
+            uint64_t best = 0ull;
+            for (int i = lane; i < rows; i += 32) best = umax64(best, make_key(res[i * M + m], n0 + i));
+            best = shfl_max_u64(best);
+            if (lane == 0) a.ws[(size_t)m * gridDim.x + blockIdx.x] = best;
+        }
+        return;
+    }
     for (int m = 0; m < M; ++m) {
         uint64_t *out = a.ws + ((size_t)m * gridDim.x + blockIdx.x) * a.k;
-        if (a.k == 1) {
-            uint64_t best = 0ull;
-            for (int i = tid; i < rows; i += kThreads) best = umax64(best, make_key(res[i * M + m], n0 + i));
-            best = block_max_u64(best, reinterpret_cast<uint64_t *>(sb));
-            if (tid == 0) out[0] = best;
-        } else {
+        {
             // Each warp keeps the best 64 of its 64-row chunks; a tree merges them.
             Key2 run{0ull, 0ull};
             for (int c0 = warp * 64; c0 < rows; c0 += kWarps * 64) {
