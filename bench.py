@@ -254,9 +254,13 @@ def run_ours(args, rank, world):
                 w4.w4_dequant_f16(qw, s, b, w16=scratch[l][name], stream=stream, flags=ov)
 
     def gemm_all():
+        first = True
         for l in range(LAYERS):
             for name, _, _, _ in FUSED:
-                w4.f16_gemm(xp[SRC[name]], scratch[l][name], y=yp[name], stream=stream)
+                # After the first GEMM every scratch is long complete: fetch the
+                # weights early and wait for the previous GEMM only for x and y.
+                w4.f16_gemm(xp[SRC[name]], scratch[l][name], y=yp[name], stream=stream, flags=0 if first else ov)
+                first = False
 
     parts = {
         "dequant": dequant_all,

@@ -246,6 +246,15 @@ W4A16_API int w4_dequant_f16_ex(const uint32_t *qweight, const uint16_t *scales,
 W4A16_API int f16_gemm(const uint16_t *x16, const uint16_t *w16, uint16_t *y,
              int M, int N, int K, void *stream);
 
+/* f16_gemm_ex - f16_gemm with flags (0 or W4A16_OVERLAP_PREVIOUS).  With the
+ * flag the kernel is a programmatic dependent of the previous kernel on the
+ * stream: it sets up and copies the w16 tiles of its first stages at once and
+ * waits for the previous kernel before it reads x16 or writes y.  w16 must
+ * therefore be complete when the call is issued (not written by the previous
+ * kernel, nor by any kernel still running beside it). */
+W4A16_API int f16_gemm_ex(const uint16_t *x16, const uint16_t *w16, uint16_t *y, int M, int N,
+                          int K, unsigned flags, void *stream);
+
 /* Human-readable name of a status code (static string). */
 W4A16_API const char *w4a16_status_string(int status);
 

@@ -54,11 +54,12 @@ def _load() -> ctypes.CDLL:
     L.w4_dequant_f16.argtypes = [P, P, P, P, I, I, I, P]
     L.w4_dequant_f16_ex.argtypes = [P, P, P, P, I, I, I, ctypes.c_uint, P]
     L.f16_gemm.argtypes = [P, P, P, I, I, I, P]
+    L.f16_gemm_ex.argtypes = [P, P, P, I, I, I, ctypes.c_uint, P]
     L.w4a16_status_string.argtypes = [I]
     L.w4a16_status_string.restype = ctypes.c_char_p
     L.w4a16_device_status.argtypes = []
     for f in ("w4_gemv", "w4_gemv_ex", "w4_gemv_seq", "lm_head_argmax_topk", "lm_head_argmax_topk_ex",
-              "w4_dequant_f16", "w4_dequant_f16_ex", "f16_gemm", "w4a16_device_status"):
+              "w4_dequant_f16", "w4_dequant_f16_ex", "f16_gemm", "f16_gemm_ex", "w4a16_device_status"):
         getattr(L, f).restype = I
     return L
 
@@ -217,16 +218,19 @@ def w4_dequant_f16(qweight: torch.Tensor, scales: torch.Tensor, biases: torch.Te
 
 
 def f16_gemm(x16: torch.Tensor, w16: torch.Tensor, y: torch.Tensor | None = None,
-             stream=None) -> torch.Tensor:
-    """y[M][N] = x16[M][K] @ w16[K][N] (fp32 accumulation, half output)."""
+             stream=None, flags: int = 0) -> torch.Tensor:
+    """y[M][N] = x16[M][K] @ w16[K][N] (fp32 accumulation, half output).  flags:
+    OVERLAP_PREVIOUS when w16 is complete before the previous kernel on the
+    stream started (the kernel then fetches it early and waits only before x16
+    and y)."""
     M, K = x16.shape
     K2, N = w16.shape
     if K2 != K:
         raise ValueError("inner dimensions differ")
     if y is None:
         y = torch.empty((M, N), dtype=torch.float16, device=x16.device)
-    _check("f16_gemm", lib.f16_gemm(_dev(x16, "x16", _H), _dev(w16, "w16", _H), _dev(y, "y", _H),
-                                    M, N, K, _stream(stream)))
+    _check("f16_gemm", lib.f16_gemm_ex(_dev(x16, "x16", _H), _dev(w16, "w16", _H), _dev(y, "y", _H),
+                                       M, N, K, flags, _stream(stream)))
     return y
 
 

@@ -91,9 +91,14 @@ __device__ __forceinline__ uint32_t pack_half2(uint32_t a, uint32_t b) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// pdl: launched as a programmatic dependent.  The kernel releases the next
+// one at once, sets up and copies the weight (B) tiles of its first stages
+// before waiting for the previous kernel; the activation (A) copies, and so
+// every read of data the previous kernel may write and every output store,
+// come after the wait.
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-                uint16_t *__restrict__ y, int M, int N, int K) {
+                uint16_t *__restrict__ y, int M, int N, int K, int pdl) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms.
     const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
@@ -107,6 +112,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t done_bar = bar0 + 8u * (2 * STAGES + 4);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 5));
 
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
     const int ntiles = tiles_m * tiles_n;
@@ -143,9 +149,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t issued_ph = 0, issued_any = 0;
             int it = 0;
             bool ok = true;
+            int pre = 0;  // first-tile stages whose B copies precede the dependency wait
+            if (pdl && blockIdx.x < ntiles) {
+                const int m0 = (blockIdx.x % tiles_m) * BM, n0 = (blockIdx.x / tiles_m) * BN;
+                pre = nk < STAGES ? nk : STAGES;
+                for (int kb = 0; kb < pre; ++kb) {  // fresh slots: no empty wait
+                    mbar_expect_tx(full_bar(kb), STAGE_BYTES);
+                    const uint32_t sb = base + kb * STAGE_BYTES + A_TILE;
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j)
+                        tma_load_2d(sb + j * B_BOX, &tma_b, n0 + 64 * j, kb * BK, full_bar(kb));
+                    issued_any |= 1u << kb;
+                }
+                pdl_wait();
+                for (int kb = 0; kb < pre; ++kb) tma_load_2d(base + kb * STAGE_BYTES, &tma_a, kb * BK, m0, full_bar(kb));
+                it = pre;
+            } else if (pdl) {
+                pdl_wait();
+            }
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
                 const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * BN;
-                for (int kb = 0; kb < nk; ++kb, ++it) {
+                for (int kb = (t == (int)blockIdx.x) ? pre : 0; kb < nk; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1;
                     if (!mbar_wait(empty_bar(s), ph ^ 1)) {
@@ -313,9 +337,11 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// pdl: as for gemm_kernel (each CTA of the pair copies its B halves of the
+// first stages before the dependency wait and its A halves after it).
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm2_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-                 uint16_t *__restrict__ y, int M, int N, int K) {
+                 uint16_t *__restrict__ y, int M, int N, int K, int pdl) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -328,6 +354,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t done_bar = bar0 + 8u * (2 * ST2 + 4);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + ST2 * STAGE2_BYTES + 8 * (2 * ST2 + 5));
 
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
@@ -368,10 +395,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t issued_ph = 0, issued_any = 0;
             int it = 0;
             bool ok = true;
+            int pre = 0;  // first-tile stages whose B copies precede the dependency wait
+            if (pdl && pair < ntiles) {
+                const int m0 = (pair % tiles_m) * 256 + 128 * (int)rank;
+                const int n0 = (pair / tiles_m) * BN + 128 * (int)rank;
+                pre = nk < ST2 ? nk : ST2;
+                for (int kb = 0; kb < pre; ++kb) {  // fresh slots: no empty wait
+                    if (rank == 0) mbar_expect_tx(full_bar(kb), 2 * STAGE2_BYTES);
+                    const uint32_t lbar = map_to_rank(full_bar(kb), 0);
+                    const uint32_t sb = base + kb * STAGE2_BYTES + A2_TILE;
+                    tma_load_2d_pair(sb, &tma_b, n0, kb * BK, lbar);
+                    tma_load_2d_pair(sb + B_BOX, &tma_b, n0 + 64, kb * BK, lbar);
+                    issued_any |= 1u << kb;
+                }
+                pdl_wait();
+                for (int kb = 0; kb < pre; ++kb)
+                    tma_load_2d_pair(base + kb * STAGE2_BYTES, &tma_a, kb * BK, m0, map_to_rank(full_bar(kb), 0));
+                it = pre;
+            } else if (pdl) {
+                pdl_wait();
+            }
             for (int t = pair; t < ntiles && ok; t += npairs) {
                 const int m0 = (t % tiles_m) * 256 + 128 * (int)rank;
                 const int n0 = (t / tiles_m) * BN + 128 * (int)rank;
-                for (int kb = 0; kb < nk; ++kb, ++it) {
+                for (int kb = (t == pair) ? pre : 0; kb < nk; ++kb, ++it) {
                     const int s = it % ST2;
                     const uint32_t ph = (it / ST2) & 1;
                     if (!mbar_wait(empty_bar(s), ph ^ 1)) {
@@ -492,8 +539,8 @@ bool make_map(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer, u
 
 using namespace w4a16;
 
-extern "C" int f16_gemm(const uint16_t *x16, const uint16_t *w16, uint16_t *y, int M, int N, int K,
-                        void *stream) {
+static int gemm_impl(const uint16_t *x16, const uint16_t *w16, uint16_t *y, int M, int N, int K, unsigned flags,
+                     void *stream) {
     if (!x16 || !w16 || !y) return W4_ERR_NULL;
     if (M < 1 || N < 8 || K < 8 || N % 8 != 0 || K % 8 != 0) return W4_ERR_SHAPE;
     if (!aligned16(x16) || !aligned16(w16) || !aligned16(y)) return W4_ERR_ALIGN;
@@ -530,21 +577,46 @@ extern "C" int f16_gemm(const uint16_t *x16, const uint16_t *w16, uint16_t *y, i
         cfg.blockDim = dim3(NUM_THREADS, 1, 1);
         cfg.dynamicSmemBytes = SMEM2_BYTES;
         cfg.stream = st;
-        cudaLaunchAttribute attr[1];
+        const int pdl = (flags & W4A16_OVERLAP_PREVIOUS) ? 1 : 0;
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm2_kernel, ta2, tb2, y, M, N, K);
+        cfg.numAttrs = pdl ? 2 : 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm2_kernel, ta2, tb2, y, M, N, K, pdl);
         return e == cudaSuccess ? W4A16_OK : W4_ERR_LAUNCH;
     }
     const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     int grid = sm_count();
     if (grid > tiles) grid = tiles;
-    gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ta, tb, y, M, N, K);
-    return launch_status();
+    const int pdl = (flags & W4A16_OVERLAP_PREVIOUS) ? 1 : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel, ta, tb, y, M, N, K, pdl);
+    return e == cudaSuccess ? W4A16_OK : W4_ERR_LAUNCH;
+}
+
+extern "C" int f16_gemm(const uint16_t *x16, const uint16_t *w16, uint16_t *y, int M, int N, int K,
+                        void *stream) {
+    return gemm_impl(x16, w16, y, M, N, K, 0u, stream);
+}
+
+extern "C" int f16_gemm_ex(const uint16_t *x16, const uint16_t *w16, uint16_t *y, int M, int N, int K,
+                           unsigned flags, void *stream) {
+    if (flags & ~(unsigned)W4A16_OVERLAP_PREVIOUS) return W4_ERR_SHAPE;
+    return gemm_impl(x16, w16, y, M, N, K, flags, stream);
 }
 
 namespace w4a16 {

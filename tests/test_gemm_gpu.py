@@ -102,3 +102,30 @@ def test_gemm_row_tail_keeps_stream_order(w4):
     assert torch.equal(y1, z1)
     assert torch.equal(y2, z2)
     assert w4.device_status() == 0
+
+
+@pytest.mark.parametrize("M", [100, 1570])
+def test_gemm_overlap_flag_keeps_dependencies(w4, M):
+    """With OVERLAP_PREVIOUS a GEMM fetches its weights early but reads x and
+    writes y only after the previous kernel: a read-after-write chain (x is
+    the previous output) and a write-after-read (y is the previous kernel's
+    input) give the same bits as with synchronisations in between."""
+    import torch
+    K, N = 1024, 1024
+    x = to_dev(synth.make_half_matrix(41, M, K))
+    w1 = to_dev(synth.make_half_matrix(42, K, N, std=0.05))
+    w2 = to_dev(synth.make_half_matrix(43, N, N, std=0.05))
+    ov = w4.OVERLAP_PREVIOUS
+    # reference, synchronised
+    r1 = w4.f16_gemm(x, w1); torch.cuda.synchronize()
+    r2 = w4.f16_gemm(r1, w2); torch.cuda.synchronize()
+    r3 = w4.f16_gemm(r2, w2); torch.cuda.synchronize()
+    # overlapped: y1 -> y2 (RAW), then y3 = f(y2) written into y1's buffer while
+    # the GEMM before it read y1 (WAR), then one more read of it
+    y1 = w4.f16_gemm(x, w1)
+    y2 = w4.f16_gemm(y1, w2, flags=ov)
+    w4.f16_gemm(y2, w2, y=y1, flags=ov)
+    torch.cuda.synchronize()
+    assert torch.equal(y2, r2)
+    assert torch.equal(y1, r3)
+    assert w4.device_status() == 0
