@@ -3,8 +3,10 @@
  *
  * The operation: a linear layer Y = X * W^T whose weight W[N][K] is stored as
  * 4-bit codes q in 0..15 with one binary16 scale and one binary16 bias per
- * group of 64 consecutive k, so that w[n][k] = scale[n][k/64]*q[n][k] +
- * bias[n][k/64].  Sources (page title, section):
+ * group of G consecutive k (G = 64 by default), so that
+ *     w[n][k] = scale[n][k/G]*q[n][k] + bias[n][k/G]          (affine), or,
+ *     w[n][k] = scale[n][k/G]*(q[n][k] - 8)                   (symmetric),
+ * when the weight has no biases.  Sources (page title, section):
  *   "The inference engine - Mojo 1.0 on Metal", "Crossing Mojo 1.0": decode
  *     is a weight-streaming multi-row GEMV plus on-device token selection;
  *     prefill dequantises each weight once into a transposed half-precision
@@ -14,12 +16,18 @@
  *   "engine-mlx", "Tech details": MLX 4-bit quantised format.
  *   "Engineering investigation ... 10x faster?", "Selective quantization":
  *     affine quantisation with group size 64.
+ *   "The inference engine - Mojo 1.0 on Metal", "What's inside the engine
+ *     today" and the appendix on porting MLX's kernels: that engine's own
+ *     weights are symmetric int4 with group 128 (scale only).
  *
  * Storage format (shared by every call):
  *   qweight  uint32 [N][K/8], row-major.  Word j of row n holds q[n][8j+i]
  *            in bits 4i..4i+3 (lowest nibble = lowest k).
- *   scales   binary16 [N][K/64], row-major.
- *   biases   binary16 [N][K/64], row-major.
+ *   scales   binary16 [N][K/G], row-major.
+ *   biases   binary16 [N][K/G], row-major; NULL selects symmetric codes.
+ *   group    G, a power of two with 32 <= G <= K and K % G == 0 (every call
+ *            that takes `group`; 64 is the affine format above, 128 with
+ *            NULL biases the symmetric group-128 format).
  *   Activations and outputs are binary16 (IEEE half, passed as uint16_t bit
  *   patterns), row-major.
  *
@@ -55,7 +63,7 @@ extern "C" {
 #define W4_ERR_NULL       1  /* a required pointer is NULL */
 #define W4_ERR_SHAPE      2  /* a dimension is out of the supported range */
 #define W4_ERR_ALIGN      3  /* a pointer or row stride is not 16-byte aligned */
-#define W4_ERR_GROUP      4  /* group size other than 64 */
+#define W4_ERR_GROUP      4  /* group not a power of two in 32..K dividing K */
 #define W4_ERR_LAUNCH     5  /* the CUDA runtime rejected a launch */
 #define W4_ERR_WORKSPACE  6  /* workspace missing or smaller than required */
 #define W4_ERR_DEVICE     7  /* current device is not sm_103 or lacks a needed driver entry point */
@@ -81,7 +89,8 @@ extern "C" {
  *   y       binary16 [M][N]          output; fp32 accumulation, rounded to
  *                                     nearest even once at the end
  *   M       1..16 activation rows, all sharing one pass over the weights
- *   N       >= 1 output features;  K  multiple of 64, >= 64;  group == 64
+ *   N       >= 1 output features;  K  multiple of 64, >= 64;
+ *   group   quantisation group (see the format); biases may be NULL
  * Errors: W4_ERR_NULL, W4_ERR_SHAPE, W4_ERR_GROUP, W4_ERR_ALIGN, W4_ERR_LAUNCH.
  */
 W4A16_API int w4_gemv(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
@@ -104,7 +113,8 @@ W4A16_API int w4_gemv_ex(const uint16_t *x, const uint32_t *qweight, const uint1
  *   complete and visible.  Weights are streamed without waiting, so they
  *   must not be written by the operations of the list.
  *   M       1..16 activation rows, shared by all operations.
- *   Each operation: N >= 1, K a multiple of 256, pointers 16-byte aligned.
+ *   Each operation: N >= 1, K a multiple of 256, group (0 means 64) and
+ *   biases (NULL: symmetric) as for w4_gemv, pointers 16-byte aligned.
  *   workspace  device buffer, 16-byte aligned, ZERO-FILLED before its first
  *              use and then passed unchanged to every later call (the library
  *              keeps its counters consistent: the last CTA of each launch
@@ -127,12 +137,12 @@ W4A16_API int w4_gemv_ex(const uint16_t *x, const uint32_t *qweight, const uint1
 typedef struct {
     const uint16_t *x;        /* binary16 [M][K] */
     const uint32_t *qweight;  /* [N][K/8] */
-    const uint16_t *scales;   /* binary16 [N][K/64] */
-    const uint16_t *biases;   /* binary16 [N][K/64] */
+    const uint16_t *scales;   /* binary16 [N][K/G] */
+    const uint16_t *biases;   /* binary16 [N][K/G], or NULL: symmetric codes */
     uint16_t *y;              /* binary16 [M][N] */
     int N, K;
     int wait_prev;            /* nonzero: x is written by an earlier operation */
-    int reserved;             /* set to 0 */
+    int group;                /* G of this operation's weight; 0 means 64 */
 } w4_gemv_op;
 
 /* Minimum workspace (completion counters only). */
@@ -157,7 +167,8 @@ W4A16_API int w4_gemv_seq(const w4_gemv_op *ops, int nops, int M, void *workspac
  *   ties broken by the lowest index (k == 1 is greedy argmax).  No logits
  *   tensor is written: a first pass leaves per-block candidates in
  *   `workspace`, a second pass merges them.
- *   M 1..16;  N >= k;  K multiple of 64;  group == 64;  1 <= k <= 64;
+ *   M 1..16;  N >= k;  K multiple of 64;  group and biases as for w4_gemv;
+ *   1 <= k <= 64;
  *   N * k must not exceed 16,777,216.
  *   workspace  device buffer of at least lm_head_workspace_bytes(M, N, k)
  *              bytes, 16-byte aligned; contents on entry are ignored.
@@ -213,8 +224,10 @@ W4A16_API size_t lm_head_workspace_bytes(int M, int N, int k);
  *   weight is dequantised once per prefill into a transposed half-precision
  *   scratch.)
  *   w16  binary16 [K][N] (= W transposed), w16[k][n] = the correctly rounded
- *        (nearest, ties to even) binary16 of the exact scale*q + bias.
- *   N >= 1;  K multiple of 64;  group == 64.
+ *        (nearest, ties to even) binary16 of the exact scale*q + bias, or of
+ *        scale*(q - 8) when biases is NULL (a zero keeps the sign of the
+ *        IEEE product scale*(q - 8)).
+ *   N >= 1;  K multiple of 64;  group as for w4_gemv.
  * Errors: W4_ERR_NULL, W4_ERR_SHAPE, W4_ERR_GROUP, W4_ERR_ALIGN, W4_ERR_LAUNCH.
  */
 W4A16_API int w4_dequant_f16(const uint32_t *qweight, const uint16_t *scales,

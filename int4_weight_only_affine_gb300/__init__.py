@@ -7,8 +7,9 @@ CPU or PyTorch fallback: if the library is missing, importing this package
 fails.
 
 Weight format: ``qweight`` int32/uint32 [N][K/8] (8 four-bit codes per word,
-lowest nibble = lowest k), ``scales`` and ``biases`` float16 [N][K/64];
-w[n][k] = scale * q + bias.
+lowest nibble = lowest k), ``scales`` and ``biases`` float16 [N][K/group]
+(group 64 unless given); w[n][k] = scale * q + bias, or, with
+``biases=None``, symmetric codes w[n][k] = scale * (q - 8).
 """
 from __future__ import annotations
 
@@ -97,9 +98,16 @@ _H = (torch.float16,)
 def _weight_dims(qweight, scales, biases, group):
     N, KW = qweight.shape
     K = KW * 8
-    if scales.shape != (N, K // group) or biases.shape != (N, K // group):
+    if group < 1 or K % group != 0:
+        raise ValueError(f"group {group} does not divide K = {K}")
+    if scales.shape != (N, K // group) or (biases is not None and biases.shape != (N, K // group)):
         raise ValueError(f"scales/biases must be [{N}][{K // group}]")
     return N, K
+
+
+def _biases(b) -> int | None:
+    """Device pointer of the biases, or NULL (None) for symmetric codes."""
+    return None if b is None else _dev(b, "biases", _H)
 
 
 def w4_gemv(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
@@ -112,7 +120,7 @@ def w4_gemv(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, biases
     if y is None:
         y = torch.empty((M, N), dtype=torch.float16, device=x.device)
     _check("w4_gemv", lib.w4_gemv_ex(_dev(x2, "x", _H), _dev(qweight, "qweight", _QW),
-                                     _dev(scales, "scales", _H), _dev(biases, "biases", _H),
+                                     _dev(scales, "scales", _H), _biases(biases),
                                      _dev(y, "y", _H), M, N, K, group, flags, _stream(stream)))
     return y
 
@@ -121,23 +129,23 @@ class GemvOp(ctypes.Structure):
     """One operation of w4_gemv_seq (mirror of the C struct w4_gemv_op)."""
     _fields_ = [("x", ctypes.c_void_p), ("qweight", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("biases", ctypes.c_void_p), ("y", ctypes.c_void_p), ("N", ctypes.c_int), ("K", ctypes.c_int),
-                ("wait_prev", ctypes.c_int), ("reserved", ctypes.c_int)]
+                ("wait_prev", ctypes.c_int), ("group", ctypes.c_int)]
 
 
 def _seq_array(ops, group):
-    if group != 64:
-        raise ValueError("group must be 64")
     arr = (GemvOp * len(ops))()
     M = None
-    for i, (x, qw, s, b, y, wait) in enumerate(ops):
-        N, K = _weight_dims(qw, s, b, group)
+    for i, op in enumerate(ops):
+        x, qw, s, b, y, wait = op[:6]
+        g = op[6] if len(op) > 6 else group
+        N, K = _weight_dims(qw, s, b, g)
         x2 = x.reshape(-1, K) if x.dim() != 2 else x
         if M is None:
             M = x2.shape[0]
         elif x2.shape[0] != M:
             raise ValueError("all operations must have the same number of activation rows")
         arr[i] = GemvOp(_dev(x2, "x", _H), _dev(qw, "qweight", _QW), _dev(s, "scales", _H),
-                        _dev(b, "biases", _H), _dev(y, "y", _H), N, K, 1 if wait else 0, 0)
+                        _biases(b), _dev(y, "y", _H), N, K, 1 if wait else 0, g)
     return arr, M
 
 
@@ -158,9 +166,9 @@ def seq_workspace(ops, group: int = 64) -> torch.Tensor:
 def w4_gemv_seq(ops, workspace: torch.Tensor | None = None, group: int = 64, stream=None):
     """Run a list of GEMVs in one persistent launch.
 
-    ops: sequence of (x, qweight, scales, biases, y, wait_prev) with torch
-    tensors; wait_prev = True when x is written by an earlier operation of the
-    list.  All x share the same number of rows M.  workspace: from
+    ops: sequence of (x, qweight, scales, biases, y, wait_prev[, group]) with
+    torch tensors (biases None: symmetric codes); wait_prev = True when x is
+    written by an earlier operation of the list; group defaults to `group`.  All x share the same number of rows M.  workspace: from
     seq_workspace(ops) (zero-filled before its first use, then passed
     unchanged to every call); a fresh one is made when None.  Returns the
     list of y."""
@@ -194,7 +202,7 @@ def lm_head_argmax_topk(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Te
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
     _check("lm_head_argmax_topk",
            lib.lm_head_argmax_topk_ex(_dev(x2, "x", _H), _dev(qweight, "qweight", _QW),
-                                      _dev(scales, "scales", _H), _dev(biases, "biases", _H),
+                                      _dev(scales, "scales", _H), _biases(biases),
                                       M, N, K, group, k, _dev(idx, "idx", (torch.int32,)),
                                       _dev(val, "val", (torch.float32,)),
                                       _dev(workspace, "workspace", (torch.uint8,)),
@@ -204,7 +212,8 @@ def lm_head_argmax_topk(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Te
 
 def w4_dequant_f16(qweight: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
                    w16: torch.Tensor | None = None, group: int = 64, stream=None, flags: int = 0) -> torch.Tensor:
-    """Transposed half scratch w16[K][N] = RNE(scale * q + bias).  flags:
+    """Transposed half scratch w16[K][N] = RNE(scale * q + bias), or
+    RNE(scale * (q - 8)) with biases None.  flags:
     OVERLAP_PREVIOUS when this call shares no memory with the previous kernel
     (it may then run concurrently with it)."""
     N, K = _weight_dims(qweight, scales, biases, group)
@@ -212,7 +221,7 @@ def w4_dequant_f16(qweight: torch.Tensor, scales: torch.Tensor, biases: torch.Te
         w16 = torch.empty((K, N), dtype=torch.float16, device=qweight.device)
     _check("w4_dequant_f16",
            lib.w4_dequant_f16_ex(_dev(qweight, "qweight", _QW), _dev(scales, "scales", _H),
-                                 _dev(biases, "biases", _H), _dev(w16, "w16", _H), N, K, group, flags,
+                                 _biases(biases), _dev(w16, "w16", _H), N, K, group, flags,
                                  _stream(stream)))
     return w16
 

@@ -10,10 +10,38 @@
 
 namespace w4a16 {
 
-constexpr int kGroup = 64;         // quantisation group along K
+// The kernels step along K in blocks of 64 codes (8 words per row); the
+// quantisation group is a runtime parameter described by WFmt.
+constexpr int kGroup = 64;         // k per code block
 constexpr int kWordsPerGroup = 8;  // 64 four-bit codes = 8 words
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Scale layout of a quantised weight: ngs scale (and bias) entries per row
+// (K / group); gs = log2(group / 32), so group = 32 << gs; sym: the weight
+// has no biases and w = scale * (q - 8) (symmetric codes).
+struct WFmt {
+    int ngs, gs, sym;
+};
+
+// Kernel variants by scale layout: group-64 affine (the workloads' format),
+// any other group of 64 or more or symmetric codes (runtime layout), and
+// group 32 (two quantisation groups per 64-k block).
+enum : int { kFmtG64 = 0, kFmtAny = 1, kFmtG32 = 2 };
+
+inline int fmt_class(const WFmt &f) { return f.gs == 0 ? kFmtG32 : (f.gs == 1 && !f.sym) ? kFmtG64 : kFmtAny; }
+
+// Host check of a (K, group) pair: group a power of two with
+// 32 <= group <= K and K % group == 0.  Fills f; false if unsupported.
+inline bool make_fmt(WFmt &f, int K, int group, bool sym) {
+    if (group < 32 || group > K || (group & (group - 1)) != 0 || K % group != 0) return false;
+    int gs = 0;
+    while ((32 << gs) < group) ++gs;
+    f.ngs = K / group;
+    f.gs = gs;
+    f.sym = sym ? 1 : 0;
+    return true;
+}
 
 inline int launch_status() {
     cudaError_t e = cudaGetLastError();

@@ -4,10 +4,12 @@
 // dequantises each weight once into a transposed half-precision scratch and
 // then runs a half-precision GEMM on it.
 //
-// w16[k][n] = RNE_binary16(scale[n][k/64] * q[n][k] + bias[n][k/64]).
+// w16[k][n] = RNE_binary16(scale[n][k/G] * q[n][k] + bias[n][k/G]), or
+// RNE_binary16(scale[n][k/G] * (q[n][k] - 8)) for symmetric codes.
 // The code is made an exact binary16 (1024 + q via the exponent trick, then an
-// exact subtraction of 1024) and one binary16 fused multiply-add rounds the
-// exact scale*q + bias once, to nearest even: the correctly rounded value.
+// exact subtraction of 1024, or of 1032 for q - 8) and one binary16 fused
+// multiply-add (a multiply for symmetric codes) rounds the exact value once,
+// to nearest even: the correctly rounded value.
 //
 // The kernels are HBM bound (0.5625 B read + 2 B written per weight).
 //
@@ -26,6 +28,8 @@
 // two adjacent rows, dequantise them as (row n, row n+1) half pairs,
 // transpose through padded shared memory, and write 128-byte segments of 64
 // consecutive n for each k.
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace w4a16 {
@@ -36,19 +40,36 @@ constexpr int kPairs = kTileN / 2;      // 32-bit (n, n+1) pairs per k row
 constexpr int kStride = kPairs + 1;     // padded shared-memory row (words)
 constexpr int kThreads = 256;
 
+// The half pairs (w(row a), w(row b)) of the eight codes of words A (row a)
+// and B (row b) with scales s2 and biases b2; symmetric: bias-free, code
+// q - 8.  koff: 1024 (affine) or 1032 (symmetric) in both halves.
+template <bool SYM>
+__device__ __forceinline__ void dequant_word_pair(uint32_t A, uint32_t B, __half2 s2, __half2 b2, __half2 koff,
+                                                  uint32_t (&o)[8]) {
+    // (row a, row b) pairs of codes 0..3 and 4..7 of this word.
+    const uint32_t lo = __byte_perm(A, B, 0x5410);
+    const uint32_t hi = __byte_perm(A, B, 0x7632);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const uint32_t src = e < 4 ? lo : hi;
+        const uint32_t v = ((src >> (4 * (e & 3))) & 0x000F000Fu) | 0x64006400u;  // 1024 + q
+        const __half2 q2 = __hsub2(*reinterpret_cast<const __half2 *>(&v), koff);  // exact q (or q - 8)
+        const __half2 w2 = SYM ? __hmul2(q2, s2) : __hfma2(q2, s2, b2);           // one rounding
+        o[e] = *reinterpret_cast<const uint32_t *>(&w2);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads)
     dequant_kernel(const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc,
                    const uint16_t *__restrict__ bi, uint16_t *__restrict__ w16, int N, int K,
-                   long long ntiles, int tiles_n) {
+                   long long ntiles, int tiles_n, WFmt f) {
     __shared__ uint32_t tile[kGroup * kStride];
-    const int ng = K / kGroup;
     // Warp w covers 8 row pairs x 4 words: shared-memory stores (bank
     // 8*word + i + pair, mod 32) are conflict free.
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int pair = (warp & 3) * 8 + (lane >> 2);  // 0..31
     const int word = (warp >> 2) * 4 + (lane & 3);  // word of the group, k = 8*word .. 8*word+7
     const bool vec_ok = (N % 8) == 0;
-    const __half2 k1024 = __float2half2_rn(1024.f);
 
     for (long long t = blockIdx.x; t < ntiles; t += gridDim.x) {
         const int G = (int)(t / tiles_n);
@@ -57,21 +78,19 @@ __global__ void __launch_bounds__(kThreads)
         const int nb = min(n0 + 2 * pair + 1, N - 1);
         const uint32_t A = __ldg(qw + (size_t)na * (K / 8) + (size_t)G * kWordsPerGroup + word);
         const uint32_t B = __ldg(qw + (size_t)nb * (K / 8) + (size_t)G * kWordsPerGroup + word);
-        const uint16_t sa = ld_nc_u16(sc + (size_t)na * ng + G), sb = ld_nc_u16(sc + (size_t)nb * ng + G);
-        const uint16_t ba = ld_nc_u16(bi + (size_t)na * ng + G), bb = ld_nc_u16(bi + (size_t)nb * ng + G);
+        const int gi = (G * kGroup + 8 * word) >> (f.gs + 5);  // quantisation group of the word
+        const uint16_t sa = ld_nc_u16(sc + (size_t)na * f.ngs + gi), sb = ld_nc_u16(sc + (size_t)nb * f.ngs + gi);
         const __half2 s2 = __halves2half2(__ushort_as_half(sa), __ushort_as_half(sb));
-        const __half2 b2 = __halves2half2(__ushort_as_half(ba), __ushort_as_half(bb));
-        // (row n, row n+1) pairs of codes 0..3 and 4..7 of this word.
-        const uint32_t lo = __byte_perm(A, B, 0x5410);
-        const uint32_t hi = __byte_perm(A, B, 0x7632);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t src = (i < 4) ? lo : hi;
-            const uint32_t v = ((src >> (4 * (i & 3))) & 0x000F000Fu) | 0x64006400u;  // 1024 + q
-            __half2 q2 = __hsub2(*reinterpret_cast<const __half2 *>(&v), k1024);   // exact q
-            __half2 w2 = __hfma2(q2, s2, b2);                                     // one rounding
-            tile[(8 * word + i) * kStride + pair] = *reinterpret_cast<uint32_t *>(&w2);
+        uint32_t o[8];
+        if (f.sym) {
+            dequant_word_pair<true>(A, B, s2, s2, __float2half2_rn(1032.f), o);
+        } else {
+            const uint16_t ba = ld_nc_u16(bi + (size_t)na * f.ngs + gi), bb = ld_nc_u16(bi + (size_t)nb * f.ngs + gi);
+            const __half2 b2 = __halves2half2(__ushort_as_half(ba), __ushort_as_half(bb));
+            dequant_word_pair<false>(A, B, s2, b2, __float2half2_rn(1024.f), o);
         }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) tile[(8 * word + i) * kStride + pair] = o[i];
         __syncthreads();
         // 64 k rows x 32 words; each thread writes 4 words (8 n) per pass.
 #pragma unroll
@@ -101,23 +120,33 @@ constexpr int kTmaK = 256;                         // k per tile (4 groups, 32 w
 constexpr int kCodeBytes = kTmaRows * kTmaK / 2;   // 8 KB
 constexpr int kOutBytes = kTmaK * kTmaRows * 2;    // 32 KB
 constexpr int kCodeStages = 4;                    // code tiles in flight per CTA
-constexpr int kTmaSmem = kCodeStages * kCodeBytes + 2 * kOutBytes + 2 * 2 * kTmaRows * 4 * 2 + 8 * kCodeStages;
+// Scale staging: ANY keeps a pair (the two 32-k chunks) per row and 64-k block.
+template <bool ANY>
+constexpr int tma_smem() {
+    return kCodeStages * kCodeBytes + 2 * kOutBytes + 2 * 2 * kTmaRows * 4 * (ANY ? 4 : 2) + 8 * kCodeStages;
+}
 
+// ANY: any scale layout (f); otherwise group-64 affine (one scale and one
+// bias per 64-k block).
+template <bool ANY>
 __global__ void __launch_bounds__(kThreads, 2)
     dequant_tma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_w,
                        const uint16_t *__restrict__ sc, const uint16_t *__restrict__ bi, int N, int K, int tiles_n,
-                       int ntiles) {
+                       int ntiles, WFmt f) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *sb = smem_raw + (base - raw);
     constexpr int kOutOff = kCodeStages * kCodeBytes;
     const uint32_t codes0 = base, out0 = base + kOutOff;
-    uint16_t *scl = reinterpret_cast<uint16_t *>(sb + kOutOff + 2 * kOutBytes);  // [2][64][4]
-    uint16_t *bia = scl + 2 * kTmaRows * 4;                                     // [2][64][4]
-    const uint32_t bar0 = base + kOutOff + 2 * kOutBytes + 2 * 2 * kTmaRows * 4 * 2;
+    // Scales and biases of each row and 64-k block of a tile, [2][64][4]:
+    // group 64 one binary16 each; ANY the pair of its 32-k chunks (low half
+    // first).
+    using SW = typename std::conditional<ANY, uint32_t, uint16_t>::type;
+    SW *scl = reinterpret_cast<SW *>(sb + kOutOff + 2 * kOutBytes);
+    SW *bia = scl + 2 * kTmaRows * 4;
+    const uint32_t bar0 = base + kOutOff + 2 * kOutBytes + 2 * 2 * kTmaRows * 4 * (int)sizeof(SW);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int ng = K / kGroup;
     const int G = gridDim.x;
     // Launched with W4A16_OVERLAP_PREVIOUS the caller guarantees independence
     // from the previous and the next kernel: release the next one at once
@@ -125,12 +154,25 @@ __global__ void __launch_bounds__(kThreads, 2)
     pdl_launch_dependents();
     auto tile_n0 = [&](int t) { return (t % tiles_n) * kTmaRows; };
     auto tile_k0 = [&](int t) { return (t / tiles_n) * kTmaK; };
-    // Thread tid stages the scale and bias of row tid/4, group tid%4 of a tile.
-    auto load_sb = [&](int t, uint16_t &s, uint16_t &b) {
+    // Thread tid stages the scales and biases of row tid/4, 64-k block tid%4
+    // of a tile.
+    auto load_sb = [&](int t, SW &s, SW &b) {
         const int n = min(tile_n0(t) + tid / 4, N - 1);
-        const int g = min(tile_k0(t) / kGroup + (tid & 3), ng - 1);
-        s = ld_nc_u16(sc + (size_t)n * ng + g);
-        b = ld_nc_u16(bi + (size_t)n * ng + g);
+        if (!ANY) {
+            const int g = min(tile_k0(t) / kGroup + (tid & 3), f.ngs - 1);
+            s = ld_nc_u16(sc + (size_t)n * f.ngs + g);
+            b = ld_nc_u16(bi + (size_t)n * f.ngs + g);
+            return;
+        }
+        const int c0 = min(tile_k0(t) + 64 * (tid & 3), K - 64) >> 5;  // first 32-k chunk along K
+        const int g0 = c0 >> f.gs, g1 = (c0 + 1) >> f.gs;
+        const uint16_t *rs = sc + (size_t)n * f.ngs;
+        s = (SW)((uint32_t)ld_nc_u16(rs + g0) | ((uint32_t)ld_nc_u16(rs + g1) << 16));
+        b = 0u;
+        if (!f.sym) {
+            const uint16_t *rb = bi + (size_t)n * f.ngs;
+            b = (SW)((uint32_t)ld_nc_u16(rb + g0) | ((uint32_t)ld_nc_u16(rb + g1) << 16));
+        }
     };
 
     if (tid == 0) {
@@ -146,9 +188,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     // Scales: tile 0's into shared memory now; tile i+1's are in registers
     // (loaded two tiles ahead) and reach shared memory at the end of tile i.
-    uint16_t ps0 = 0, pb0 = 0, ps1 = 0, pb1 = 0;  // register sets for even / odd tiles
+    SW ps0 = 0, pb0 = 0, ps1 = 0, pb1 = 0;  // register sets for even / odd tiles
     if (blockIdx.x < ntiles) {
-        uint16_t s, b;
+        SW s, b;
         load_sb(blockIdx.x, s, b);
         scl[tid] = s;
         bia[tid] = b;
@@ -161,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int rowa = 2 * lane, rowb = 2 * lane + 1;
     const uint32_t offa = rowa * 128 + ((c ^ (rowa & 7)) << 4);
     const uint32_t offb = rowb * 128 + ((c ^ (rowb & 7)) << 4);
-    const __half2 k1024 = __float2half2_rn(1024.f);
+    const __half2 koff = __float2half2_rn(ANY && f.sym ? 1032.f : 1024.f);
     bool ok = true;
     int waited = 0;  // tiles whose codes this thread has waited for
     for (int i = 0;; ++i) {
@@ -186,25 +228,32 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint8_t *cs = sb + cst * kCodeBytes;
             const uint4 A = *reinterpret_cast<const uint4 *>(cs + offa);
             const uint4 B = *reinterpret_cast<const uint4 *>(cs + offb);
-            const int gl = c >> 1;  // group of the chunk within the tile
-            const __half2 s2 = __halves2half2(__ushort_as_half(scl[st * 256 + rowa * 4 + gl]),
-                                              __ushort_as_half(scl[st * 256 + rowb * 4 + gl]));
-            const __half2 b2 = __halves2half2(__ushort_as_half(bia[st * 256 + rowa * 4 + gl]),
-                                              __ushort_as_half(bia[st * 256 + rowb * 4 + gl]));
+            // Scale and bias of chunk c: block c/2 of the row's set (ANY: half c%2).
+            const int sh = 16 * (c & 1), wi = c >> 1;
+            auto pair = [&](const SW *arr) {
+                const uint32_t va = arr[st * 256 + rowa * 4 + wi], vb = arr[st * 256 + rowb * 4 + wi];
+                const uint32_t p = ANY ? __byte_perm(va >> sh, vb >> sh, 0x5410) : __byte_perm(va, vb, 0x5410);
+                return *reinterpret_cast<const __half2 *>(&p);
+            };
+            const __half2 s2 = pair(scl);
             uint32_t *out = reinterpret_cast<uint32_t *>(sb + kOutOff + st * kOutBytes);
             const uint32_t wa[4] = {A.x, A.y, A.z, A.w}, wb[4] = {B.x, B.y, B.z, B.w};
+            if (ANY && f.sym) {
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const uint32_t lo = __byte_perm(wa[w], wb[w], 0x5410);  // codes 0..3 of (row a, row b)
-                const uint32_t hi = __byte_perm(wa[w], wb[w], 0x7632);  // codes 4..7
+                for (int w = 0; w < 4; ++w) {
+                    uint32_t o[8];
+                    dequant_word_pair<true>(wa[w], wb[w], s2, s2, koff, o);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint32_t src = e < 4 ? lo : hi;
-                    const uint32_t v = ((src >> (4 * (e & 3))) & 0x000F000Fu) | 0x64006400u;  // 1024 + q
-                    const __half2 q2 = __hsub2(*reinterpret_cast<const __half2 *>(&v), k1024);  // exact q
-                    const __half2 w2 = __hfma2(q2, s2, b2);                                      // one rounding
-                    const int k = 32 * c + 8 * w + e;
-                    out[k * (kTmaRows / 2) + lane] = *reinterpret_cast<const uint32_t *>(&w2);
+                    for (int e = 0; e < 8; ++e) out[(32 * c + 8 * w + e) * (kTmaRows / 2) + lane] = o[e];
+                }
+            } else {
+                const __half2 b2 = pair(bia);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    uint32_t o[8];
+                    dequant_word_pair<false>(wa[w], wb[w], s2, b2, koff, o);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) out[(32 * c + 8 * w + e) * (kTmaRows / 2) + lane] = o[e];
                 }
             }
         }
@@ -242,10 +291,11 @@ using namespace w4a16;
 
 static int dequant_impl(const uint32_t *qweight, const uint16_t *scales, const uint16_t *biases, uint16_t *w16,
                         int N, int K, int group, unsigned flags, void *stream) {
-    if (!qweight || !scales || !biases || !w16) return W4_ERR_NULL;
-    if (group != kGroup) return W4_ERR_GROUP;
+    if (!qweight || !scales || !w16) return W4_ERR_NULL;
     if (N < 1 || K < kGroup || K % kGroup != 0) return W4_ERR_SHAPE;
-    if (!aligned16(qweight) || !aligned16(scales) || !aligned16(biases) || !aligned16(w16))
+    WFmt f;
+    if (!make_fmt(f, K, group, biases == nullptr)) return W4_ERR_GROUP;
+    if (!aligned16(qweight) || !aligned16(scales) || (biases && !aligned16(biases)) || !aligned16(w16))
         return W4_ERR_ALIGN;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (N % 8 == 0) {
@@ -260,36 +310,37 @@ static int dequant_impl(const uint32_t *qweight, const uint16_t *scales, const u
         const int tiles_n = (N + kTmaRows - 1) / kTmaRows;
         const long long ntiles = (long long)tiles_n * ((K + kTmaK - 1) / kTmaK);
         if (ntiles > 0x7fffffffLL) return W4_ERR_SHAPE;
-        static bool attr_set[64] = {false};
+        const bool any = !(f.gs == 1 && !f.sym);
+        auto kern = any ? dequant_tma_kernel<true> : dequant_tma_kernel<false>;
+        const int smem = (any ? tma_smem<true>() : tma_smem<false>()) + 1024;
+        static bool attr_set[2][64] = {{false}};
         int dev = 0;
         cudaGetDevice(&dev);
-        if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-            if (cudaFuncSetAttribute(dequant_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmem + 1024) !=
-                cudaSuccess)
+        if (dev >= 0 && dev < 64 && !attr_set[any][dev]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
                 return W4_ERR_LAUNCH;
-            attr_set[dev] = true;
+            attr_set[any][dev] = true;
         }
         long long grid = (long long)sm_count() * 2;
         if (grid > ntiles) grid = ntiles;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid, 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = kTmaSmem + 1024;
+        cfg.dynamicSmemBytes = smem;
         cfg.stream = st;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = (flags & W4A16_OVERLAP_PREVIOUS) ? 1 : 0;
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, dequant_tma_kernel, mq, mw, scales, biases, N, K, tiles_n,
-                                                 (int)ntiles);
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mq, mw, scales, biases, N, K, tiles_n, (int)ntiles, f);
         return e == cudaSuccess ? W4A16_OK : W4_ERR_LAUNCH;
     }
     const int tiles_n = (N + kTileN - 1) / kTileN;
     const long long ntiles = (long long)tiles_n * (K / kGroup);
     long long grid = (long long)sm_count() * 8;
     if (grid > ntiles) grid = ntiles;
-    dequant_kernel<<<(unsigned)grid, kThreads, 0, st>>>(qweight, scales, biases, w16, N, K, ntiles, tiles_n);
+    dequant_kernel<<<(unsigned)grid, kThreads, 0, st>>>(qweight, scales, biases, w16, N, K, ntiles, tiles_n, f);
     return launch_status();
 }
 

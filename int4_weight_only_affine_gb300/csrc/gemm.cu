@@ -647,7 +647,7 @@ extern "C" const char *w4a16_status_string(int status) {
         case W4_ERR_NULL: return "null pointer";
         case W4_ERR_SHAPE: return "unsupported shape";
         case W4_ERR_ALIGN: return "pointer or stride not 16-byte aligned";
-        case W4_ERR_GROUP: return "group size must be 64";
+        case W4_ERR_GROUP: return "group must be a power of two in 32..K that divides K";
         case W4_ERR_LAUNCH: return "CUDA launch error";
         case W4_ERR_WORKSPACE: return "workspace missing or too small";
         case W4_ERR_DEVICE: return "unsupported device (needs sm_103) or missing driver entry point";

@@ -212,7 +212,8 @@ struct StreamArgs {
     int C;       // CTAs per cluster splitting K
     int tiles;   // ceil(N / 16)
     int stages;  // ring depth
-    int ng;      // groups along K
+    int ng;      // groups (64-k blocks) along K
+    WFmt f;      // scale layout (quantisation group, symmetric codes)
     int units;   // 8-group units along K
     int nq_full; // whole 128-byte quads (4 groups) per row
     int cq;      // quads per 3-D copy
@@ -223,7 +224,8 @@ struct StreamArgs {
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
 
-template <int NT, bool LMHEAD, bool M1>
+// FMT: the scale-layout class of the weight (kFmtG64, kFmtAny, kFmtG32).
+template <int NT, bool LMHEAD, bool M1, int FMT>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
     stream_kernel(const __grid_constant__ CUtensorMap tm3, const __grid_constant__ CUtensorMap tm2,
                   const StreamArgs a) {
@@ -286,22 +288,28 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
                     const int len = min(kChunkGroups, gs1 - cg0);
                     const int q0 = cg0 / kBoxGroups;
                     const int nbox = (len + kBoxGroups - 1) / kBoxGroups;
-                    const uint32_t sbytes = tail ? 0u : 32u * ng;
+                    // The tile's scale rows (and bias rows) are contiguous: [16][ngs].
+                    const bool sym = FMT != kFmtG64 && a.f.sym;
+                    const int ngs = FMT == kFmtG64 ? ng : a.f.ngs;
+                    const uint32_t sbytes = tail ? 0u : 32u * ngs;
+                    const uint32_t sball = sym ? sbytes : 2 * sbytes;
                     const uint32_t st = base + s * a.stage_bytes;
                     if (q0 + nbox <= a.nq_full) {
                         // One 3-D copy: cq quads x 16 rows x 128 B, the same swizzled
                         // image as cq separate 16 x 128 B boxes.
-                        mbar_expect_tx(full_bar(s), a.cq * kBoxBytes + 2 * sbytes);
+                        mbar_expect_tx(full_bar(s), a.cq * kBoxBytes + sball);
                         tma_load_3d(st, &tm3, 0, t * kTileRows, q0, full_bar(s));
                     } else {
                         // The chunk holding the ragged end of a row: one box per quad.
-                        mbar_expect_tx(full_bar(s), nbox * kBoxBytes + 2 * sbytes);
+                        mbar_expect_tx(full_bar(s), nbox * kBoxBytes + sball);
                         for (int b = 0; b < nbox; ++b)
                             tma_load_2d(st + b * kBoxBytes, &tm2, (q0 + b) * 32, t * kTileRows, full_bar(s));
                     }
                     if (!tail) {
-                        bulk_load(st + a.w_bytes, a.sc + (size_t)t * kTileRows * ng, sbytes, full_bar(s));
-                        bulk_load(st + a.w_bytes + sbytes, a.bi + (size_t)t * kTileRows * ng, sbytes, full_bar(s));
+                        bulk_load(st + a.w_bytes, a.sc + (size_t)t * kTileRows * ngs, sbytes, full_bar(s));
+                        if (!sym)
+                            bulk_load(st + a.w_bytes + sbytes, a.bi + (size_t)t * kTileRows * ngs, sbytes,
+                                      full_bar(s));
                     }
                     issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
                     issued_any |= 1u << s;
@@ -318,9 +326,13 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
         int off[4];
         box_offsets(off, warp, lg, lt);
         const int xoff = lane_xoff(M, lg, lt), xd1 = lane_xd1(M, lg);
-        const bool vec = (ng & 3) == 0;
+        const uint32_t hmask = FMT == kFmtG32 ? g32_m1_mask(lg, lt) : 0u;
+        WFmt f = a.f;
+        if (FMT == kFmtG64) f.ngs = ng;  // one scale per group (the same value, one register)
+        const bool sym = FMT != kFmtG64 && f.sym;
+        const bool vec = FMT == kFmtG64 ? (f.ngs & 3) == 0 : box_vec_ok(f);
         pdl_wait();
-        stage_activations<M1 ? 2 : 4>(a.x, M, a.K, gs0, ngl, xf, xsum, tid, kConsumers);
+        stage_activations<M1 ? 2 : 4, FMT == kFmtG32>(a.x, M, a.K, gs0, ngl, xf, xsum, tid, kConsumers);
         consumer_sync();
         int s = 0;
         uint32_t ph = 0;
@@ -337,10 +349,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
                 if (tail) {
                     // The producer copies no scales for the ragged last tile (its rows
                     // end inside the arrays); fill them here, rows past N repeated.
-                    for (int i = tid; i < 2 * kTileRows * ng; i += kConsumers) {
-                        const int arr = i / (kTileRows * ng), r = (i / ng) % kTileRows, gi = i % ng;
+                    const int ngs = f.ngs;
+                    for (int i = tid; i < (sym ? 1 : 2) * kTileRows * ngs; i += kConsumers) {
+                        const int arr = i / (kTileRows * ngs), r = (i / ngs) % kTileRows, gi = i % ngs;
                         const uint16_t *src = arr ? a.bi : a.sc;
-                        sp[i] = src[(size_t)min(row0 + r, N - 1) * ng + gi];
+                        sp[i] = src[(size_t)min(row0 + r, N - 1) * ngs + gi];
                     }
                     fence_proxy_async_smem();  // a later bulk copy reuses these bytes
                     consumer_sync();
@@ -350,10 +363,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
                     const int n = min(kBoxGroups, gs1 - g);
                     const int gl = g - gs0;
                     const uint4 *xl = reinterpret_cast<const uint4 *>(xf) + (size_t)gl * 2 * M * 4 + xoff;
+                    const float *xs = xsum + gl * M * (FMT == kFmtG32 ? 2 : 1);
                     if (n == kBoxGroups && vec)
-                        box_mma<NT, M1, true>(acc, st, off, sp, ng, g, n, xl, xd1, xsum + gl * M, M, lg, lt);
+                        box_mma<NT, M1, true, FMT>(acc, st, off, sp, f, g, n, xl, xd1, xs, M, lg, lt, hmask);
                     else if (n > 0)
-                        box_mma<NT, M1, false>(acc, st, off, sp, ng, g, n, xl, xd1, xsum + gl * M, M, lg, lt);
+                        box_mma<NT, M1, false, FMT>(acc, st, off, sp, f, g, n, xl, xd1, xs, M, lg, lt, hmask);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_bar(s));
@@ -504,6 +518,7 @@ struct SeqOp {
     uint32_t *yt;        // tagged copy of y for later operations, or null
     int N, K, wait_prev, cq;
     int src;             // operation (of this launch) that writes xt
+    WFmt f;              // scale layout
 };
 
 struct SeqParams {
@@ -535,7 +550,9 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
     return v;
 }
 
-template <int NT, bool M1>
+// FMT: the scale-layout class shared by every operation of the launch (the
+// host splits lists so).
+template <int NT, bool M1, int FMT>
 __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_constant__ SeqParams P) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
@@ -577,7 +594,10 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
                 const int ng = o.K / kGroup, nch = (ng + kChunkGroups - 1) / kChunkGroups;
                 for (int t = t0; t < t1 && ok; ++t) {
                     const bool tail = (t + 1) * kTileRows > o.N;
-                    const uint32_t sbytes = tail ? 0u : 32u * ng;
+                    const bool sym = FMT != kFmtG64 && o.f.sym;
+                    const int ngs = FMT == kFmtG64 ? ng : o.f.ngs;
+                    const uint32_t sbytes = tail ? 0u : 32u * ngs;
+                    const uint32_t sball = sym ? sbytes : 2 * sbytes;
                     for (int ch = 0; ch < nch; ++ch, ++it) {
                         const int s = it % S;
                         const uint32_t ph = (it / S) & 1;
@@ -586,11 +606,13 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
                             break;
                         }
                         const uint32_t st = base + s * P.stage_bytes;
-                        mbar_expect_tx(full_bar(s), o.cq * kBoxBytes + 2 * sbytes);
+                        mbar_expect_tx(full_bar(s), o.cq * kBoxBytes + sball);
                         tma_load_3d(st, &P.maps[op], 0, t * kTileRows, ch * (kChunkGroups / kBoxGroups), full_bar(s));
                         if (!tail) {
-                            bulk_load(st + P.w_bytes, o.sc + (size_t)t * kTileRows * ng, sbytes, full_bar(s));
-                            bulk_load(st + P.w_bytes + sbytes, o.bi + (size_t)t * kTileRows * ng, sbytes, full_bar(s));
+                            bulk_load(st + P.w_bytes, o.sc + (size_t)t * kTileRows * ngs, sbytes, full_bar(s));
+                            if (!sym)
+                                bulk_load(st + P.w_bytes + sbytes, o.bi + (size_t)t * kTileRows * ngs, sbytes,
+                                          full_bar(s));
                         }
                         issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
                         issued_any |= 1u << s;
@@ -608,6 +630,7 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
         int off[4];
         box_offsets(off, tw, lg, lt);
         const int xoff = lane_xoff(M, lg, lt), xd1 = lane_xd1(M, lg);
+        const uint32_t hmask = FMT == kFmtG32 ? g32_m1_mask(lg, lt) : 0u;
         // The workspace epoch counts completed launches; (epoch, operation)
         // names the 16-bit tag of every tagged word an operation writes, so a
         // word left by an earlier launch never matches.
@@ -618,6 +641,10 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
         for (int op = 0; op < P.nops; ++op) {
             const SeqOp &o = P.ops[op];
             const int N = o.N, ng = o.K / kGroup, nch = (ng + kChunkGroups - 1) / kChunkGroups;
+            // K % 256 == 0: every full box reads its scales as one vector.
+            WFmt f = o.f;
+            if (FMT == kFmtG64) f.ngs = ng;  // one scale per group (the same value, one register)
+            const bool sym = FMT != kFmtG64 && f.sym;
             const int T = (N + kTileRows - 1) / kTileRows;
             const int t0 = (int)((long long)blk * T / G), t1 = (int)((long long)(blk + 1) * T / G);
             const int ntl = t1 - t0;
@@ -638,10 +665,10 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
             if (o.xt) {
                 // Activations produced by an earlier operation of this launch: poll
                 // the tagged words themselves (one L2 round trip, no counter).
-                stage_activations_t<true>(nullptr, o.xt, seq_tag(epoch, P.nops, o.src), M, o.K, 0, ng, xf, xsum,
-                                          tid, kSeqConsumers, true, abort_flag);
+                stage_activations_t<true, 2, FMT == kFmtG32>(nullptr, o.xt, seq_tag(epoch, P.nops, o.src), M, o.K, 0,
+                                                             ng, xf, xsum, tid, kSeqConsumers, true, abort_flag);
             } else {
-                stage_activations(o.x, M, o.K, 0, ng, xf, xsum, tid, kSeqConsumers, true);
+                stage_activations<2, FMT == kFmtG32>(o.x, M, o.K, 0, ng, xf, xsum, tid, kSeqConsumers, true);
             }
             seq_sync();
             for (int tl = team; tl < ntl; tl += 2) {
@@ -661,10 +688,11 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
                     if (tail) {
                         // Only the last tile of the operation is ragged; its team
                         // fills the scales the producer could not copy.
-                        for (int i = tw * 32 + lane; i < 2 * kTileRows * ng; i += kSeqTeamWarps * 32) {
-                            const int arr = i / (kTileRows * ng), r = (i / ng) % kTileRows, gi = i % ng;
+                        const int ngs = f.ngs;
+                        for (int i = tw * 32 + lane; i < (sym ? 1 : 2) * kTileRows * ngs; i += kSeqTeamWarps * 32) {
+                            const int arr = i / (kTileRows * ngs), r = (i / ngs) % kTileRows, gi = i % ngs;
                             const uint16_t *src = arr ? o.bi : o.sc;
-                            sp[i] = src[(size_t)min(row0 + r, N - 1) * ng + gi];
+                            sp[i] = src[(size_t)min(row0 + r, N - 1) * ngs + gi];
                         }
                         fence_proxy_async_smem();  // a later bulk copy reuses these bytes
                         team_sync(team);
@@ -673,10 +701,15 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
                         const int g = ch * kChunkGroups + kBoxGroups * tw;
                         const int n = min(kBoxGroups, ng - g);
                         const uint4 *xl = reinterpret_cast<const uint4 *>(xf) + (size_t)g * 2 * M * 4 + xoff;
-                        if (n == kBoxGroups)  // ng % 4 == 0 holds for every operation here
-                            box_mma<NT, M1, true>(acc, st, off, sp, ng, g, n, xl, xd1, xsum + g * M, M, lg, lt);
+                        // (The sums' address is formed inside each call: this keeps the
+                        // group-64 M = 1 variant within its 96 registers.)
+                        constexpr int xsg = FMT == kFmtG32 ? 2 : 1;  // sums per group and row
+                        if (n == kBoxGroups)
+                            box_mma<NT, M1, true, FMT>(acc, st, off, sp, f, g, n, xl, xd1, xsum + g * M * xsg, M, lg,
+                                                       lt, hmask);
                         else if (n > 0)
-                            box_mma<NT, M1, false>(acc, st, off, sp, ng, g, n, xl, xd1, xsum + g * M, M, lg, lt);
+                            box_mma<NT, M1, false, FMT>(acc, st, off, sp, f, g, n, xl, xd1, xsum + g * M * xsg, M, lg,
+                                                        lt, hmask);
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(empty_bar(s));
@@ -736,12 +769,21 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
     __syncthreads();
 }
 
-const void *stream_kernel_ptr(int M, bool lmhead) {
+template <int FMT>
+const void *stream_kernel_ptr_f(int M, bool lmhead) {
     if (lmhead)
-        return M == 1 ? (const void *)stream_kernel<1, true, true>
-                      : M <= 8 ? (const void *)stream_kernel<1, true, false> : (const void *)stream_kernel<2, true, false>;
-    return M == 1 ? (const void *)stream_kernel<1, false, true>
-                  : M <= 8 ? (const void *)stream_kernel<1, false, false> : (const void *)stream_kernel<2, false, false>;
+        return M == 1 ? (const void *)stream_kernel<1, true, true, FMT>
+               : M <= 8 ? (const void *)stream_kernel<1, true, false, FMT>
+                        : (const void *)stream_kernel<2, true, false, FMT>;
+    return M == 1 ? (const void *)stream_kernel<1, false, true, FMT>
+           : M <= 8 ? (const void *)stream_kernel<1, false, false, FMT>
+                    : (const void *)stream_kernel<2, false, false, FMT>;
+}
+
+const void *stream_kernel_ptr(int M, bool lmhead, int fmt) {
+    return fmt == kFmtG64 ? stream_kernel_ptr_f<kFmtG64>(M, lmhead)
+           : fmt == kFmtG32 ? stream_kernel_ptr_f<kFmtG32>(M, lmhead)
+                            : stream_kernel_ptr_f<kFmtAny>(M, lmhead);
 }
 
 // lm_head pass 2: one CTA per activation row merges the G*k candidates
@@ -914,12 +956,13 @@ struct StreamPlan {
 bool layout_stream(StreamPlan &p, int M, bool lmhead, size_t ring_budget, int tpc, int slice_groups,
                    bool force_defer = false) {
     StreamArgs &a = p.a;
-    const int ng = a.ng;
     const int wbox = min(kChunkGroups, slice_groups + kBoxGroups - 1) / kBoxGroups;
+    const int xsums = a.f.gs == 0 ? 2 : 1;  // activation sums per group and row
     a.w_bytes = (uint32_t)(wbox * kBoxBytes);
     a.cq = wbox;
     a.nq_full = a.K / 256;
-    a.stage_bytes = (uint32_t)align_up((size_t)a.w_bytes + 64u * ng, 1024);
+    // Codes, then the tile's scale rows [16][ngs] (and bias rows).
+    a.stage_bytes = (uint32_t)align_up((size_t)a.w_bytes + (a.f.sym ? 32u : 64u) * a.f.ngs, 1024);
     // As many stages as the byte budget allows: the ring is what keeps HBM busy.
     const int stages = (int)max((size_t)2, min((size_t)kMaxStages, ring_budget / a.stage_bytes));
     a.stages = stages;
@@ -932,7 +975,7 @@ bool layout_stream(StreamPlan &p, int M, bool lmhead, size_t ring_budget, int tp
     a.off_xf = (uint32_t)off;
     off = align_up(off + (size_t)slice_groups * M * 128, 16);
     a.off_xsum = (uint32_t)off;
-    off = align_up(off + (size_t)slice_groups * M * 4, 16);
+    off = align_up(off + (size_t)slice_groups * M * 4 * xsums, 16);
     a.off_red = (uint32_t)off;
     const size_t red_all = (size_t)tpc * kConsumerWarps * kTileRows * M * 4;
     a.defer = (force_defer || red_all <= 32 * 1024) ? 1 : 0;
@@ -949,7 +992,7 @@ bool layout_stream(StreamPlan &p, int M, bool lmhead, size_t ring_budget, int tp
 // two rings in flight), one otherwise.
 int ctas_per_sm(int M) { return M <= 8 ? 2 : 1; }
 
-const void *stream_kernel_ptr(int M, bool lmhead);
+const void *stream_kernel_ptr(int M, bool lmhead, int fmt);
 bool ensure_smem(const void *kern, size_t bytes);
 
 // Clusters of C CTAs (this kernel, this shared memory) that can be resident
@@ -1024,7 +1067,7 @@ bool plan_with_cluster(StreamPlan &p, int C, int slots, int per_sm, bool lmhead)
         // of the layout actually launched (fewer clusters mean more tiles per
         // cluster and possibly a larger layout, so check again).
         for (int iter = 0; iter < 3; ++iter) {
-            const int act = max_active_clusters(stream_kernel_ptr(a.M, lmhead), C, p.smem, ncl);
+            const int act = max_active_clusters(stream_kernel_ptr(a.M, lmhead, fmt_class(a.f)), C, p.smem, ncl);
             if (act >= ncl) break;
             ncl = max(1, act);
             if (!fit_layout(p, lmhead, per_sm, (a.tiles + ncl - 1) / ncl, slice)) return false;
@@ -1034,12 +1077,13 @@ bool plan_with_cluster(StreamPlan &p, int C, int slots, int per_sm, bool lmhead)
     return true;
 }
 
-bool plan_stream(StreamPlan &p, int M, int N, int K, bool lmhead, int k) {
+bool plan_stream(StreamPlan &p, int M, int N, int K, const WFmt &f, bool lmhead, int k) {
     StreamArgs &a = p.a;
     a.M = M;
     a.N = N;
     a.K = K;
     a.k = k;
+    a.f = f;
     a.ng = K / kGroup;
     a.units = (a.ng + 7) / 8;
     a.tiles = (N + kTileRows - 1) / kTileRows;
@@ -1096,7 +1140,7 @@ bool ensure_smem(const void *kern, size_t bytes) {
     return true;
 }
 
-template <int NT, bool LM, bool M1>
+template <int NT, bool LM, bool M1, int FMT>
 int launch_stream(const StreamPlan &p, const uint32_t *qw, bool overlap, cudaStream_t st) {
     CUtensorMap tm3, tm2;
     const uint64_t KW = (uint64_t)p.a.K / 8;
@@ -1110,7 +1154,7 @@ int launch_stream(const StreamPlan &p, const uint32_t *qw, bool overlap, cudaStr
     } else {
         tm3 = tm2;  // never used: every chunk takes the 2-D path
     }
-    auto kern = stream_kernel<NT, LM, M1>;
+    auto kern = stream_kernel<NT, LM, M1, FMT>;
     if (!ensure_smem(reinterpret_cast<const void *>(kern), p.smem)) return W4_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.grid, 1, 1);
@@ -1137,24 +1181,42 @@ int launch_stream(const StreamPlan &p, const uint32_t *qw, bool overlap, cudaStr
     return e == cudaSuccess ? W4A16_OK : W4_ERR_LAUNCH;
 }
 
+// bi == nullptr: symmetric codes.  Fills the scale layout f.
 int check_common(const void *x, const uint32_t *qw, const uint16_t *sc, const uint16_t *bi, int M, int N, int K,
-                 int group) {
-    if (!x || !qw || !sc || !bi) return W4_ERR_NULL;
-    if (group != kGroup) return W4_ERR_GROUP;
+                 int group, WFmt &f) {
+    if (!x || !qw || !sc) return W4_ERR_NULL;
     if (M < 1 || M > 16 || N < 1 || K < kGroup || K % kGroup != 0) return W4_ERR_SHAPE;
-    if (!aligned16(x) || !aligned16(qw) || !aligned16(sc) || !aligned16(bi)) return W4_ERR_ALIGN;
+    if (!make_fmt(f, K, group, bi == nullptr)) return W4_ERR_GROUP;
+    if (!aligned16(x) || !aligned16(qw) || !aligned16(sc) || (bi && !aligned16(bi))) return W4_ERR_ALIGN;
     return W4A16_OK;
+}
+
+template <bool LM, int FMT>
+int launch_stream_f(const StreamPlan &p, const uint32_t *qw, bool ov, cudaStream_t s) {
+    const int M = p.a.M;
+    return M == 1 ? launch_stream<1, LM, true, FMT>(p, qw, ov, s)
+           : M <= 8 ? launch_stream<1, LM, false, FMT>(p, qw, ov, s)
+                    : launch_stream<2, LM, false, FMT>(p, qw, ov, s);
+}
+
+template <bool LM>
+int launch_stream_any(const StreamPlan &p, const uint32_t *qw, bool ov, cudaStream_t s) {
+    const int fmt = fmt_class(p.a.f);
+    return fmt == kFmtG64 ? launch_stream_f<LM, kFmtG64>(p, qw, ov, s)
+           : fmt == kFmtG32 ? launch_stream_f<LM, kFmtG32>(p, qw, ov, s)
+                            : launch_stream_f<LM, kFmtAny>(p, qw, ov, s);
 }
 
 int gemv_impl(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, const uint16_t *bi, uint16_t *y, int M,
               int N, int K, int group, unsigned flags, void *stream) {
-    int st = check_common(x, qw, sc, bi, M, N, K, group);
+    WFmt f;
+    int st = check_common(x, qw, sc, bi, M, N, K, group, f);
     if (st != W4A16_OK) return st;
     if (!y) return W4_ERR_NULL;
     if (!aligned16(y)) return W4_ERR_ALIGN;
     if (flags & ~(unsigned)W4A16_OVERLAP_PREVIOUS) return W4_ERR_SHAPE;
     StreamPlan p;
-    if (!plan_stream(p, M, N, K, false, 1)) return W4_ERR_SHAPE;
+    if (!plan_stream(p, M, N, K, f, false, 1)) return W4_ERR_SHAPE;
     p.a.x = x;
     p.a.sc = sc;
     p.a.bi = bi;
@@ -1162,15 +1224,14 @@ int gemv_impl(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, const u
     p.a.ws = nullptr;
     const bool ov = (flags & W4A16_OVERLAP_PREVIOUS) != 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    return M == 1 ? launch_stream<1, false, true>(p, qw, ov, s)
-                  : M <= 8 ? launch_stream<1, false, false>(p, qw, ov, s) : launch_stream<2, false, false>(p, qw, ov, s);
+    return launch_stream_any<false>(p, qw, ov, s);
 }
 
 int lmhead_impl(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, const uint16_t *bi, int M, int N, int K,
-                int group, int k, int32_t *idx, float *val, uint64_t *ws, size_t ws_bytes, unsigned flags,
+                const WFmt &f, int k, int32_t *idx, float *val, uint64_t *ws, size_t ws_bytes, unsigned flags,
                 void *stream) {
     StreamPlan p;
-    if (!plan_stream(p, M, N, K, true, k)) return W4_ERR_SHAPE;
+    if (!plan_stream(p, M, N, K, f, true, k)) return W4_ERR_SHAPE;
     const int G = p.grid;
     if ((long long)G > lm_max_blocks(N, k)) return W4_ERR_SHAPE;
     if (ws_bytes < (size_t)M * G * k * sizeof(uint64_t)) return W4_ERR_WORKSPACE;
@@ -1181,8 +1242,7 @@ int lmhead_impl(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, const
     p.a.ws = ws;
     const bool ov = (flags & W4A16_OVERLAP_PREVIOUS) != 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int st = M == 1 ? launch_stream<1, true, true>(p, qw, ov, s)
-                   : M <= 8 ? launch_stream<1, true, false>(p, qw, ov, s) : launch_stream<2, true, false>(p, qw, ov, s);
+    const int st = launch_stream_any<true>(p, qw, ov, s);
     if (st != W4A16_OK) return st;
     // Pass 2 is launched as a programmatic dependent: its launch overlaps pass 1
     // and it waits (griddepcontrol.wait) for pass 1's results.
@@ -1201,8 +1261,8 @@ int lmhead_impl(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, const
 }
 
 int lmhead_checks(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, const uint16_t *bi, int M, int N, int K,
-                  int group, int k, int32_t *idx, float *val) {
-    int st = check_common(x, qw, sc, bi, M, N, K, group);
+                  int group, int k, int32_t *idx, float *val, WFmt &f) {
+    int st = check_common(x, qw, sc, bi, M, N, K, group, f);
     if (st != W4A16_OK) return st;
     if (!idx || !val) return W4_ERR_NULL;
     if (k < 1 || k > 64 || k > N || (long long)N * k > 16777216LL) return W4_ERR_SHAPE;
@@ -1211,11 +1271,14 @@ int lmhead_checks(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, con
 }
 
 // Shared-memory layout of one sequence launch; false if it cannot fit.
-bool plan_seq(SeqParams &P, size_t &smem, int ng_max, int ntl_max) {
+// sc_max: the largest scale (and bias) bytes of a tile row block over the
+// operations; xs_max: the most activation sums per row (groups, twice for
+// group 32).
+bool plan_seq(SeqParams &P, size_t &smem, int ng_max, size_t sc_max, int xs_max, int ntl_max) {
     const int M = P.M;
     P.w_bytes = (uint32_t)(kChunkGroups / kBoxGroups) * kBoxBytes;
-    P.stage_bytes = (uint32_t)align_up((size_t)P.w_bytes + 64u * ng_max, 1024);
-    const size_t fixed = align_up((size_t)ng_max * M * 128, 16) + align_up((size_t)ng_max * M * 4, 16) +
+    P.stage_bytes = (uint32_t)align_up((size_t)P.w_bytes + sc_max, 1024);
+    const size_t fixed = align_up((size_t)ng_max * M * 128, 16) + align_up((size_t)xs_max * M * 4, 16) +
                          align_up((size_t)ntl_max * kSeqTeamWarps * kTileRows * M * 4, 16) + 16 * kMaxStages + 16 + 1024;
     if (fixed + 2 * (size_t)P.stage_bytes > (size_t)kMaxSmem) return false;
     P.stages = (int)min((size_t)kMaxStages, ((size_t)kMaxSmem - fixed) / P.stage_bytes);
@@ -1223,7 +1286,7 @@ bool plan_seq(SeqParams &P, size_t &smem, int ng_max, int ntl_max) {
     P.off_xf = (uint32_t)off;
     off = align_up(off + (size_t)ng_max * M * 128, 16);
     P.off_xsum = (uint32_t)off;
-    off = align_up(off + (size_t)ng_max * M * 4, 16);
+    off = align_up(off + (size_t)xs_max * M * 4, 16);
     P.off_red = (uint32_t)off;
     off = align_up(off + (size_t)ntl_max * kSeqTeamWarps * kTileRows * M * 4, 16);
     P.off_bar = (uint32_t)off;
@@ -1264,6 +1327,12 @@ size_t seq_sources(const w4_gemv_op *ops, int nops, int M, int *src, bool *tagge
     return bytes;
 }
 
+template <int FMT>
+const void *seq_kernel_ptr(int M) {
+    return M == 1 ? (const void *)seq_kernel<1, true, FMT>
+           : M <= 8 ? (const void *)seq_kernel<1, false, FMT> : (const void *)seq_kernel<2, false, FMT>;
+}
+
 int seq_launch(const w4_gemv_op *ops, int nops, int M, unsigned *ws, uint8_t *tagbuf, size_t tag_bytes,
                cudaStream_t st) {
     static SeqParams P;  // large: kept off the stack (calls are host-serialised per process)
@@ -1283,7 +1352,8 @@ int seq_launch(const w4_gemv_op *ops, int nops, int M, unsigned *ws, uint8_t *ta
             toff += align_up((size_t)M * ops[i].N * 4, 16);
         }
     }
-    int ng_max = 1, ntl_max = 1;
+    int ng_max = 1, ntl_max = 1, xs_max = 1;
+    size_t sc_max = 0;
     for (int i = 0; i < nops; ++i) {
         const w4_gemv_op &o = ops[i];
         SeqOp &d = P.ops[i];
@@ -1300,6 +1370,10 @@ int seq_launch(const w4_gemv_op *ops, int nops, int M, unsigned *ws, uint8_t *ta
         const int nq = o.K / 256;
         d.cq = min(kChunkGroups / kBoxGroups, nq);
         ng_max = max(ng_max, o.K / kGroup);
+        // Checked by the caller.
+        make_fmt(d.f, o.K, o.group ? o.group : kGroup, o.biases == nullptr);
+        sc_max = std::max(sc_max, (size_t)(d.f.sym ? 32 : 64) * d.f.ngs);
+        xs_max = max(xs_max, (o.K / kGroup) * (d.f.gs == 0 ? 2 : 1));
         ntl_max = max(ntl_max, ((o.N + kTileRows - 1) / kTileRows + G - 1) / G);
         const uint64_t KW = (uint64_t)o.K / 8;
         if (!make_map_3d(&P.maps[i], CU_TENSOR_MAP_DATA_TYPE_UINT32, o.qweight, 32, (uint64_t)o.N, (uint64_t)nq,
@@ -1313,9 +1387,11 @@ int seq_launch(const w4_gemv_op *ops, int nops, int M, unsigned *ws, uint8_t *ta
     for (int i = 1; i < nops; ++i)
         if (P.ops[i].wait_prev && !P.ops[i].xt) P.publish = 1;
     size_t smem = 0;
-    if (!plan_seq(P, smem, ng_max, ntl_max)) return W4_ERR_SHAPE;
-    const void *kern = M == 1 ? (const void *)seq_kernel<1, true>
-                       : M <= 8 ? (const void *)seq_kernel<1, false> : (const void *)seq_kernel<2, false>;
+    if (!plan_seq(P, smem, ng_max, sc_max, xs_max, ntl_max)) return W4_ERR_SHAPE;
+    const int fmt = fmt_class(P.ops[0].f);  // the same for every operation of a launch
+    const void *kern = fmt == kFmtG64   ? seq_kernel_ptr<kFmtG64>(M)
+                       : fmt == kFmtG32 ? seq_kernel_ptr<kFmtG32>(M)
+                                        : seq_kernel_ptr<kFmtAny>(M);
     if (!ensure_smem(kern, smem)) return W4_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G, 1, 1);
@@ -1327,9 +1403,8 @@ int seq_launch(const w4_gemv_op *ops, int nops, int M, unsigned *ws, uint8_t *ta
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = M == 1  ? cudaLaunchKernelEx(&cfg, seq_kernel<1, true>, P)
-                          : M <= 8 ? cudaLaunchKernelEx(&cfg, seq_kernel<1, false>, P)
-                                   : cudaLaunchKernelEx(&cfg, seq_kernel<2, false>, P);
+    void *args[] = {&P};
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, kern, args);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return W4_ERR_LAUNCH;
@@ -1361,11 +1436,12 @@ extern "C" size_t lm_head_workspace_bytes(int M, int N, int k) {
 extern "C" int lm_head_argmax_topk(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
                                    const uint16_t *biases, int M, int N, int K, int group, int k, int32_t *idx,
                                    float *val, void *workspace, size_t workspace_bytes, void *stream) {
-    int st = lmhead_checks(x, qweight, scales, biases, M, N, K, group, k, idx, val);
+    WFmt f;
+    int st = lmhead_checks(x, qweight, scales, biases, M, N, K, group, k, idx, val, f);
     if (st != W4A16_OK) return st;
     if (!workspace || workspace_bytes < lm_head_workspace_bytes(M, N, k)) return W4_ERR_WORKSPACE;
     if (!aligned16(workspace)) return W4_ERR_ALIGN;
-    return lmhead_impl(x, qweight, scales, biases, M, N, K, group, k, idx, val,
+    return lmhead_impl(x, qweight, scales, biases, M, N, K, f, k, idx, val,
                        reinterpret_cast<uint64_t *>(workspace), workspace_bytes, 0u, stream);
 }
 
@@ -1373,13 +1449,29 @@ extern "C" int lm_head_argmax_topk_ex(const uint16_t *x, const uint32_t *qweight
                                       const uint16_t *biases, int M, int N, int K, int group, int k, int32_t *idx,
                                       float *val, void *workspace, size_t workspace_bytes, unsigned flags,
                                       void *stream) {
-    int st = lmhead_checks(x, qweight, scales, biases, M, N, K, group, k, idx, val);
+    WFmt f;
+    int st = lmhead_checks(x, qweight, scales, biases, M, N, K, group, k, idx, val, f);
     if (st != W4A16_OK) return st;
     if (flags & ~(unsigned)W4A16_OVERLAP_PREVIOUS) return W4_ERR_SHAPE;
     if (!workspace || workspace_bytes < lm_head_workspace_bytes(M, N, k)) return W4_ERR_WORKSPACE;
     if (!aligned16(workspace)) return W4_ERR_ALIGN;
-    return lmhead_impl(x, qweight, scales, biases, M, N, K, group, k, idx, val,
+    return lmhead_impl(x, qweight, scales, biases, M, N, K, f, k, idx, val,
                        reinterpret_cast<uint64_t *>(workspace), workspace_bytes, flags, stream);
+}
+
+// Scale-layout class of an operation (its arguments need not be valid yet).
+static int seq_op_class(const w4_gemv_op &o) {
+    const int group = o.group ? o.group : kGroup;
+    return group == 32 ? kFmtG32 : (group == kGroup && o.biases) ? kFmtG64 : kFmtAny;
+}
+
+// Operations of the next launch of a list: up to kSeqMaxOps of one scale-layout
+// class (one kernel variant per launch).
+static int seq_launch_ops(const w4_gemv_op *ops, int nops) {
+    const int c = seq_op_class(ops[0]);
+    int n = 1;
+    while (n < nops && n < kSeqMaxOps && seq_op_class(ops[n]) == c) ++n;
+    return n;
 }
 
 extern "C" size_t w4_gemv_seq_workspace_bytes(void) { return kSeqCounterBytes; }
@@ -1391,8 +1483,8 @@ extern "C" size_t w4_gemv_seq_workspace_bytes_ex(const w4_gemv_op *ops, int nops
     static int src[kSeqMaxOps];
     static bool tagged[kSeqMaxOps];
     size_t most = 0;
-    for (int first = 0; first < nops; first += kSeqMaxOps) {
-        const int n = min(kSeqMaxOps, nops - first);
+    for (int first = 0, n = 0; first < nops; first += n) {
+        n = seq_launch_ops(ops + first, nops - first);
         most = std::max(most, seq_sources(ops + first, n, M, src, tagged));
     }
     return kSeqCounterBytes + most;
@@ -1406,15 +1498,17 @@ extern "C" int w4_gemv_seq(const w4_gemv_op *ops, int nops, int M, void *workspa
     if (nops < 1 || M < 1 || M > 16 || flags != 0) return W4_ERR_SHAPE;
     for (int i = 0; i < nops; ++i) {
         const w4_gemv_op &o = ops[i];
-        int st = check_common(o.x, o.qweight, o.scales, o.biases, M, o.N, o.K, kGroup);
+        WFmt f;
+        if (o.group < 0) return W4_ERR_GROUP;
+        int st = check_common(o.x, o.qweight, o.scales, o.biases, M, o.N, o.K, o.group ? o.group : kGroup, f);
         if (st != W4A16_OK) return st;
         if (!o.y) return W4_ERR_NULL;
         if (!aligned16(o.y)) return W4_ERR_ALIGN;
         if (o.K % 256 != 0) return W4_ERR_SHAPE;  // whole 128-byte quads per row
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    for (int first = 0; first < nops; first += kSeqMaxOps) {
-        const int n = min(kSeqMaxOps, nops - first);
+    for (int first = 0, n = 0; first < nops; first += n) {
+        n = seq_launch_ops(ops + first, nops - first);
         uint8_t *ws8 = reinterpret_cast<uint8_t *>(workspace);
         const int st = seq_launch(ops + first, n, M, reinterpret_cast<unsigned *>(workspace),
                                   workspace_bytes > kSeqCounterBytes ? ws8 + kSeqCounterBytes : nullptr,
@@ -1463,12 +1557,13 @@ void *noalloc_scratch() {
 extern "C" int lm_head_argmax_topk_noalloc(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
                                            const uint16_t *biases, int M, int N, int K, int group, int k,
                                            int32_t *idx, float *val, void *stream) {
-    int st = lmhead_checks(x, qweight, scales, biases, M, N, K, group, k, idx, val);
+    WFmt f;
+    int st = lmhead_checks(x, qweight, scales, biases, M, N, K, group, k, idx, val, f);
     if (st != W4A16_OK) return st;
     const size_t need = lm_head_workspace_bytes(M, N, k);
     if (need == 0 || need > kNoAllocScratchBytes) return W4_ERR_WORKSPACE;
     void *scratch = noalloc_scratch();
     if (!scratch) return W4_ERR_DEVICE;
-    return lmhead_impl(x, qweight, scales, biases, M, N, K, group, k, idx, val,
+    return lmhead_impl(x, qweight, scales, biases, M, N, K, f, k, idx, val,
                        reinterpret_cast<uint64_t *>(scratch), kNoAllocScratchBytes, 0u, stream);
 }

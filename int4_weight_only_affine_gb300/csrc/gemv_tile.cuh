@@ -1,6 +1,11 @@
 // Consumer-side arithmetic of the W4A16 GEMV kernels: activation staging in
 // MMA fragment order and the per-group tensor-core dot products with the
 // affine step folded in.  Shared by the streaming and projection-list kernels.
+//
+// Here a "group" is a 64-k block of codes (8 words of a row), the unit the
+// kernels step by.  The quantisation group (WFmt) may span several blocks
+// (group 128, 256, ...: the blocks share a scale) or half of one (group 32:
+// the G32 variants keep the two halves' sums apart).
 #pragma once
 
 #include "common.cuh"
@@ -34,7 +39,8 @@ __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a -
 // 2h+1), activation row c and lane quad t, four words are stored at
 //   xf[(((gl*2 + h)*M + c)*4 + t)*4 ...]  =  {b0(2h), b1(2h), b0(2h+1), b1(2h+1)}
 // with b0(j) = (x[c][k+j], x[c][k+j+4]), b1(j) = (x[c][k+8+j], x[c][k+12+j]),
-// k = 64G + 16t.  xsum[gl*M + c] = sum of the group's 64 activations (fp32).
+// k = 64G + 16t.  xsum[gl*M + c] = sum of the group's 64 activations (fp32);
+// G32: xsum[(gl*M + c)*2 + h] = sum of its half h (k = 64G + 32h ...).
 // The operands of the MMAs for j = 1 and 3 are stored divided by 16 (exact
 // for |x| >= 2^-10; below that the halving error is at most 2^-25), because
 // their codes are extracted 4 bits higher (see group_mma).
@@ -129,7 +135,7 @@ __device__ __forceinline__ float item_store(uint4 lo, uint4 hi, int gl, int c, i
 // read-only path, for activations written earlier in the same kernel).
 // A thread takes kB items (it, it + nthreads, ...) together, so their loads
 // are in flight at once.
-template <bool TAGGED, int kB = 2>
+template <bool TAGGED, int kB = 2, bool G32 = false>
 __device__ void stage_activations_t(const uint16_t *__restrict__ x, const uint32_t *xt, uint32_t tag, int M, int K,
                                     int g0, int ngl, uint32_t *xf, float *xsum, int tid, int nthreads, bool coherent,
                                     volatile int *abort) {
@@ -151,17 +157,23 @@ __device__ void stage_activations_t(const uint16_t *__restrict__ x, const uint32
             float part = 0.f;
             if (it < items) part = item_store(lo[u], hi[u], (it >> 2) / M, (it >> 2) % M, it & 3, M, xf);
             part += __shfl_xor_sync(0xffffffffu, part, 1);
-            part += __shfl_xor_sync(0xffffffffu, part, 2);
-            if (it < items && (it & 3) == 0) xsum[it >> 2] = part;
+            if (G32) {
+                // Items t = 0, 1 hold the first 32 activations, t = 2, 3 the rest.
+                if (it < items && (it & 1) == 0) xsum[((it >> 2) << 1) + ((it >> 1) & 1)] = part;
+            } else {
+                part += __shfl_xor_sync(0xffffffffu, part, 2);
+                if (it < items && (it & 3) == 0) xsum[it >> 2] = part;
+            }
         }
     }
 }
 
-template <int kB = 2>
+template <int kB = 2, bool G32 = false>
 __device__ __forceinline__ void stage_activations(const uint16_t *__restrict__ x, int M, int K, int g0, int ngl,
                                                   uint32_t *xf, float *xsum, int tid, int nthreads,
                                                   bool coherent = false) {
-    stage_activations_t<false, kB>(x, nullptr, 0u, M, K, g0, ngl, xf, xsum, tid, nthreads, coherent, nullptr);
+    stage_activations_t<false, kB, G32>(x, nullptr, 0u, M, K, g0, ngl, xf, xsum, tid, nthreads, coherent,
+                                        nullptr);
 }
 
 template <int NT>
@@ -245,6 +257,83 @@ __device__ __forceinline__ void group_mma(Acc<NT> &acc, uint2 wa, uint2 wb, floa
     }
 }
 
+// Group 32: a 64-k group holds two quantisation groups, k 0..31 in the MMA
+// k slots of lanes t = 0, 1 and k 32..63 in those of lanes t = 2, 3.
+// sa[h], sb[h], ba[h], bb[h]: scale and bias of half h for rows g and g+8;
+// xs[c*2 + h]: half sums of activation row c.
+// M1: B column 0 keeps the first half (lanes t >= 2 of column 0 pass zero)
+// and column 1 the second half (fed by the lanes of column 1 with t < 2
+// zeroed), so the four MMAs give both halves at once: `hmask` is that
+// lane's mask.  M > 1: each fragment runs twice, masked to either half.
+template <int NT, bool M1>
+__device__ __forceinline__ void group_mma_g32(Acc<NT> &acc, uint2 wa, uint2 wb, const float (&sa)[2],
+                                              const float (&sb)[2], const float (&ba)[2], const float (&bb)[2],
+                                              const uint4 *xl, int xd1, const float *xs, int M, int lt,
+                                              uint32_t hmask) {
+    uint32_t a0[4], a1[4], a2[4], a3[4];
+    const uint32_t w8[4] = {wa.x >> 8, wb.x >> 8, wa.y >> 8, wb.y >> 8};
+    a0[0] = wa.x & kNibPair;
+    a1[0] = wb.x & kNibPair;
+    a2[0] = wa.y & kNibPair;
+    a3[0] = wb.y & kNibPair;
+    a0[1] = wa.x & kNibPairHi;
+    a1[1] = wb.x & kNibPairHi;
+    a2[1] = wa.y & kNibPairHi;
+    a3[1] = wb.y & kNibPairHi;
+    a0[2] = w8[0] & kNibPair;
+    a1[2] = w8[1] & kNibPair;
+    a2[2] = w8[2] & kNibPair;
+    a3[2] = w8[3] & kNibPair;
+    a0[3] = w8[0] & kNibPairHi;
+    a1[3] = w8[1] & kNibPairHi;
+    a2[3] = w8[2] & kNibPairHi;
+    a3[3] = w8[3] & kNibPairHi;
+    if (M1) {
+        const uint4 f0 = xl[0], f1 = xl[4];
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_16816(d, a0[0], a1[0], a2[0], a3[0], f0.x & hmask, f0.y & hmask);
+        mma_16816(d, a0[1], a1[1], a2[1], a3[1], f0.z & hmask, f0.w & hmask);
+        mma_16816(d, a0[2], a1[2], a2[2], a3[2], f1.x & hmask, f1.y & hmask);
+        mma_16816(d, a0[3], a1[3], a2[3], a3[3], f1.z & hmask, f1.w & hmask);
+        // Lanes t = 0: d[0], d[2] = first half of rows g, g+8; d[1], d[3] = second.
+        ffma2(acc.s[0][0], acc.s[0][2], sa[0], sb[0], d[0], d[2]);
+        ffma2(acc.s[0][0], acc.s[0][2], sa[1], sb[1], d[1], d[3]);
+        ffma2(acc.b[0][0], acc.b[0][2], ba[0], bb[0], xs[0], xs[0]);
+        ffma2(acc.b[0][0], acc.b[0][2], ba[1], bb[1], xs[1], xs[1]);
+        return;
+    }
+    const uint32_t lo = lt < 2 ? 0xffffffffu : 0u, hi = ~lo;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int xo = nt ? xd1 : 0;
+        const uint4 f0 = xl[xo];
+        const uint4 f1 = xl[xo + M * 4];
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_16816(d0, a0[0], a1[0], a2[0], a3[0], f0.x & lo, f0.y & lo);
+        mma_16816(d0, a0[1], a1[1], a2[1], a3[1], f0.z & lo, f0.w & lo);
+        mma_16816(d0, a0[2], a1[2], a2[2], a3[2], f1.x & lo, f1.y & lo);
+        mma_16816(d0, a0[3], a1[3], a2[3], a3[3], f1.z & lo, f1.w & lo);
+        mma_16816(d1, a0[0], a1[0], a2[0], a3[0], f0.x & hi, f0.y & hi);
+        mma_16816(d1, a0[1], a1[1], a2[1], a3[1], f0.z & hi, f0.w & hi);
+        mma_16816(d1, a0[2], a1[2], a2[2], a3[2], f1.x & hi, f1.y & hi);
+        mma_16816(d1, a0[3], a1[3], a2[3], a3[3], f1.z & hi, f1.w & hi);
+        const int c0 = min(nt * 8 + 2 * lt, M - 1), c1 = min(nt * 8 + 2 * lt + 1, M - 1);
+        ffma2(acc.s[nt][0], acc.s[nt][2], sa[0], sb[0], d0[0], d0[2]);
+        ffma2(acc.s[nt][0], acc.s[nt][2], sa[1], sb[1], d1[0], d1[2]);
+        ffma2(acc.s[nt][1], acc.s[nt][3], sa[0], sb[0], d0[1], d0[3]);
+        ffma2(acc.s[nt][1], acc.s[nt][3], sa[1], sb[1], d1[1], d1[3]);
+        ffma2(acc.b[nt][0], acc.b[nt][2], ba[0], bb[0], xs[2 * c0], xs[2 * c0]);
+        ffma2(acc.b[nt][0], acc.b[nt][2], ba[1], bb[1], xs[2 * c0 + 1], xs[2 * c0 + 1]);
+        ffma2(acc.b[nt][1], acc.b[nt][3], ba[0], bb[0], xs[2 * c1], xs[2 * c1]);
+        ffma2(acc.b[nt][1], acc.b[nt][3], ba[1], bb[1], xs[2 * c1 + 1], xs[2 * c1 + 1]);
+    }
+}
+
+// The lane's B mask of the group-32 M1 path (see group_mma_g32).
+__device__ __forceinline__ uint32_t g32_m1_mask(int lg, int lt) {
+    return ((lt >> 1) == (lg & 1)) ? 0xffffffffu : 0u;
+}
+
 // Shared-memory byte offsets, within a stage, of the words a lane reads for
 // group j (0..3) of box `box`: row g, 16-byte chunk 2j + t/2 under the
 // 128-byte swizzle (chunk index XOR row % 8), word pair t % 2.  Row g+8 is
@@ -264,35 +353,146 @@ __device__ __forceinline__ void unpack4h(uint2 v, float (&f)[4]) {
     f[3] = hi.y;
 }
 
-// The warp's box of a stage: n (1..4) consecutive groups of a 16-row tile.
-// st: the stage; sp: the tile's scales [16][ng] (biases follow);
-// g: the box's first group (index into a scale row); xl: the lane's staged
-// activation fragments of that group (see group_mma); xs: its activation
-// sums.  FULL: n == 4 and ng % 4 == 0, so a lane's four scales of a row are
-// one aligned 8-byte word.
-template <int NT, bool M1, bool FULL>
-__device__ __forceinline__ void box_mma(Acc<NT> &acc, const uint8_t *st, const int (&off)[4], const uint16_t *sp,
-                                        int ng, int g, int n, const uint4 *xl, int xd1, const float *xs, int M,
-                                        int lg, int lt) {
-    const uint16_t *sa = sp + lg * ng + g;  // scales of row g; row g+8 is 8 rows on
-    const uint16_t *ba = sa + kTileRows * ng;
-    float fsa[4], fsb[4], fba[4], fbb[4];
-    if (FULL) {
-        unpack4h(*reinterpret_cast<const uint2 *>(sa), fsa);
-        unpack4h(*reinterpret_cast<const uint2 *>(sa + 8 * ng), fsb);
-        unpack4h(*reinterpret_cast<const uint2 *>(ba), fba);
-        unpack4h(*reinterpret_cast<const uint2 *>(ba + 8 * ng), fbb);
-    } else {
+// Whether a full box (4 groups from a multiple of 4) can read its scales as
+// one aligned vector: the rows' scale arrays keep that alignment.  (For
+// group 64 this is K % 256 == 0.)
+__host__ __device__ inline bool box_vec_ok(const WFmt &f) {
+    if (f.gs == 0) return f.ngs % 8 == 0;  // 8 scales per row: 16 bytes
+    if (f.gs == 1) return f.ngs % 4 == 0;  // 4 scales: 8 bytes
+    if (f.gs == 2) return f.ngs % 2 == 0;  // 2 scales: 4 bytes
+    return true;                           // one scale
+}
+
+// Scale and bias of groups g .. g+3 (entries j < n) of rows g and g+8 (lane
+// row lg): one quantisation group spans 1 << (gs - 1) groups (gs >= 1).
+// sp: the tile's scales [16][ngs], followed by its biases unless f.sym
+// (then bias = -8 * scale, exact in fp32).
+template <bool FULL>
+__device__ __forceinline__ void box_scales(float (&fsa)[4], float (&fsb)[4], float (&fba)[4], float (&fbb)[4],
+                                           const uint16_t *sp, const WFmt &f, int g, int n, int lg) {
+    const int ngs = f.ngs, sh = f.gs - 1;
+    const uint16_t *ra = sp + lg * ngs;
+    const uint16_t *rb = ra + 8 * ngs;
+    auto load = [&](const uint16_t *r, float (&o)[4]) {
+        if (FULL && sh == 0) {
+            unpack4h(*reinterpret_cast<const uint2 *>(r + g), o);
+        } else if (FULL && sh == 1) {
+            const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(r + (g >> 1)));
+            o[0] = o[1] = v.x;
+            o[2] = o[3] = v.y;
+        } else if (FULL) {
+            o[0] = o[1] = o[2] = o[3] = h2f(r[g >> sh]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[j] = h2f(r[(g + (j < n ? j : 0)) >> sh]);
+        }
+    };
+    load(ra, fsa);
+    load(rb, fsb);
+    if (f.sym) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int jj = j < n ? j : 0;
-            fsa[j] = h2f(sa[jj]);
-            fsb[j] = h2f(sa[8 * ng + jj]);
-            fba[j] = h2f(ba[jj]);
-            fbb[j] = h2f(ba[8 * ng + jj]);
+            fba[j] = -8.f * fsa[j];
+            fbb[j] = -8.f * fsb[j];
         }
+    } else {
+        load(ra + kTileRows * ngs, fba);
+        load(rb + kTileRows * ngs, fbb);
     }
+}
+
+// Group 32: the two halves' scales (and biases) of groups g .. g+3.
+template <bool FULL>
+__device__ __forceinline__ void box_scales_g32(float (&fsa)[4][2], float (&fsb)[4][2], float (&fba)[4][2],
+                                               float (&fbb)[4][2], const uint16_t *sp, const WFmt &f, int g, int n,
+                                               int lg) {
+    const int ngs = f.ngs;
+    const uint16_t *ra = sp + lg * ngs;
+    const uint16_t *rb = ra + 8 * ngs;
+    auto load = [&](const uint16_t *r, float (&o)[4][2]) {
+        if (FULL) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(r + 2 * g);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 p = __half22float2(*reinterpret_cast<const __half2 *>(&w[j]));
+                o[j][0] = p.x;
+                o[j][1] = p.y;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int jj = j < n ? j : 0;
+                o[j][0] = h2f(r[2 * (g + jj)]);
+                o[j][1] = h2f(r[2 * (g + jj) + 1]);
+            }
+        }
+    };
+    load(ra, fsa);
+    load(rb, fsb);
+    if (f.sym) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                fba[j][h] = -8.f * fsa[j][h];
+                fbb[j][h] = -8.f * fsb[j][h];
+            }
+    } else {
+        load(ra + kTileRows * ngs, fba);
+        load(rb + kTileRows * ngs, fbb);
+    }
+}
+
+// The warp's box of a stage: n (1..4) consecutive groups of a 16-row tile.
+// st: the stage; sp: the tile's scales and biases (see box_scales);
+// g: the box's first group; xl: the lane's staged activation fragments of
+// that group (see group_mma); xs: its activation sums.  FULL: n == 4 and
+// box_vec_ok(f).  FMT: kFmtG64 reads one scale and one bias per group
+// (f.ngs groups per row), kFmtAny follows f, kFmtG32 is the group-32 variant
+// (hmask: see group_mma_g32).
+template <int NT, bool M1, bool FULL, int FMT>
+__device__ __forceinline__ void box_mma(Acc<NT> &acc, const uint8_t *st, const int (&off)[4], const uint16_t *sp,
+                                        const WFmt &f, int g, int n, const uint4 *xl, int xd1, const float *xs,
+                                        int M, int lg, int lt, uint32_t hmask = 0u) {
     const int xstep = 2 * M * 4;  // uint4 words of staged activations per group
+    if (FMT == kFmtG32) {
+        float fsa[4][2], fsb[4][2], fba[4][2], fbb[4][2];
+        box_scales_g32<FULL>(fsa, fsb, fba, fbb, sp, f, g, n, lg);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (FULL || j < n) {
+                const uint2 wa = *reinterpret_cast<const uint2 *>(st + off[j]);
+                const uint2 wb = *reinterpret_cast<const uint2 *>(st + off[j] + 8 * 128);
+                group_mma_g32<NT, M1>(acc, wa, wb, fsa[j], fsb[j], fba[j], fbb[j], xl + j * (M1 ? 8 : xstep), xd1,
+                                      xs + j * 2 * M, M, lt, hmask);
+            }
+        }
+        return;
+    }
+    float fsa[4], fsb[4], fba[4], fbb[4];
+    if (FMT == kFmtG64) {
+        const int ng = f.ngs;
+        const uint16_t *sa = sp + lg * ng + g;  // scales of row g; row g+8 is 8 rows on
+        const uint16_t *ba = sa + kTileRows * ng;
+        if (FULL) {
+            unpack4h(*reinterpret_cast<const uint2 *>(sa), fsa);
+            unpack4h(*reinterpret_cast<const uint2 *>(sa + 8 * ng), fsb);
+            unpack4h(*reinterpret_cast<const uint2 *>(ba), fba);
+            unpack4h(*reinterpret_cast<const uint2 *>(ba + 8 * ng), fbb);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int jj = j < n ? j : 0;
+                fsa[j] = h2f(sa[jj]);
+                fsb[j] = h2f(sa[8 * ng + jj]);
+                fba[j] = h2f(ba[jj]);
+                fbb[j] = h2f(ba[8 * ng + jj]);
+            }
+        }
+    } else {
+        box_scales<FULL>(fsa, fsb, fba, fbb, sp, f, g, n, lg);
+    }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         if (FULL || j < n) {

@@ -6,6 +6,9 @@ baseline / reference arm may import this package.  It loads
 its plain binary64 loops for numpy arrays.  It shares no code with the CUDA
 library and never imports it.
 
+Weights are affine (w = scale*q + bias) or, with ``biases=None``, symmetric
+(w = scale*(q - 8)); ``group`` is the quantisation group along K.
+
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (exhaustive binary16 decode, correctly rounded encode against numpy and
 Fraction arithmetic, exact-rational brute force, closed forms, invariants).
@@ -79,6 +82,11 @@ def _bits16(a) -> np.ndarray:
     return np.ascontiguousarray(a)
 
 
+def _pb(biases):
+    """Pointer to the biases, or NULL for symmetric codes (biases None)."""
+    return None if biases is None else _p(_bits16(biases))
+
+
 def _u32(a) -> np.ndarray:
     a = np.ascontiguousarray(np.asarray(a))
     assert a.dtype == np.uint32
@@ -109,7 +117,7 @@ def unpack(qweight, N: int, K: int) -> np.ndarray:
 def dequant_exact_rows(qweight, scales, biases, K: int, rows, group: int = 64) -> np.ndarray:
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
     w = np.empty((len(rows), K), dtype=np.float64)
-    _load().orc_dequant_exact_rows(_p(_u32(qweight)), _p(_bits16(scales)), _p(_bits16(biases)),
+    _load().orc_dequant_exact_rows(_p(_u32(qweight)), _p(_bits16(scales)), _pb(biases),
                                    K, group, _p(rows), len(rows), _p(w))
     return w
 
@@ -117,7 +125,7 @@ def dequant_exact_rows(qweight, scales, biases, K: int, rows, group: int = 64) -
 def dequant_f16_t(qweight, scales, biases, N: int, K: int, group: int = 64) -> np.ndarray:
     """Transposed binary16 scratch as uint16 bits, shape [K][N]."""
     w16 = np.empty((K, N), dtype=np.uint16)
-    _load().orc_dequant_f16_t(_p(_u32(qweight)), _p(_bits16(scales)), _p(_bits16(biases)),
+    _load().orc_dequant_f16_t(_p(_u32(qweight)), _p(_bits16(scales)), _pb(biases),
                               N, K, group, _p(w16))
     return w16
 
@@ -126,7 +134,7 @@ def dequant_f16_rows(qweight, scales, biases, K: int, rows, group: int = 64) -> 
     """Rows ``rows`` of the dequantised weight as binary16 bits, shape [len(rows)][K]."""
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
     out = np.empty((len(rows), K), dtype=np.uint16)
-    _load().orc_dequant_f16_rows(_p(_u32(qweight)), _p(_bits16(scales)), _p(_bits16(biases)),
+    _load().orc_dequant_f16_rows(_p(_u32(qweight)), _p(_bits16(scales)), _pb(biases),
                                  K, group, _p(rows), len(rows), _p(out))
     return out
 
@@ -138,7 +146,7 @@ def gemv_rows(x, qweight, scales, biases, K: int, rows, group: int = 64):
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
     y = np.empty((M, len(rows)), dtype=np.float64)
     ad = np.empty((M, len(rows)), dtype=np.float64)
-    _load().orc_gemv_rows(_p(x), _p(_u32(qweight)), _p(_bits16(scales)), _p(_bits16(biases)),
+    _load().orc_gemv_rows(_p(x), _p(_u32(qweight)), _p(_bits16(scales)), _pb(biases),
                           M, K, group, _p(rows), len(rows), _p(y), _p(ad))
     return y, ad
 

@@ -19,16 +19,24 @@
  *  - "engine-mlx", "Tech details": models in the MLX 4-bit quantised format.
  *  - "Engineering investigation ... 10x faster?", "Selective quantization":
  *    nn.quantize with affine quantisation, group size 64.
+ *  - "The inference engine - Mojo 1.0 on Metal", "What's inside the engine
+ *    today" and the appendix on porting MLX's kernels: that engine's own
+ *    weights are symmetric int4 in groups of 128 (a scale, no bias).
  *
  * Readings (the pages print neither the formula nor the packing):
- *  - affine dequantisation per group of G = 64 consecutive k:
+ *  - affine dequantisation per group of G consecutive k (G = 64 in the
+ *    workloads; any G dividing K here):
  *        w[n][k] = scale[n][k/G] * q[n][k] + bias[n][k/G],  q in 0..15;
+ *  - symmetric codes (no bias array, passed as NULL): the code is a signed
+ *    4-bit value stored with offset 8,
+ *        w[n][k] = scale[n][k/G] * (q[n][k] - 8);
  *  - qweight is uint32 [N][K/8]; word j of row n holds q[n][8j+i] in bits
  *    4i..4i+3 (lowest nibble = lowest k), the MLX packing order;
  *  - scales and biases are binary16 [N][K/G], row-major;
  *  - the dequantised half scratch is the correctly rounded (round to nearest,
- *    ties to even) binary16 of the exact real scale*q + bias, stored
- *    transposed as w16[K][N];
+ *    ties to even) binary16 of the exact real scale*q + bias (or
+ *    scale*(q - 8)), stored transposed as w16[K][N]; a zero result keeps the
+ *    sign binary64 arithmetic gives it;
  *  - token selection orders logits by value, descending, ties to the lowest
  *    index.
  *
@@ -114,13 +122,16 @@ void orc_unpack(const uint32_t *qweight, int N, int K, uint8_t *q)
         }
 }
 
-/* Exact dequantised weight of one element. */
+/* Exact dequantised weight of one element; biases == NULL: symmetric codes.
+ * s * (q - 8) has at most 11 + 4 significant bits: exact in binary64. */
 static double dequant_one(const uint32_t *qweight, const uint16_t *scales,
                           const uint16_t *biases, int K, int G, int n, int k)
 {
     uint32_t word = qweight[(size_t)n * (K / 8) + k / 8];
     int q = (int)((word >> (4 * (k % 8))) & 0xFu);
     double s = orc_half_to_double(scales[(size_t)n * (K / G) + k / G]);
+    if (biases == NULL)
+        return s * (double)(q - 8);
     double b = orc_half_to_double(biases[(size_t)n * (K / G) + k / G]);
     return s * (double)q + b;
 }

@@ -3,7 +3,8 @@
 This module serves both the CUDA path's tests/benchmark and the CPU oracle.
 It holds no arithmetic of the method: it only draws random numbers and lays
 them out in the storage format (8 four-bit codes per 32-bit word, lowest
-nibble = lowest k; binary16 scales and biases per group of 64 along K).
+nibble = lowest k; binary16 scales, and biases unless the codes are
+symmetric, per group along K: 64 unless stated).
 
 Distributions follow the workloads the pages describe with model shapes:
 codes q uniform on 0..15, scale ~ U(0.002, 0.02), bias = -8*scale +
@@ -58,6 +59,16 @@ def make_linear(seed: int, N: int, K: int, group: int = GROUP):
     qweight = g.integers(0, 2**32, size=(N, K // 8), dtype=np.uint32)
     s16, b16 = make_scales_biases(g, N, K, group)
     return qweight, s16, b16
+
+
+def make_linear_sym(seed: int, N: int, K: int, group: int = 128):
+    """Random int4 symmetric weight (codes read as q - 8, no biases):
+    (qweight uint32 [N][K/8], scales f16 [N][K/group], None).  Scales are
+    drawn like the affine ones, ~ U(0.002, 0.02)."""
+    g = rng(seed)
+    qweight = g.integers(0, 2**32, size=(N, K // 8), dtype=np.uint32)
+    s16 = g.uniform(0.002, 0.02, size=(N, K // group)).astype(np.float16)
+    return qweight, s16, None
 
 
 def make_x(seed: int, M: int, K: int) -> np.ndarray:

@@ -64,7 +64,13 @@ def test_host_validation_codes(lib):
     # w4_gemv
     assert L.w4_gemv(None, f, f, f, f, 1, 8, 64, 64, None) == c["W4_ERR_NULL"]
     assert L.w4_gemv(f, f, f, f, None, 1, 8, 64, 64, None) == c["W4_ERR_NULL"]
-    assert L.w4_gemv(f, f, f, f, f, 1, 8, 64, 32, None) == c["W4_ERR_GROUP"]
+    assert L.w4_gemv(f, None, f, f, f, 1, 8, 64, 64, None) == c["W4_ERR_NULL"]
+    assert L.w4_gemv(f, f, None, f, f, 1, 8, 64, 64, None) == c["W4_ERR_NULL"]
+    for bad in (0, -64, 16, 48, 96, 128):  # not a power of two in 32..K, or above K = 64
+        assert L.w4_gemv(f, f, f, f, f, 1, 8, 64, bad, None) == c["W4_ERR_GROUP"], bad
+        assert L.w4_gemv(f, f, f, None, f, 1, 8, 64, bad, None) == c["W4_ERR_GROUP"], bad
+    assert L.w4_gemv(f, f, f, f, f, 1, 8, 192, 128, None) == c["W4_ERR_GROUP"]  # 192 % 128 != 0
+    assert L.w4_gemv(f, f, f, f + 8, f, 1, 8, 64, 64, None) == c["W4_ERR_ALIGN"]
     assert L.w4_gemv(f, f, f, f, f, 0, 8, 64, 64, None) == c["W4_ERR_SHAPE"]
     assert L.w4_gemv(f, f, f, f, f, 17, 8, 64, 64, None) == c["W4_ERR_SHAPE"]
     assert L.w4_gemv(f, f, f, f, f, 1, 0, 64, 64, None) == c["W4_ERR_SHAPE"]
@@ -85,6 +91,9 @@ def test_host_validation_codes(lib):
     assert L.w4_dequant_f16(f, f, f, None, 8, 64, 64, None) == c["W4_ERR_NULL"]
     assert L.w4_dequant_f16(f, f, f, f, 8, 100, 64, None) == c["W4_ERR_SHAPE"]
     assert L.w4_dequant_f16(f, f, f, f, 8, 64, 128, None) == c["W4_ERR_GROUP"]
+    assert L.w4_dequant_f16(f, None, f, f, 8, 64, 64, None) == c["W4_ERR_NULL"]
+    assert L.w4_dequant_f16(f, f, None, f, 8, 128, 96, None) == c["W4_ERR_GROUP"]
+    assert L.w4_dequant_f16(f, f, None, f, 8, 128, 256, None) == c["W4_ERR_GROUP"]
     assert L.w4_dequant_f16(f, f + 4, f, f, 8, 64, 64, None) == c["W4_ERR_ALIGN"]
     # f16_gemm
     assert L.f16_gemm(None, f, f, 4, 8, 8, None) == c["W4_ERR_NULL"]
@@ -117,7 +126,7 @@ class _Op(ctypes.Structure):
     """Mirror of w4_gemv_op (the C struct of include/w4a16.h)."""
     _fields_ = [("x", ctypes.c_void_p), ("qweight", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("biases", ctypes.c_void_p), ("y", ctypes.c_void_p), ("N", ctypes.c_int), ("K", ctypes.c_int),
-                ("wait_prev", ctypes.c_int), ("reserved", ctypes.c_int)]
+                ("wait_prev", ctypes.c_int), ("group", ctypes.c_int)]
 
 
 def _seq_bytes(lib, ops, M):
@@ -154,3 +163,29 @@ def test_seq_workspace_sizes_follow_the_producer_of_each_input(lib):
     ops3 = [_Op(a, W, W, W, b, 512, 256, 0, 0), _Op(a, W, W, W, b, 256, 256, 0, 0),
             _Op(b, W, W, W, c, 256, 256, 1, 0)]
     assert _seq_bytes(lib, ops3, 1) == head + 256 * 4
+
+
+def test_seq_group_32_lists_split_into_their_own_launches(lib):
+    """Host-only: group-32 operations and operations of other groups run in
+    separate launches (one kernel variant each), so an activation exchange
+    between them needs no tagged copy; within a run of one kind it does."""
+    lib.w4_gemv_seq_workspace_bytes.restype = ctypes.c_size_t
+    head = lib.w4_gemv_seq_workspace_bytes()
+    W = 0x7000_0000
+    a, b, c = 0x1000_0000, 0x2000_0000, 0x3000_0000
+    mixed = [_Op(a, W, W, W, b, 512, 256, 0, 64), _Op(b, W, W, 0, c, 256, 512, 1, 32)]
+    assert _seq_bytes(lib, mixed, 1) == head
+    same = [_Op(a, W, W, W, b, 512, 256, 0, 32), _Op(b, W, W, 0, c, 256, 512, 1, 32)]
+    assert _seq_bytes(lib, same, 1) == head + 512 * 4
+    default = [_Op(a, W, W, W, b, 512, 256, 0, 0), _Op(b, W, W, 0, c, 256, 512, 1, 128)]
+    assert _seq_bytes(lib, default, 2) == head + 2 * 512 * 4
+
+
+def test_seq_rejects_bad_operation_groups(lib):
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.w4_gemv_seq.argtypes = [P, I, I, P, Z, ctypes.c_uint, P]
+    c = _status_codes()
+    f = FAKE
+    for bad in (-1, 16, 48, 512):
+        ops = (_Op * 1)(_Op(f, f, f, f, f, 64, 256, 0, bad))
+        assert lib.w4_gemv_seq(ctypes.cast(ops, P), 1, 1, f, 16, 0, None) == c["W4_ERR_GROUP"], bad

@@ -1,0 +1,186 @@
+"""Other quantisation groups and symmetric codes on the GPU, against the oracle.
+
+The group is a runtime argument (32, 64, 128, 256, ...; the affine format of
+the workloads is group 64) and a weight without biases holds symmetric codes,
+w = scale * (q - 8): the format of group-128 int4 engines.  Every call takes
+the same kernels as the group-64 affine format (group 32 its own variant), so
+these tests cover each format through every entry point: GEMV (tolerance
+1e-3 * sum|w x| + 1e-3), token selection (exact indices where decidable),
+the projection list, and dequantisation (bit-exact)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from _gpu import require_gpu, to_dev, topk_check, within_tol
+
+pytestmark = pytest.mark.gpu
+
+FORMATS = [(32, False), (128, False), (256, False), (32, True), (64, True), (128, True)]
+
+
+@pytest.fixture(scope="module")
+def w4():
+    require_gpu()
+    import int4_weight_only_affine_gb300 as w4
+    return w4
+
+
+def _linear(seed, N, K, group, sym):
+    if sym:
+        return synth.make_linear_sym(seed, N, K, group)
+    return synth.make_linear(seed, N, K, group)
+
+
+def _dv(a):
+    return None if a is None else to_dev(a)
+
+
+# ------------------------------------------------------------------ GEMV
+
+SHAPES = [
+    (1, 896, 896),     # K % 256 != 0: the ragged code chunk
+    (1, 257, 512),     # ragged row tail
+    (3, 33, 256),
+    (9, 130, 1024),    # second activation tile
+    (16, 300, 2048),
+    (4, 2048, 2048),   # cluster split along K
+    (2, 256, 11008),   # K = 172 groups of 64 (43 of 256: no vector scale loads at group 256)
+]
+
+
+@pytest.mark.parametrize("group,sym", FORMATS)
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_gemv_formats(w4, group, sym, M, N, K):
+    if K % group:
+        pytest.skip("group does not divide K")
+    qw, s, b = _linear(5000 + group + 7 * sym + N, N, K, group, sym)
+    x = synth.make_x(17 + M, M, K)
+    y = w4.w4_gemv(to_dev(x), to_dev(qw), to_dev(s), _dv(b), group=group).cpu().numpy()
+    yo, ad = oracle.gemv(x, qw, s, b, N, K, group=group, threads=8)
+    ok, worst = within_tol(y, yo, ad)
+    assert ok, f"worst err/tol = {worst}"
+
+
+@pytest.mark.parametrize("group,sym", [(128, True), (32, False), (32, True)])
+@pytest.mark.parametrize("M", [1, 16])
+@pytest.mark.parametrize("K,N", [(2048, 22016), (11008, 2048), (2048, 2560)])
+def test_gemv_formats_full_size_sampled(w4, group, sym, M, K, N):
+    qw, s, b = _linear(6000 + N + group, N, K, group, sym)
+    x = synth.make_x(6100 + M, M, K)
+    y = w4.w4_gemv(to_dev(x), to_dev(qw), to_dev(s), _dv(b), group=group).cpu().numpy()
+    g = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([[0, 15, 16, N // 2, N - 1], g.integers(0, N, size=48)])).astype(np.int32)
+    yo, ad = oracle.gemv_rows(x, qw, s, b, K, rows, group=group)
+    ok, worst = within_tol(y[:, rows], yo, ad)
+    assert ok, f"worst err/tol = {worst}"
+
+
+def test_gemv_symmetric_closed_form(w4):
+    """All q = 9 with symmetric codes: y = sum_g scale_g * sum_{k in g} x_k."""
+    M, N, K, G = 3, 96, 1024, 128
+    g = np.random.default_rng(8)
+    qw = np.full((N, K // 8), 0x99999999, dtype=np.uint32)
+    s = g.uniform(0.002, 0.02, size=(N, K // G)).astype(np.float16)
+    x = g.integers(-3, 4, size=(M, K)).astype(np.float16)
+    y = w4.w4_gemv(to_dev(x), to_dev(qw), to_dev(s), None, group=G).cpu().numpy().astype(np.float64)
+    want = x.astype(np.float64).reshape(M, K // G, G).sum(axis=2) @ s.astype(np.float64).T
+    assert np.all(np.abs(y - want) <= 1e-3 * np.abs(want) + 1e-3)
+    z = w4.w4_gemv(to_dev(x), to_dev(np.full_like(qw, 0x88888888)), to_dev(s), None, group=G)
+    assert float(z.abs().max()) == 0.0
+
+
+# ------------------------------------------------------------------ token selection
+
+@pytest.mark.parametrize("group,sym", FORMATS)
+@pytest.mark.parametrize("M,N,K,k", [(1, 1000, 896, 5), (3, 3000, 512, 50), (16, 257, 256, 1)])
+def test_topk_formats(w4, group, sym, M, N, K, k):
+    if K % group:
+        pytest.skip("group does not divide K")
+    import torch
+    qw, s, b = _linear(7000 + group + N, N, K, group, sym)
+    x = synth.make_x(7100 + M, M, K)
+    ws = torch.randint(0, 255, (w4.lm_head_workspace_bytes(M, N, k),), dtype=torch.uint8, device="cuda")
+    idx, val = w4.lm_head_argmax_topk(to_dev(x), to_dev(qw), to_dev(s), _dv(b), k=k, workspace=ws, group=group)
+    idx, val = idx.cpu().numpy(), val.cpu().numpy()
+    for m in range(M):
+        lg, ad = oracle.gemv(x[m:m + 1], qw, s, b, N, K, group=group, threads=16)
+        topk_check(idx[m], val[m], lg[0], ad[0], k)
+
+
+def test_topk_lm_head_symmetric_group128_full_size(w4):
+    """The 151,936 x 2048 LM head in the symmetric group-128 format, top-50."""
+    N, K, k = 151936, 2048, 50
+    qw, s, b = synth.make_linear_sym(7300, N, K, 128)
+    x = synth.make_x(7301, 1, K)
+    idx, val = w4.lm_head_argmax_topk(to_dev(x), to_dev(qw), to_dev(s), None, k=k, group=128)
+    idx, val = idx.cpu().numpy(), val.cpu().numpy()
+    lg, ad = oracle.gemv(x, qw, s, None, N, K, group=128, threads=16)
+    topk_check(idx[0], val[0], lg[0], ad[0], k)
+
+
+# ------------------------------------------------------------------ projection list
+
+def test_seq_mixed_formats_chain(w4):
+    """One list whose operations use different formats, chained through their
+    outputs; group-32 runs go to their own launches."""
+    import torch
+    M = 2
+    plan = [  # (K, N, group, sym, chained)
+        (2048, 2560, 64, False, False),
+        (2560, 2048, 128, True, True),
+        (2048, 1024, 32, False, True),
+        (1024, 1536, 32, True, True),
+        (1536, 512, 256, False, True),
+        (512, 768, 64, True, True),
+    ]
+    mats = [_linear(7400 + i, N, K, gr, sy) for i, (K, N, gr, sy, _) in enumerate(plan)]
+    x = synth.make_x(7450, M, plan[0][0])
+    xs, outs, ads = [], [], []
+    for i, ((K, N, gr, sy, ch), (qw, s, b)) in enumerate(zip(plan, mats)):
+        if ch:
+            x = oracle.double_to_half_array(outs[-1].ravel()).reshape(M, -1).view(np.float16)
+        y, ad = oracle.gemv(x, qw, s, b, N, K, group=gr, threads=16)
+        xs.append(x)
+        outs.append(y)
+        ads.append(ad)
+    ys = [torch.empty((M, N), dtype=torch.float16, device="cuda") for _, N, _, _, _ in plan]
+    ops = []
+    for i, ((K, N, gr, sy, ch), (qw, s, b)) in enumerate(zip(plan, mats)):
+        xin = ys[i - 1] if ch else to_dev(xs[i])
+        ops.append((xin, to_dev(qw), to_dev(s), _dv(b), ys[i], ch, gr))
+    ws = w4.seq_workspace(ops)
+    for _ in range(2):
+        w4.w4_gemv_seq(ops, ws)
+        torch.cuda.synchronize()
+        assert w4.device_status() == 0
+        for i in range(len(plan)):
+            ok, worst = within_tol(ys[i].cpu().numpy(), outs[i], ads[i])
+            assert ok, f"op {i}: worst err/tol = {worst}"
+
+
+# ------------------------------------------------------------------ dequantisation
+
+@pytest.mark.parametrize("group,sym", FORMATS + [(64, False)])
+@pytest.mark.parametrize("N,K", [(1000, 896), (257, 512), (64, 256), (130, 1024), (4104, 2304), (3, 1024)])
+def test_dequant_formats_bit_exact(w4, group, sym, N, K):
+    if K % group:
+        pytest.skip("group does not divide K")
+    qw, s, b = _linear(7500 + N + group, N, K, group, sym)
+    got = w4.w4_dequant_f16(to_dev(qw), to_dev(s), _dv(b), group=group).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, oracle.dequant_f16_t(qw, s, b, N, K, group=group))
+
+
+@pytest.mark.parametrize("N", [512, 510])
+def test_dequant_symmetric_extreme_scales(w4, N):
+    """Symmetric codes with scales from every binary16 exponent and sign
+    (subnormals, overflow to infinity, signed zeros at q = 8)."""
+    g = np.random.default_rng(97)
+    K, G = 512, 128
+    e = g.integers(0, 31, size=N * K // G)
+    f = g.integers(0, 1024, size=N * K // G)
+    sg = g.integers(0, 2, size=N * K // G)
+    s = ((sg << 15) | (e << 10) | f).astype(np.uint16).reshape(N, K // G).view(np.float16)
+    qw = g.integers(0, 2**32, size=(N, K // 8), dtype=np.uint32)
+    got = w4.w4_dequant_f16(to_dev(qw), to_dev(s), None, group=G).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, oracle.dequant_f16_t(qw, s, None, N, K, group=G))

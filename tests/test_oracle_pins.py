@@ -298,3 +298,113 @@ def test_gemm_of_dequant_scratch_equals_gemv():
     yg, adg = oracle.gemm(x, w16, M, N, K)
     assert np.all(np.abs(yg - yv) <= 2.0**-11 * ad + 1e-12)
     assert np.all(np.abs(adg - ad) <= 2.0**-11 * ad + 1e-12)
+
+
+# ------------------------------------------------- group size and symmetric codes
+
+def test_dequant_symmetric_vs_fraction():
+    """Symmetric codes: scale*(q - 8) exactly (binary64) and its binary16
+    rounding, q = 0..15, against a wide random spread of binary16 scales; an
+    exact zero (q = 8) carries the sign of the IEEE product scale * (+0)."""
+    g = np.random.default_rng(6)
+    N = 1024
+    s = _random_half_bits(g, N)
+    qw = np.zeros((N, 8), dtype=np.uint32)
+    qw[:, 0] = 0x76543210
+    qw[:, 1] = 0xFEDCBA98                       # k = 0..15 hold q = 0..15
+    rows = np.arange(N)
+    w = oracle.dequant_exact_rows(qw, s[:, None], None, 64, rows)
+    w16 = oracle.dequant_f16_rows(qw, s[:, None], None, 64, rows)
+    for n in range(N):
+        sf = Fraction(_half_value(int(s[n])))
+        for q in range(16):
+            exact = sf * (q - 8)
+            assert Fraction(w[n, q]) == exact
+            if exact == 0:
+                assert int(w16[n, q]) == (int(s[n]) & 0x8000), hex(s[n])
+            else:
+                assert int(w16[n, q]) == _rne_half_fraction(exact), (hex(s[n]), q)
+    # codes 16..63 (all zero words) are q = 0: w = -8 * scale
+    assert np.array_equal(w[:, 16:], np.repeat(-8.0 * w[:, 9:10], 48, axis=1))
+
+
+def _linear(seed, N, K, group, sym):
+    if sym:
+        return synth.make_linear_sym(seed, N, K, group)
+    return synth.make_linear(seed, N, K, group)
+
+
+@pytest.mark.parametrize("group,sym", [(32, False), (128, False), (256, False), (32, True), (64, True),
+                                       (128, True), (256, True)])
+def test_gemv_fraction_brute_force_formats(group, sym):
+    """Tiny GEMVs of every supported format against exact rational arithmetic
+    on the unpacked codes: the scale (and bias) of element k is entry k // group."""
+    N, K, M = 3, 256, 2
+    qw, s, b = _linear(300 + group + sym, N, K, group, sym)
+    x = synth.make_x(400 + group, M, K)
+    y, ad = oracle.gemv(x, qw, s, b, N, K, group=group)
+    for n in range(N):
+        for m in range(M):
+            acc = Fraction(0)
+            aacc = Fraction(0)
+            for k in range(K):
+                q = (int(qw[n, k // 8]) >> (4 * (k % 8))) & 0xF
+                sc = Fraction(float(s[n, k // group]))
+                w = sc * (q - 8) if sym else sc * q + Fraction(float(b[n, k // group]))
+                p = w * Fraction(float(x[m, k]))
+                acc += p
+                aacc += abs(p)
+            assert abs(Fraction(y[m, n]) - acc) <= Fraction(1, 10**12) * aacc
+            assert abs(Fraction(ad[m, n]) - aacc) <= Fraction(1, 10**12) * aacc
+
+
+@pytest.mark.parametrize("sym", [False, True])
+def test_group_invariant_under_repeated_scales(sym):
+    """A group-G weight equals the group-G/2 weight whose scales (and biases)
+    are each repeated twice: the dequantised values bit for bit and the GEMV
+    exactly, for G = 64 and 128."""
+    N, K = 5, 512
+    x = synth.make_x(51, 2, K)
+    for G in (64, 128):
+        qw, s, b = _linear(50 + G, N, K, G, sym)
+        s2 = np.repeat(s, 2, axis=1)
+        b2 = None if b is None else np.repeat(b, 2, axis=1)
+        assert np.array_equal(oracle.dequant_f16_t(qw, s, b, N, K, group=G),
+                              oracle.dequant_f16_t(qw, s2, b2, N, K, group=G // 2))
+        y, _ = oracle.gemv(x, qw, s, b, N, K, group=G)
+        y2, _ = oracle.gemv(x, qw, s2, b2, N, K, group=G // 2)
+        assert np.array_equal(y, y2)
+
+
+def test_symmetric_equals_affine_with_bias_minus_eight_scales():
+    """Symmetric codes are the affine format with bias = -8 * scale (exact in
+    binary16 for these scales): same dequantised bits, same GEMV."""
+    N, K = 7, 384
+    qw, s, _ = synth.make_linear_sym(61, N, K, 128)
+    b = (-8.0 * s.astype(np.float64)).astype(np.float16)
+    assert np.array_equal(b.astype(np.float64), -8.0 * s.astype(np.float64))
+    assert np.array_equal(oracle.dequant_f16_t(qw, s, None, N, K, group=128),
+                          oracle.dequant_f16_t(qw, s, b, N, K, group=128))
+    x = synth.make_x(62, 3, K)
+    y, _ = oracle.gemv(x, qw, s, None, N, K, group=128)
+    ya, _ = oracle.gemv(x, qw, s, b, N, K, group=128)
+    assert np.array_equal(y, ya)
+
+
+def test_gemv_symmetric_closed_forms():
+    """Symmetric codes: all q = 8 gives y = 0 exactly; all q = 9 gives
+    y[n] = sum_g scale[n][g] * sum_{k in g} x[k] (exact for small integer x)."""
+    g = np.random.default_rng(71)
+    N, K, M, G = 4, 512, 2, 128
+    s = g.uniform(0.002, 0.02, size=(N, K // G)).astype(np.float16)
+    x = g.integers(-4, 5, size=(M, K)).astype(np.float16)
+    q8 = np.full((N, K // 8), 0x88888888, dtype=np.uint32)
+    y, _ = oracle.gemv(x, q8, s, None, N, K, group=G)
+    assert np.all(y == 0.0)
+    q9 = np.full((N, K // 8), 0x99999999, dtype=np.uint32)
+    y, _ = oracle.gemv(x, q9, s, None, N, K, group=G)
+    for m in range(M):
+        for n in range(N):
+            want = sum(Fraction(float(s[n, gi])) * sum(int(v) for v in x[m, gi * G:(gi + 1) * G])
+                       for gi in range(K // G))
+            assert Fraction(y[m, n]) == want
