@@ -165,10 +165,11 @@ def test_seq_workspace_sizes_follow_the_producer_of_each_input(lib):
     assert _seq_bytes(lib, ops3, 1) == head + 256 * 4
 
 
-def test_seq_group_32_lists_split_into_their_own_launches(lib):
-    """Host-only: group-32 operations and operations of other groups run in
-    separate launches (one kernel variant each), so an activation exchange
-    between them needs no tagged copy; within a run of one kind it does."""
+def test_seq_lists_split_by_scale_layout_class(lib):
+    """Host-only: a launch runs operations of one scale-layout class (group-64
+    affine, group 32, any other layout: one kernel variant each), so an
+    activation exchange between classes needs no tagged copy (stream order
+    covers it); within a run of one class it does."""
     lib.w4_gemv_seq_workspace_bytes.restype = ctypes.c_size_t
     head = lib.w4_gemv_seq_workspace_bytes()
     W = 0x7000_0000
@@ -177,8 +178,12 @@ def test_seq_group_32_lists_split_into_their_own_launches(lib):
     assert _seq_bytes(lib, mixed, 1) == head
     same = [_Op(a, W, W, W, b, 512, 256, 0, 32), _Op(b, W, W, 0, c, 256, 512, 1, 32)]
     assert _seq_bytes(lib, same, 1) == head + 512 * 4
-    default = [_Op(a, W, W, W, b, 512, 256, 0, 0), _Op(b, W, W, 0, c, 256, 512, 1, 128)]
+    default = [_Op(a, W, W, W, b, 512, 256, 0, 0), _Op(b, W, W, W, c, 256, 512, 1, 64)]
     assert _seq_bytes(lib, default, 2) == head + 2 * 512 * 4
+    sym_after_affine = [_Op(a, W, W, W, b, 512, 256, 0, 0), _Op(b, W, W, 0, c, 256, 512, 1, 128)]
+    assert _seq_bytes(lib, sym_after_affine, 2) == head
+    other = [_Op(a, W, W, 0, b, 512, 256, 0, 128), _Op(b, W, W, W, c, 256, 512, 1, 256)]
+    assert _seq_bytes(lib, other, 2) == head + 2 * 512 * 4
 
 
 def test_seq_rejects_bad_operation_groups(lib):
