@@ -25,11 +25,16 @@ struct WFmt {
 };
 
 // Kernel variants by scale layout: group-64 affine (the workloads' format),
-// any other group of 64 or more or symmetric codes (runtime layout), and
+// symmetric group 128, any other group of 64 or more (runtime layout), and
 // group 32 (two quantisation groups per 64-k block).
-enum : int { kFmtG64 = 0, kFmtAny = 1, kFmtG32 = 2 };
+enum : int { kFmtG64 = 0, kFmtAny = 1, kFmtG32 = 2, kFmtS128 = 3 };
 
-inline int fmt_class(const WFmt &f) { return f.gs == 0 ? kFmtG32 : (f.gs == 1 && !f.sym) ? kFmtG64 : kFmtAny; }
+inline int fmt_class(const WFmt &f) {
+    if (f.gs == 0) return kFmtG32;
+    if (f.gs == 1 && !f.sym) return kFmtG64;
+    if (f.gs == 2 && f.sym) return kFmtS128;
+    return kFmtAny;
+}
 
 // Host check of a (K, group) pair: group a power of two with
 // 32 <= group <= K and K % group == 0.  Fills f; false if unsupported.

@@ -224,7 +224,8 @@ struct StreamArgs {
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
 
-// FMT: the scale-layout class of the weight (kFmtG64, kFmtAny, kFmtG32).
+// FMT: the scale-layout class of the weight (kFmtG64, kFmtS128, kFmtAny,
+// kFmtG32).
 template <int NT, bool LMHEAD, bool M1, int FMT>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
     stream_kernel(const __grid_constant__ CUtensorMap tm3, const __grid_constant__ CUtensorMap tm2,
@@ -289,8 +290,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
                     const int q0 = cg0 / kBoxGroups;
                     const int nbox = (len + kBoxGroups - 1) / kBoxGroups;
                     // The tile's scale rows (and bias rows) are contiguous: [16][ngs].
-                    const bool sym = FMT != kFmtG64 && a.f.sym;
-                    const int ngs = FMT == kFmtG64 ? ng : a.f.ngs;
+                    const bool sym = FMT == kFmtS128 || (FMT != kFmtG64 && a.f.sym);
+                    const int ngs = FMT == kFmtG64 ? ng : FMT == kFmtS128 ? ng >> 1 : a.f.ngs;
                     const uint32_t sbytes = tail ? 0u : 32u * ngs;
                     const uint32_t sball = sym ? sbytes : 2 * sbytes;
                     const uint32_t st = base + s * a.stage_bytes;
@@ -328,9 +329,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
         const int xoff = lane_xoff(M, lg, lt), xd1 = lane_xd1(M, lg);
         const uint32_t hmask = FMT == kFmtG32 ? g32_m1_mask(lg, lt) : 0u;
         WFmt f = a.f;
-        if (FMT == kFmtG64) f.ngs = ng;  // one scale per group (the same value, one register)
-        const bool sym = FMT != kFmtG64 && f.sym;
-        const bool vec = FMT == kFmtG64 ? (f.ngs & 3) == 0 : box_vec_ok(f);
+        // The fixed classes' layouts follow from ng (fewer live registers).
+        if (FMT == kFmtG64) f.ngs = ng;
+        if (FMT == kFmtS128) f.ngs = ng >> 1;
+        const bool sym = FMT == kFmtS128 || (FMT != kFmtG64 && f.sym);
+        const bool vec = FMT == kFmtG64 ? (ng & 3) == 0 : FMT == kFmtS128 ? (ng & 3) == 0 : box_vec_ok(f);
         pdl_wait();
         stage_activations<M1 ? 2 : 4, FMT == kFmtG32>(a.x, M, a.K, gs0, ngl, xf, xsum, tid, kConsumers);
         consumer_sync();
@@ -385,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
                     for (int i = 0; i < 4; ++i) {
                         const int row = lg + ((i & 2) ? 8 : 0);
                         const int col = nt * 8 + 2 * lt + (i & 1);
-                        if (col < M) mine[row * M + col] = acc.value(nt, i);
+                        if (col < M) mine[row * M + col] = acc.template value<FMT == kFmtS128 ? -8 : 1>(nt, i);
                     }
                 continue;
             }
@@ -397,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
                 for (int i = 0; i < 4; ++i) {
                     const int row = lg + ((i & 2) ? 8 : 0);
                     const int col = nt * 8 + 2 * lt + (i & 1);
-                    if (col < M) mine[row * M + col] = acc.value(nt, i);
+                    if (col < M) mine[row * M + col] = acc.template value<FMT == kFmtS128 ? -8 : 1>(nt, i);
                 }
             consumer_sync();
             if (warp == (tl & (kConsumerWarps - 1))) {
@@ -594,8 +597,8 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
                 const int ng = o.K / kGroup, nch = (ng + kChunkGroups - 1) / kChunkGroups;
                 for (int t = t0; t < t1 && ok; ++t) {
                     const bool tail = (t + 1) * kTileRows > o.N;
-                    const bool sym = FMT != kFmtG64 && o.f.sym;
-                    const int ngs = FMT == kFmtG64 ? ng : o.f.ngs;
+                    const bool sym = FMT == kFmtS128 || (FMT != kFmtG64 && o.f.sym);
+                    const int ngs = FMT == kFmtG64 ? ng : FMT == kFmtS128 ? ng >> 1 : o.f.ngs;
                     const uint32_t sbytes = tail ? 0u : 32u * ngs;
                     const uint32_t sball = sym ? sbytes : 2 * sbytes;
                     for (int ch = 0; ch < nch; ++ch, ++it) {
@@ -643,8 +646,10 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
             const int N = o.N, ng = o.K / kGroup, nch = (ng + kChunkGroups - 1) / kChunkGroups;
             // K % 256 == 0: every full box reads its scales as one vector.
             WFmt f = o.f;
-            if (FMT == kFmtG64) f.ngs = ng;  // one scale per group (the same value, one register)
-            const bool sym = FMT != kFmtG64 && f.sym;
+            // The fixed classes' layouts follow from ng (fewer live registers).
+            if (FMT == kFmtG64) f.ngs = ng;
+            if (FMT == kFmtS128) f.ngs = ng >> 1;
+            const bool sym = FMT == kFmtS128 || (FMT != kFmtG64 && f.sym);
             const int T = (N + kTileRows - 1) / kTileRows;
             const int t0 = (int)((long long)blk * T / G), t1 = (int)((long long)(blk + 1) * T / G);
             const int ntl = t1 - t0;
@@ -725,7 +730,7 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
                     for (int i = 0; i < 4; ++i) {
                         const int row = lg + ((i & 2) ? 8 : 0);
                         const int col = nt * 8 + 2 * lt + (i & 1);
-                        if (col < M) mine[row * M + col] = acc.value(nt, i);
+                        if (col < M) mine[row * M + col] = acc.template value<FMT == kFmtS128 ? -8 : 1>(nt, i);
                     }
             }
             base_it += ntl * nch;
@@ -781,9 +786,10 @@ const void *stream_kernel_ptr_f(int M, bool lmhead) {
 }
 
 const void *stream_kernel_ptr(int M, bool lmhead, int fmt) {
-    return fmt == kFmtG64 ? stream_kernel_ptr_f<kFmtG64>(M, lmhead)
-           : fmt == kFmtG32 ? stream_kernel_ptr_f<kFmtG32>(M, lmhead)
-                            : stream_kernel_ptr_f<kFmtAny>(M, lmhead);
+    return fmt == kFmtG64    ? stream_kernel_ptr_f<kFmtG64>(M, lmhead)
+           : fmt == kFmtS128 ? stream_kernel_ptr_f<kFmtS128>(M, lmhead)
+           : fmt == kFmtG32  ? stream_kernel_ptr_f<kFmtG32>(M, lmhead)
+                             : stream_kernel_ptr_f<kFmtAny>(M, lmhead);
 }
 
 // lm_head pass 2: one CTA per activation row merges the G*k candidates
@@ -1202,9 +1208,10 @@ int launch_stream_f(const StreamPlan &p, const uint32_t *qw, bool ov, cudaStream
 template <bool LM>
 int launch_stream_any(const StreamPlan &p, const uint32_t *qw, bool ov, cudaStream_t s) {
     const int fmt = fmt_class(p.a.f);
-    return fmt == kFmtG64 ? launch_stream_f<LM, kFmtG64>(p, qw, ov, s)
-           : fmt == kFmtG32 ? launch_stream_f<LM, kFmtG32>(p, qw, ov, s)
-                            : launch_stream_f<LM, kFmtAny>(p, qw, ov, s);
+    return fmt == kFmtG64    ? launch_stream_f<LM, kFmtG64>(p, qw, ov, s)
+           : fmt == kFmtS128 ? launch_stream_f<LM, kFmtS128>(p, qw, ov, s)
+           : fmt == kFmtG32  ? launch_stream_f<LM, kFmtG32>(p, qw, ov, s)
+                             : launch_stream_f<LM, kFmtAny>(p, qw, ov, s);
 }
 
 int gemv_impl(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, const uint16_t *bi, uint16_t *y, int M,
@@ -1389,9 +1396,10 @@ int seq_launch(const w4_gemv_op *ops, int nops, int M, unsigned *ws, uint8_t *ta
     size_t smem = 0;
     if (!plan_seq(P, smem, ng_max, sc_max, xs_max, ntl_max)) return W4_ERR_SHAPE;
     const int fmt = fmt_class(P.ops[0].f);  // the same for every operation of a launch
-    const void *kern = fmt == kFmtG64   ? seq_kernel_ptr<kFmtG64>(M)
-                       : fmt == kFmtG32 ? seq_kernel_ptr<kFmtG32>(M)
-                                        : seq_kernel_ptr<kFmtAny>(M);
+    const void *kern = fmt == kFmtG64    ? seq_kernel_ptr<kFmtG64>(M)
+                       : fmt == kFmtS128 ? seq_kernel_ptr<kFmtS128>(M)
+                       : fmt == kFmtG32  ? seq_kernel_ptr<kFmtG32>(M)
+                                         : seq_kernel_ptr<kFmtAny>(M);
     if (!ensure_smem(kern, smem)) return W4_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G, 1, 1);
@@ -1462,7 +1470,10 @@ extern "C" int lm_head_argmax_topk_ex(const uint16_t *x, const uint32_t *qweight
 // Scale-layout class of an operation (its arguments need not be valid yet).
 static int seq_op_class(const w4_gemv_op &o) {
     const int group = o.group ? o.group : kGroup;
-    return group == 32 ? kFmtG32 : (group == kGroup && o.biases) ? kFmtG64 : kFmtAny;
+    if (group == 32) return kFmtG32;
+    if (group == kGroup && o.biases) return kFmtG64;
+    if (group == 2 * kGroup && !o.biases) return kFmtS128;
+    return kFmtAny;
 }
 
 // Operations of the next launch of a list: up to kSeqMaxOps of one scale-layout

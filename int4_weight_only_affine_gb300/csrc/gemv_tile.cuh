@@ -186,7 +186,12 @@ struct Acc {
 #pragma unroll
             for (int i = 0; i < 4; ++i) s[n][i] = b[n][i] = 0.f;
     }
-    __device__ __forceinline__ float value(int nt, int i) const { return fmaf(kTwo24, s[nt][i], b[nt][i]); }
+    // BF: the factor of the bias sums (1; -8 when they hold scale * sum x of
+    // symmetric codes, an exact power-of-two scaling).
+    template <int BF = 1>
+    __device__ __forceinline__ float value(int nt, int i) const {
+        return fmaf(kTwo24, s[nt][i], BF == 1 ? b[nt][i] : (float)BF * b[nt][i]);
+    }
 };
 
 // acc0 += s0 * d0 and acc1 += s1 * d1 in one packed fp32 instruction (each
@@ -449,8 +454,9 @@ __device__ __forceinline__ void box_scales_g32(float (&fsa)[4][2], float (&fsb)[
 // g: the box's first group; xl: the lane's staged activation fragments of
 // that group (see group_mma); xs: its activation sums.  FULL: n == 4 and
 // box_vec_ok(f).  FMT: kFmtG64 reads one scale and one bias per group
-// (f.ngs groups per row), kFmtAny follows f, kFmtG32 is the group-32 variant
-// (hmask: see group_mma_g32).
+// (f.ngs groups per row), kFmtS128 one scale per two groups and no bias (the
+// bias sums then accumulate scale * sum x: see Acc::value), kFmtAny follows
+// f, kFmtG32 is the group-32 variant (hmask: see group_mma_g32).
 template <int NT, bool M1, bool FULL, int FMT>
 __device__ __forceinline__ void box_mma(Acc<NT> &acc, const uint8_t *st, const int (&off)[4], const uint16_t *sp,
                                         const WFmt &f, int g, int n, const uint4 *xl, int xd1, const float *xs,
@@ -489,6 +495,29 @@ __device__ __forceinline__ void box_mma(Acc<NT> &acc, const uint8_t *st, const i
                 fba[j] = h2f(ba[jj]);
                 fbb[j] = h2f(ba[8 * ng + jj]);
             }
+        }
+    } else if (FMT == kFmtS128) {
+        const int ngs = f.ngs;
+        const uint16_t *sa = sp + lg * ngs;
+        if (FULL) {
+            const float2 va = __half22float2(*reinterpret_cast<const __half2 *>(sa + (g >> 1)));
+            const float2 vb = __half22float2(*reinterpret_cast<const __half2 *>(sa + 8 * ngs + (g >> 1)));
+            fsa[0] = fsa[1] = va.x;
+            fsa[2] = fsa[3] = va.y;
+            fsb[0] = fsb[1] = vb.x;
+            fsb[2] = fsb[3] = vb.y;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int gj = (g + (j < n ? j : 0)) >> 1;
+                fsa[j] = h2f(sa[gj]);
+                fsb[j] = h2f(sa[8 * ngs + gj]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            fba[j] = fsa[j];
+            fbb[j] = fsb[j];
         }
     } else {
         box_scales<FULL>(fsa, fsb, fba, fbb, sp, f, g, n, lg);
