@@ -167,7 +167,8 @@ def test_seq_workspace_sizes_follow_the_producer_of_each_input(lib):
 
 def test_seq_lists_split_by_scale_layout_class(lib):
     """Host-only: a launch runs operations of one scale-layout class (group-64
-    affine, group 32, any other layout: one kernel variant each), so an
+    affine, symmetric group 128, group 32, any other layout: one kernel
+    variant each), so an
     activation exchange between classes needs no tagged copy (stream order
     covers it); within a run of one class it does."""
     lib.w4_gemv_seq_workspace_bytes.restype = ctypes.c_size_t
@@ -182,8 +183,12 @@ def test_seq_lists_split_by_scale_layout_class(lib):
     assert _seq_bytes(lib, default, 2) == head + 2 * 512 * 4
     sym_after_affine = [_Op(a, W, W, W, b, 512, 256, 0, 0), _Op(b, W, W, 0, c, 256, 512, 1, 128)]
     assert _seq_bytes(lib, sym_after_affine, 2) == head
-    other = [_Op(a, W, W, 0, b, 512, 256, 0, 128), _Op(b, W, W, W, c, 256, 512, 1, 256)]
+    other = [_Op(a, W, W, W, b, 512, 256, 0, 128), _Op(b, W, W, 0, c, 256, 512, 1, 256)]
     assert _seq_bytes(lib, other, 2) == head + 2 * 512 * 4
+    sym128 = [_Op(a, W, W, 0, b, 512, 256, 0, 128), _Op(b, W, W, 0, c, 256, 512, 1, 128)]
+    assert _seq_bytes(lib, sym128, 2) == head + 2 * 512 * 4
+    sym128_then_other = [_Op(a, W, W, 0, b, 512, 256, 0, 128), _Op(b, W, W, W, c, 256, 512, 1, 128)]
+    assert _seq_bytes(lib, sym128_then_other, 2) == head
 
 
 def test_seq_rejects_bad_operation_groups(lib):
