@@ -14,7 +14,9 @@ blocks that share an input stored contiguously):
              per block, each streaming its weights while the previous kernel
              finishes), then per-row greedy argmax over the lm_head;
   kernels  - the lm_head GEMV + top-50 alone, and the 36 gate|up GEMVs
-             (2048 -> 22016) back to back: per-kernel decode bandwidth.
+             (2048 -> 22016) back to back: per-kernel decode bandwidth;
+  sym128   - the decode token again with the same shapes in the symmetric
+             group-128 format (scale only, w = scale * (q - 8)).
 Each part is a CUDA graph replayed on one stream; CUDA events time each part.
 The headline `value` is the decode GEMV bandwidth (algorithmic bytes of the
 token's weights / decode time), the first quantity of the metric; the other
@@ -57,7 +59,12 @@ def weight_bytes(N, K):
     return N * K // 2 + 2 * 2 * N * (K // 64)   # codes + fp16 scale + fp16 bias
 
 
+def weight_bytes_sym128(N, K):
+    return N * K // 2 + 2 * N * (K // 128)      # codes + fp16 scale
+
+
 DECODE_BYTES = LAYERS * sum(weight_bytes(N, K) for _, K, N in PROJ) + weight_bytes(LM_N, LM_K)
+DECODE_BYTES_SYM128 = LAYERS * sum(weight_bytes_sym128(N, K) for _, K, N in PROJ) + weight_bytes_sym128(LM_N, LM_K)
 PROJ_WEIGHTS = LAYERS * sum(N * K for _, K, N in PROJ)
 PREFILL_FLOPS = 2.0 * PREFILL_M * PROJ_WEIGHTS
 DEQUANT_BYTES = LAYERS * sum(weight_bytes(N, K) + 2 * N * K for _, K, N in PROJ)
@@ -168,6 +175,18 @@ class Model:
             self.layers.append(blocks)
         qw, s, b = synth.make_linear(99, LM_N, LM_K)
         self.lm = (self._up(qw.view(np.int32)), self._up(s), self._up(b), LM_N, LM_K)
+        # The same shapes in the symmetric group-128 format (scales only).
+        self.layers_s128 = []
+        for l in range(LAYERS):
+            blocks = {}
+            for name, K, N, parts in FUSED:
+                mats = [synth.make_linear_sym(synth.layer_seed(5000, l, seeds[q]), rows[q], K, 128) for q in parts]
+                qw = np.concatenate([m[0] for m in mats])
+                s = np.concatenate([m[1] for m in mats])
+                blocks[name] = (self._up(qw.view(np.int32)), self._up(s), None, N, K)
+            self.layers_s128.append(blocks)
+        qw, s, _ = synth.make_linear_sym(98, LM_N, LM_K, 128)
+        self.lm_s128 = (self._up(qw.view(np.int32)), self._up(s), None, LM_N, LM_K)
         self.setup_s = time.time() - t0
 
     def _up(self, a):
@@ -219,6 +238,12 @@ def run_ours(args, rank, world):
             qw, s, b, N, K = model.layers[l][name]
             seq_ops.append((xs1[SRC[name]], qw, s, b, ys1[name], len(seq_ops) > 0))
     seq_ws = w4.seq_workspace(seq_ops)  # zero-filled once; its counters reset themselves
+    seq_ops_s128 = []
+    for l in range(LAYERS):
+        for name, _, _, _ in FUSED:
+            qw, s, b, N, K = model.layers_s128[l][name]
+            seq_ops_s128.append((xs1[SRC[name]], qw, s, None, ys1[name], len(seq_ops_s128) > 0, 128))
+    seq_ws_s128 = w4.seq_workspace(seq_ops_s128)
     ys_gu = torch.empty((1, 2 * 11008), dtype=torch.float16, device=dev)
 
     def decode_seq():
@@ -226,6 +251,12 @@ def run_ours(args, rank, world):
         qw, s, b, N, K = model.lm
         w4.lm_head_argmax_topk(xs1["lm"], qw, s, b, k=TOPK, idx=idx1, val=val1, workspace=ws1, stream=stream,
                                flags=ov)
+
+    def decode_seq_s128():
+        w4.w4_gemv_seq(seq_ops_s128, workspace=seq_ws_s128, stream=stream)
+        qw, s, b, N, K = model.lm_s128
+        w4.lm_head_argmax_topk(xs1["lm"], qw, s, None, k=TOPK, idx=idx1, val=val1, workspace=ws1, stream=stream,
+                               flags=ov, group=128)
 
     def lm_only():
         qw, s, b, N, K = model.lm
@@ -269,11 +300,12 @@ def run_ours(args, rank, world):
         "decode_m16": lambda: decode(xs16, ys16, BATCH_M, 1, idx16, val16, ws16),
         "lm_head_m1": lm_only,
         "gate_up_m1": gate_up_only,
+        "decode_m1_s128": decode_seq_s128,
     }
     nb = LAYERS * len(FUSED)
     n_seq = (nb + 95) // 96
     launches = {"dequant": nb, "gemm": nb, "decode_m1": n_seq + 2, "decode_m16": nb + 2, "lm_head_m1": 2,
-                "gate_up_m1": LAYERS}
+                "gate_up_m1": LAYERS, "decode_m1_s128": n_seq + 2}
     # eager warm-up (sets kernel attributes), then capture one graph per part
     with torch.cuda.stream(stream):
         for f in parts.values():
@@ -289,7 +321,7 @@ def run_ours(args, rank, world):
     if w4.device_status() != 0:
         raise RuntimeError("device-side wait expired during warm-up")
 
-    order = ["dequant", "gemm", "decode_m1", "decode_m16", "lm_head_m1", "gate_up_m1"]
+    order = ["dequant", "gemm", "decode_m1", "decode_m16", "lm_head_m1", "gate_up_m1", "decode_m1_s128"]
     ev = {n: [] for n in order}
 
     def step(record):
@@ -518,6 +550,7 @@ def main():
     m16_gbs = DECODE_BYTES / (pm["decode_m16"] / 1e3) / 1e9
     lm_gbs = weight_bytes(LM_N, LM_K) / (pm["lm_head_m1"] / 1e3) / 1e9
     gu_gbs = LAYERS * weight_bytes(2 * 11008, 2048) / (pm["gate_up_m1"] / 1e3) / 1e9
+    s128_gbs = DECODE_BYTES_SYM128 / (pm["decode_m1_s128"] / 1e3) / 1e9
     line = {
         "metric": METRIC,
         "value": decode_gbs * world,
@@ -547,6 +580,9 @@ def main():
             "gemm_m1570": {"ms": pm["gemm"], "TFLOP_s": gemm_tflops, "frac_tensor": gemm_tflops / tflops},
             "lm_head_m1_top50": {"ms": pm["lm_head_m1"], "GB_s": lm_gbs, "frac_hbm": lm_gbs / hbm},
             "gemv_gate_up_m1_x36": {"ms": pm["gate_up_m1"], "GB_s": gu_gbs, "frac_hbm": gu_gbs / hbm},
+            "decode_m1_sym128": {"ms": pm["decode_m1_s128"], "GB_s": s128_gbs, "tok_s": 1e3 / pm["decode_m1_s128"],
+                                 "frac_hbm": s128_gbs / hbm,
+                                 "format": "symmetric int4, group 128 (scale only), same shapes"},
         },
         "roofline": {"bound": "tensor", "kernel": "f16_gemm (tcgen05)", "achieved": gemm_tflops,
                      "peak": tflops, "unit": "TFLOP/s", "frac": gemm_tflops / tflops, "traffic": None,
