@@ -246,6 +246,46 @@ W4A16_API int w4_dequant_f16_ex(const uint32_t *qweight, const uint16_t *scales,
                                 int group, unsigned flags, void *stream);
 
 /*
+ * w4_gemm - int4 GEMM with the dequantisation fused into the tensor-core
+ * pipeline, for prefill with few activation rows:
+ *   y[m][n] = sum_k w[n][k] * x[m][k],  w[n][k] = RNE_binary16(scale*q + bias)
+ *   (or of scale*(q - 8) without biases): the weight values of
+ *   w4_dequant_f16, multiplied without writing a scratch.
+ *   ("The inference engine - Mojo 1.0 on Metal", "Crossing Mojo 1.0": the
+ *   prefill GEMM over dequantised weights; here the weights are dequantised
+ *   tile by tile in shared memory and read from HBM only as 4-bit codes.)
+ *   x        binary16 [M][K]   activations
+ *   qweight, scales, biases, group    the int4 weight (format above)
+ *   y        binary16 [M][N]   output; fp32 accumulation, one rounding
+ *   M 1..128;  N >= 8, N % 8 == 0;  K >= 64, K % 64 == 0.
+ *   workspace  device buffer of at least w4_gemm_workspace_bytes(M, N, K)
+ *              bytes, 16-byte aligned, ZERO-FILLED before its first use and
+ *              then passed unchanged to later calls (its tile counters return
+ *              to zero at the end of every call); used by one call at a time.
+ *              Small N splits K over several blocks whose fp32 partial sums
+ *              it holds.
+ *   With a single K split (large N) the result equals f16_gemm on the
+ *   w4_dequant_f16 scratch bit for bit; with several, the partial sums are
+ *   added in split order (deterministic).
+ * Errors: W4_ERR_NULL, W4_ERR_SHAPE, W4_ERR_GROUP, W4_ERR_ALIGN,
+ * W4_ERR_WORKSPACE, W4_ERR_DEVICE, W4_ERR_LAUNCH.
+ */
+W4A16_API int w4_gemm(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                      const uint16_t *biases, uint16_t *y, int M, int N, int K, int group,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/* w4_gemm with launch flags (W4A16_OVERLAP_PREVIOUS: the weights are not
+ * written by the previous kernel; their first tiles are fetched and
+ * converted before it finishes). */
+W4A16_API int w4_gemm_ex(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                         const uint16_t *biases, uint16_t *y, int M, int N, int K, int group,
+                         void *workspace, size_t workspace_bytes, unsigned flags, void *stream);
+
+/* Workspace bytes for w4_gemm (0 if the sizes are invalid).  Depends only on
+ * its arguments. */
+W4A16_API size_t w4_gemm_workspace_bytes(int M, int N, int K);
+
+/*
  * f16_gemm - dense half GEMM for prefill, y = x16 * w16.
  *   ("The inference engine - Mojo 1.0 on Metal", "Crossing Mojo 1.0": the
  *   half-precision GEMM that follows the dequantise-once step.)

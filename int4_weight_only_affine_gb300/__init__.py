@@ -19,7 +19,7 @@ import os
 import torch
 
 __all__ = ["OVERLAP_PREVIOUS", "w4_gemv", "w4_gemv_seq", "seq_workspace", "seq_workspace_bytes", "GemvOp", "lm_head_argmax_topk", "lm_head_workspace_bytes", "w4_dequant_f16",
-           "f16_gemm", "device_status", "W4A16Error", "LIB_PATH", "lib"]
+           "f16_gemm", "w4_gemm", "w4_gemm_workspace", "w4_gemm_workspace_bytes", "device_status", "W4A16Error", "LIB_PATH", "lib"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libw4a16.so")
@@ -55,6 +55,10 @@ def _load() -> ctypes.CDLL:
     L.w4_dequant_f16.argtypes = [P, P, P, P, I, I, I, P]
     L.w4_dequant_f16_ex.argtypes = [P, P, P, P, I, I, I, ctypes.c_uint, P]
     L.f16_gemm.argtypes = [P, P, P, I, I, I, P]
+    L.w4_gemm.argtypes = [P, P, P, P, P, I, I, I, I, P, Z, P]
+    L.w4_gemm_ex.argtypes = [P, P, P, P, P, I, I, I, I, P, Z, ctypes.c_uint, P]
+    L.w4_gemm_workspace_bytes.argtypes = [I, I, I]
+    L.w4_gemm_workspace_bytes.restype = Z
     L.f16_gemm_ex.argtypes = [P, P, P, I, I, I, ctypes.c_uint, P]
     L.w4a16_status_string.argtypes = [I]
     L.w4a16_status_string.restype = ctypes.c_char_p
@@ -224,6 +228,36 @@ def w4_dequant_f16(qweight: torch.Tensor, scales: torch.Tensor, biases: torch.Te
                                  _biases(biases), _dev(w16, "w16", _H), N, K, group, flags,
                                  _stream(stream)))
     return w16
+
+
+def w4_gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib.w4_gemm_workspace_bytes(M, N, K))
+
+
+def w4_gemm_workspace(M: int, N: int, K: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace for w4_gemm at these sizes (reusable by every
+    later call with sizes that need no more)."""
+    return torch.zeros(max(w4_gemm_workspace_bytes(M, N, K), 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def w4_gemm(x: torch.Tensor, qweight: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor | None,
+            y: torch.Tensor | None = None, group: int = 64, workspace: torch.Tensor | None = None, stream=None,
+            flags: int = 0) -> torch.Tensor:
+    """y[M][N] = x[M][K] @ W^T with the int4 weight dequantised inside the
+    tensor-core GEMM (M <= 128).  workspace: from w4_gemm_workspace (zero-filled
+    once, then reused); a fresh one is made when None."""
+    N, K = _weight_dims(qweight, scales, biases, group)
+    x2 = x.reshape(-1, K) if x.dim() != 2 else x
+    M = x2.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float16, device=x.device)
+    if workspace is None:
+        workspace = w4_gemm_workspace(M, N, K, x.device)
+    _check("w4_gemm", lib.w4_gemm_ex(_dev(x2, "x", _H), _dev(qweight, "qweight", _QW), _dev(scales, "scales", _H),
+                                     _biases(biases), _dev(y, "y", _H), M, N, K, group,
+                                     _dev(workspace, "workspace", (torch.uint8,)), workspace.numel(), flags,
+                                     _stream(stream)))
+    return y
 
 
 def f16_gemm(x16: torch.Tensor, w16: torch.Tensor, y: torch.Tensor | None = None,

@@ -528,6 +528,469 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// w4_gemm: the int4 GEMM with the dequantisation inside the tensor-core
+// pipeline, for prefill with few activation rows (M <= 128).  The weight is
+// read once as 4-bit codes (0.5625 B per weight for group-64 affine) instead
+// of being dequantised into a half scratch (2 B written + 2 B read per
+// weight) and then multiplied.
+//
+//  * Tiles of 128 weight rows (output columns) x all M <= 128 activation rows
+//    (one 128-row MMA tile, rows past M zero-filled by the copies).  Small-N
+//    shapes split K over several CTAs (units = tiles x splits).
+//  * Two rings.  Codes: 3 stages of 16 KB (128 rows x 256 k: four 64-k steps
+//    in one tensor copy of 128-byte rows, 128-byte swizzle), deep enough to
+//    cover HBM latency.  Operands: 5 stages of the X tile (K-major, 128-byte
+//    swizzle, from L2) and the converted weights of one 64-k step.
+//  * Warp 0: one thread issues the code copies (weights are constants: no
+//    dependency wait).  Warp 14: one thread issues the X copies (after the
+//    dependency wait when launched as a programmatic dependent).
+//  * Warps 6-13: converters, two teams of four warps taking alternate code
+//    stages (a code slot is released after the proxy fence that also
+//    publishes the converted weights of its last step).  Lane l of team warp
+//    v turns rows 2p, 2p+1 (p = 32 (v % 2) + l) and k half v / 2 of each
+//    64-k step into binary16 pairs (w[n][k], w[n+1][k])
+//    -- exactly the w4_dequant_f16 value, RNE(scale*q + bias) -- and writes
+//    them in the layout the f16_gemm B operand has after its tensor copies
+//    (two 64 k x 64 n boxes, N-major, 128-byte swizzle).  Each store
+//    instruction of a warp fills one 128-byte k row: no bank conflicts.
+//    Scales and biases are loaded one team code stage (eight steps) ahead.
+//  * Warp 1: one thread issues tcgen05.mma.kind::f16 (M = 128, N = 128,
+//    K = 16), four per stage, and commits each operand stage back.
+//  * Warps 2-5: epilogue.  One split: round and store y.  Several: write
+//    the fp32 partial tile to the workspace; the CTA that completes a tile
+//    (arrival counter) sums the partials in split order and stores y, and
+//    resets the counter for the next call.
+// With one split the arithmetic is that of f16_gemm on the w4_dequant_f16
+// scratch (same operand values and layout, same MMA sequence).
+// ---------------------------------------------------------------------------
+constexpr int FBN = 128;                              // weight rows per tile
+constexpr int XST = 5;                                // operand stages
+constexpr int CST = 3;                                // code stages
+constexpr int CK = 4;                                 // 64-k steps per code stage
+constexpr int FA_TILE = BM * BK * 2;                  // 16 KB: X, 128 rows x 64 k
+constexpr int FB_TILE = BK * FBN * 2;                 // 16 KB: converted weights
+constexpr int FXW = FA_TILE + FB_TILE;                // 32 KB operand stage
+constexpr int FC_TILE = FBN * 128;                    // 16 KB code stage: 128 rows x 32 words
+constexpr int F_TEAM_WARPS = 4;                       // converter warps per stage
+constexpr int F_CONV_WARP0 = 6;
+constexpr int F_XPROD_WARP = F_CONV_WARP0 + 2 * F_TEAM_WARPS;  // 14
+constexpr int F_THREADS = (F_XPROD_WARP + 1) * 32;    // 480
+constexpr int F_TMEM_COLS = 2 * FBN;
+constexpr int F_BARS = 2 * CST + 3 * XST + 5;
+constexpr size_t F_SMEM = 1024 + (size_t)XST * FXW + (size_t)CST * FC_TILE + 8 * F_BARS + 16;
+constexpr int kMaxSplit = 8;
+constexpr uint32_t kInstrDescF = (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (1u << 16) |
+                                 ((uint32_t)(FBN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+struct W4GemmArgs {
+    const uint16_t *sc, *bi;  // scales, biases (null: symmetric codes)
+    uint16_t *y;              // [M][N]
+    float *part;              // [S][M][N] fp32 partial tiles (S > 1)
+    unsigned *cnt;            // [tiles] arrival counters (S > 1), zero between calls
+    int M, N, K;
+    WFmt f;
+    int S;                    // K splits per tile
+    int pdl;
+};
+
+__device__ __forceinline__ void mma_f16_desc(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum));
+}
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__global__ void __launch_bounds__(F_THREADS, 1)
+    w4gemm_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_constant__ CUtensorMap tma_q,
+                  const __grid_constant__ W4GemmArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const uint32_t codes0 = base + XST * FXW;               // code ring
+    const uint32_t bar0 = codes0 + CST * FC_TILE;
+    auto code_full = [&](int c) { return bar0 + 8u * c; };             // codes landed
+    auto code_empty = [&](int c) { return bar0 + 8u * (CST + c); };    // codes read by the converters
+    auto xin_bar = [&](int s) { return bar0 + 8u * (2 * CST + s); };   // X tile landed
+    auto conv_bar = [&](int s) { return bar0 + 8u * (2 * CST + XST + s); };   // weights converted
+    auto empty_bar = [&](int s) { return bar0 + 8u * (2 * CST + 2 * XST + s); };  // MMAs done with the stage
+    auto accf_bar = [&](int x) { return bar0 + 8u * (2 * CST + 3 * XST + x); };
+    auto acce_bar = [&](int x) { return bar0 + 8u * (2 * CST + 3 * XST + 2 + x); };
+    const uint32_t done_bar = bar0 + 8u * (2 * CST + 3 * XST + 4);
+    const size_t tail_off = (size_t)XST * FXW + (size_t)CST * FC_TILE + 8 * F_BARS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + tail_off);
+    volatile int *last_flag = reinterpret_cast<volatile int *>(gbase + tail_off + 4);
+
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int M = a.M, N = a.N, S = a.S;
+    const int nk = a.K / BK;
+    const int tiles = (N + FBN - 1) / FBN;
+    const int units = tiles * S;
+    // Unit u: tile u / S (weight rows n0 ..), k steps [kb0, kb1) of split u % S.
+    auto unit_range = [&](int u, int &n0, int &kb0, int &kb1) {
+        const int sp = u % S;
+        n0 = (u / S) * FBN;
+        kb0 = sp * nk / S;  // S <= 8 and nk < 2^24: no overflow
+        kb1 = (sp + 1) * nk / S;
+    };
+
+    if (threadIdx.x == 0) {
+        for (int c = 0; c < CST; ++c) {
+            mbar_init(code_full(c), 1);
+            mbar_init(code_empty(c), F_TEAM_WARPS);
+        }
+        for (int s = 0; s < XST; ++s) {
+            mbar_init(xin_bar(s), 1);
+            mbar_init(conv_bar(s), F_TEAM_WARPS);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(accf_bar(x), 1);
+            mbar_init(acce_bar(x), 4);
+        }
+        mbar_init(done_bar, 1);
+        *last_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tma_x) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tma_q) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         (uint32_t)__cvta_generic_to_shared(tmem_slot)),
+                     "r"(F_TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- code producer (weights: no dependency wait) ----------------
+            uint32_t issued_ph = 0, issued_any = 0;
+            int cs = 0;  // code stages issued
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                int n0, kb0, kb1;
+                unit_range(u, n0, kb0, kb1);
+                for (int k = kb0; k < kb1; k += CK, ++cs) {
+                    const int c = cs % CST;
+                    const uint32_t ph = (cs / CST) & 1;
+                    if (!mbar_wait(code_empty(c), ph ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    // Steps k .. k+3 (words 8k ..); past K the copy fills zeros.
+                    mbar_expect_tx(code_full(c), FC_TILE);
+                    tma_load_2d(codes0 + c * FC_TILE, &tma_q, 8 * k, n0, code_full(c));
+                    issued_ph = (issued_ph & ~(1u << c)) | (ph << c);
+                    issued_any |= 1u << c;
+                }
+            }
+            // Drain: every copy this thread issued has landed before exit.
+            for (int c = 0; c < CST; ++c)
+                if (issued_any & (1u << c)) mbar_wait(code_full(c), (issued_ph >> c) & 1);
+        }
+    } else if (warp == F_XPROD_WARP) {
+        if (lane == 0) {
+            // ---------------- X producer ----------------
+            if (a.pdl) pdl_wait();  // x may be written by the previous kernel
+            uint32_t issued_ph = 0, issued_any = 0;
+            int it = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                int n0, kb0, kb1;
+                unit_range(u, n0, kb0, kb1);
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int s = it % XST;
+                    const uint32_t ph = (it / XST) & 1;
+                    if (!mbar_wait(empty_bar(s), ph ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(xin_bar(s), FA_TILE);
+                    tma_load_2d(base + s * FXW, &tma_x, kb * BK, 0, xin_bar(s));
+                    issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+                    issued_any |= 1u << s;
+                }
+            }
+            for (int s = 0; s < XST; ++s)
+                if (issued_any & (1u << s)) mbar_wait(xin_bar(s), (issued_ph >> s) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            int it = 0, tc = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++tc) {
+                int n0, kb0, kb1;
+                unit_range(u, n0, kb0, kb1);
+                const int acc = tc & 1;
+                const uint32_t aph = (tc >> 1) & 1;
+                if (!mbar_wait(acce_bar(acc), aph ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t dst = tmem + acc * FBN;
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int s = it % XST;
+                    const uint32_t ph = (it / XST) & 1;
+                    if (!mbar_wait(xin_bar(s), ph) || !mbar_wait(conv_bar(s), ph)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + s * FXW;
+                    const uint32_t sb = sa + FA_TILE;
+#pragma unroll
+                    for (int ks = 0; ks < BK / 16; ++ks) {
+                        const uint64_t ad = smem_desc(sa + ks * 32, 16, 1024);
+                        const uint64_t bd = smem_desc(sb + ks * 2048, B_BOX, 1024);
+                        mma_f16_desc(dst, ad, bd, kInstrDescF, (kb != kb0 || ks != 0) ? 1u : 0u);
+                    }
+                    mma_commit(empty_bar(s));
+                }
+                if (!ok) break;
+                mma_commit(accf_bar(acc));
+            }
+            mma_commit(done_bar);
+            mbar_wait(done_bar, 0);
+        }
+    } else if (warp >= 2 && warp < F_CONV_WARP0) {
+        // ---------------- epilogue: warps 2..5 ----------------
+        // After an expired wait a warp skips its work but still takes part in
+        // the named barriers of every unit (no warp is left waiting there).
+        const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31 = activation rows
+        const int row = quad * 32 + lane;
+        bool ok = true;
+        int tc = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++tc) {
+            int n0, kb0, kb1;
+            unit_range(u, n0, kb0, kb1);
+            const int acc = tc & 1;
+            const uint32_t aph = (tc >> 1) & 1;
+            if (ok && !mbar_wait(accf_bar(acc), aph)) ok = false;
+            if (ok) tc_fence_after();
+            for (int c = 0; c < FBN / 32 && ok; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + acc * FBN + c * 32, r);
+                if (c == FBN / 32 - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acce_bar(acc));
+                }
+                if (row >= M) continue;
+                const int nc = n0 + c * 32;
+                if (S == 1) {
+                    uint16_t *dst = a.y + (size_t)row * N + nc;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        if (nc + 8 * v < N) {
+                            uint4 o;
+                            o.x = pack_half2(r[8 * v + 0], r[8 * v + 1]);
+                            o.y = pack_half2(r[8 * v + 2], r[8 * v + 3]);
+                            o.z = pack_half2(r[8 * v + 4], r[8 * v + 5]);
+                            o.w = pack_half2(r[8 * v + 6], r[8 * v + 7]);
+                            *reinterpret_cast<uint4 *>(dst + 8 * v) = o;
+                        }
+                    }
+                } else {
+                    float *dst = a.part + ((size_t)(u % S) * M + row) * N + nc;
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        if (nc + 4 * v < N)
+                            __stcg(reinterpret_cast<float4 *>(dst + 4 * v),
+                                   make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                               __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
+                    }
+                }
+            }
+            if (S > 1) {
+                // The CTA that brings a tile's S-th partial sums them in split order.
+                __threadfence();
+                epi_sync();
+                if (warp == 2 && lane == 0) {
+                    const int t = u / S;
+                    const unsigned prev = atomicAdd(a.cnt + t, 1u);
+                    const int last = prev == (unsigned)(S - 1);
+                    if (last) a.cnt[t] = 0u;  // every split has arrived: ready for the next call
+                    *last_flag = last;
+                }
+                epi_sync();
+                if (*last_flag && ok) {
+                    __threadfence();
+                    // 8-column chunks of the tile over all 128 epilogue threads;
+                    // every split's loads of a chunk are in flight together.
+                    const int et = (warp - 2) * 32 + lane;
+                    for (int ci = et; ci < M * (FBN / 8); ci += 128) {
+                        const int r = ci / (FBN / 8), n = n0 + 8 * (ci % (FBN / 8));
+                        if (n >= N) continue;
+                        float4 p0[kMaxSplit], p1[kMaxSplit];
+#pragma unroll
+                        for (int sp = 0; sp < kMaxSplit; ++sp) {
+                            if (sp < S) {
+                                const float *src = a.part + ((size_t)sp * M + r) * N + n;
+                                p0[sp] = __ldcg(reinterpret_cast<const float4 *>(src));
+                                p1[sp] = __ldcg(reinterpret_cast<const float4 *>(src + 4));
+                            }
+                        }
+                        float4 s0 = p0[0], s1 = p1[0];
+#pragma unroll
+                        for (int sp = 1; sp < kMaxSplit; ++sp) {
+                            if (sp < S) {
+                                s0.x += p0[sp].x; s0.y += p0[sp].y; s0.z += p0[sp].z; s0.w += p0[sp].w;
+                                s1.x += p1[sp].x; s1.y += p1[sp].y; s1.z += p1[sp].z; s1.w += p1[sp].w;
+                            }
+                        }
+                        uint4 o;
+                        o.x = pack_half2(__float_as_uint(s0.x), __float_as_uint(s0.y));
+                        o.y = pack_half2(__float_as_uint(s0.z), __float_as_uint(s0.w));
+                        o.z = pack_half2(__float_as_uint(s1.x), __float_as_uint(s1.y));
+                        o.w = pack_half2(__float_as_uint(s1.z), __float_as_uint(s1.w));
+                        *reinterpret_cast<uint4 *>(a.y + (size_t)r * N + n) = o;
+                    }
+                }
+                epi_sync();  // the flag is read by every epilogue thread before the next unit
+            }
+        }
+    } else if (warp >= F_CONV_WARP0 && warp < F_XPROD_WARP) {
+        // ---------------- converters: warps 6..13, two teams ----------------
+        const int cw = warp - F_CONV_WARP0;
+        const int team = cw / F_TEAM_WARPS, v = cw % F_TEAM_WARPS;
+        const int p = 32 * (v & 1) + lane;  // row pair 2p, 2p+1 of the tile
+        const int kh = v >> 1;              // k half of the stage: k 32 kh .. 32 kh + 31
+        const int box = v & 1;              // 64-n box of the pair (n = 2p: 64 box + 2 lane)
+        // Byte offset, within the B tile, of (k = 32 kh + 8 w + e, n = 2p) is
+        //   box*8192 + (4 kh + w)*1024 + e*128 + (((lane/4) ^ e) << 4) + 4 (lane % 4).
+        const uint32_t off0 = (uint32_t)(box * B_BOX + kh * 4096 + 4 * (lane & 3));
+        const int lq = lane >> 2;
+        const bool sym = a.f.sym != 0;
+        const __half2 koff = __float2half2_rn(sym ? 1032.f : 1024.f);
+        const int ngs = a.f.ngs, gshift = a.f.gs + 5;
+        // Position of a code stage of this CTA: unit u (rows n0, steps
+        // [kb0, kb1)) and its first step k; advanced one code stage at a time.
+        struct CPos {
+            int u, n0, kb0, kb1, k;
+        };
+        auto cstep = [&](CPos &q) {
+            q.k += CK;
+            if (q.k < q.kb1) return;
+            q.u += gridDim.x;
+            if (q.u < units) {
+                unit_range(q.u, q.n0, q.kb0, q.kb1);
+                q.k = q.kb0;
+            }
+        };
+        // Scale and bias pairs (rows 2p, 2p+1) of the steps of the code stage
+        // at q, as half2 bit patterns.
+        auto load_sb = [&](const CPos &q, uint32_t (&s2)[CK], uint32_t (&b2)[CK]) {
+            const int ra = min(q.n0 + 2 * p, N - 1), rb = min(q.n0 + 2 * p + 1, N - 1);
+#pragma unroll
+            for (int j = 0; j < CK; ++j) {
+                const int gi = (min(q.k + j, q.kb1 - 1) * BK + 32 * kh) >> gshift;
+                s2[j] = (uint32_t)ld_nc_u16(a.sc + (size_t)ra * ngs + gi) |
+                        ((uint32_t)ld_nc_u16(a.sc + (size_t)rb * ngs + gi) << 16);
+                b2[j] = 0u;
+                if (!sym)
+                    b2[j] = (uint32_t)ld_nc_u16(a.bi + (size_t)ra * ngs + gi) |
+                            ((uint32_t)ld_nc_u16(a.bi + (size_t)rb * ngs + gi) << 16);
+            }
+        };
+        // The team converts code stages team, team + 2, ...; the scales of its
+        // next stage are loaded when it starts the current one.
+        CPos pf;
+        pf.u = blockIdx.x;
+        unit_range(pf.u, pf.n0, pf.kb0, pf.kb1);
+        pf.k = pf.kb0;
+        if (team) cstep(pf);
+        uint32_t nxs[CK], nxb[CK];
+        if (pf.u < units) load_sb(pf, nxs, nxb);
+        bool ok = true;
+        int cs = 0, itb = 0;  // code stages, and 64-k steps of earlier units
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            int n0, kb0, kb1;
+            unit_range(u, n0, kb0, kb1);
+            for (int k = kb0; k < kb1 && ok; k += CK, ++cs) {
+                if ((cs & 1) != team) continue;  // the other team's code stage
+                uint32_t cus[CK], cub[CK];
+#pragma unroll
+                for (int j = 0; j < CK; ++j) {
+                    cus[j] = nxs[j];
+                    cub[j] = nxb[j];
+                }
+                cstep(pf);
+                cstep(pf);
+                if (pf.u < units) load_sb(pf, nxs, nxb);
+                const int c = cs % CST;
+                if (!mbar_wait(code_full(c), (cs / CST) & 1)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *crow_a = gbase + XST * FXW + c * FC_TILE + (2 * p) * 128;
+                const uint8_t *crow_b = crow_a + 128;
+                const int swa = (2 * p) & 7, swb = (2 * p + 1) & 7;  // 128-byte swizzle phases
+#pragma unroll
+                for (int j = 0; j < CK; ++j) {
+                    if (k + j >= kb1) break;
+                    const int it = itb + (k - kb0) + j;  // operand ring position of this step
+                    const int s = it % XST;
+                    // 16-byte chunk 2j + kh of each row: k 64 (k0 + j) + 32 kh ...
+                    const uint4 A = *reinterpret_cast<const uint4 *>(crow_a + (((2 * j + kh) ^ swa) << 4));
+                    const uint4 B = *reinterpret_cast<const uint4 *>(crow_b + (((2 * j + kh) ^ swb) << 4));
+                    // The operand stage is free once the MMAs of its previous use are done.
+                    if (!mbar_wait(empty_bar(s), ((it / XST) & 1) ^ 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const __half2 s2 = *reinterpret_cast<const __half2 *>(&cus[j]);
+                    const __half2 b2 = *reinterpret_cast<const __half2 *>(&cub[j]);
+                    uint8_t *bt = gbase + s * FXW + FA_TILE + off0;
+                    const uint32_t wa[4] = {A.x, A.y, A.z, A.w}, wb[4] = {B.x, B.y, B.z, B.w};
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const uint32_t lo = __byte_perm(wa[w], wb[w], 0x5410);  // codes 0..3 of (row a, row b)
+                        const uint32_t hi = __byte_perm(wa[w], wb[w], 0x7632);  // codes 4..7
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const uint32_t src = e < 4 ? lo : hi;
+                            const uint32_t q4 = ((src >> (4 * (e & 3))) & 0x000F000Fu) | 0x64006400u;  // 1024 + q
+                            const __half2 q2 = __hsub2(*reinterpret_cast<const __half2 *>(&q4), koff);
+                            const __half2 w2 = sym ? __hmul2(q2, s2) : __hfma2(q2, s2, b2);  // one rounding
+                            *reinterpret_cast<uint32_t *>(bt + w * 1024 + e * 128 + ((lq ^ e) << 4)) =
+                                *reinterpret_cast<const uint32_t *>(&w2);
+                        }
+                    }
+                    // Generic accesses before any async-proxy access of the same
+                    // bytes: the tensor cores read the converted weights, and the
+                    // code slot is released after the last step's fence, so the
+                    // next tensor copy into it cannot overtake the code reads.
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(conv_bar(s));
+                }
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(code_empty(c));
+            }
+            itb += kb1 - kb0;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(F_TMEM_COLS));
+    }
+}
+
 bool make_map(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
               uint32_t box_outer) {
     return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ptr, inner, outer, inner * 2, box_inner, box_outer,
@@ -617,6 +1080,117 @@ extern "C" int f16_gemm_ex(const uint16_t *x16, const uint16_t *w16, uint16_t *y
                            unsigned flags, void *stream) {
     if (flags & ~(unsigned)W4A16_OVERLAP_PREVIOUS) return W4_ERR_SHAPE;
     return gemm_impl(x16, w16, y, M, N, K, flags, stream);
+}
+
+// ---------------------------------------------------------------------------
+// w4_gemm host side.
+// ---------------------------------------------------------------------------
+namespace w4a16 {
+namespace {
+
+// K splits per 128-row weight tile, S in {1, 2, 4, 8} (at most one per 64-k
+// step), from a cost estimate in units of one L2 round trip: a 64-k step
+// takes about a fifth of one (the MMA time of a 128 x 128 x 64 step), and the
+// CTA that completes a split tile pays one round trip per 8-column chunk each
+// of its 128 epilogue threads reduces (all splits' loads of a chunk in
+// flight); waves of units beyond one per SM add up.
+int w4gemm_splits(int M, int N, int K, int sms) {
+    const int tiles = (N + FBN - 1) / FBN, nk = K / BK;
+    int best = 1;
+    double best_cost = 0.0;
+    for (int S = 1; S <= kMaxSplit && S <= nk; S *= 2) {
+        const double waves = (double)((tiles * S + sms - 1) / sms);
+        const double reduce = S > 1 ? (double)((M * (FBN / 8) + 127) / 128) : 0.0;
+        const double cost = waves * (0.2 * ((nk + S - 1) / S) + reduce);
+        if (S == 1 || cost < best_cost) {
+            best = S;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+size_t w4gemm_counter_bytes(int N) { return (((size_t)((N + FBN - 1) / FBN) * 4 + 255) / 256) * 256; }
+
+bool w4gemm_shape_ok(int M, int N, int K) {
+    return M >= 1 && M <= BM && N >= 8 && N % 8 == 0 && K >= BK && K % BK == 0;
+}
+
+int w4gemm_impl(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales, const uint16_t *biases,
+                uint16_t *y, int M, int N, int K, int group, void *workspace, size_t workspace_bytes, unsigned flags,
+                void *stream) {
+    if (!x || !qweight || !scales || !y) return W4_ERR_NULL;
+    if (flags & ~(unsigned)W4A16_OVERLAP_PREVIOUS) return W4_ERR_SHAPE;
+    if (!w4gemm_shape_ok(M, N, K)) return W4_ERR_SHAPE;
+    WFmt f;
+    if (!make_fmt(f, K, group, biases == nullptr)) return W4_ERR_GROUP;
+    const size_t need = w4gemm_counter_bytes(N) + (size_t)kMaxSplit * M * N * 4;
+    if (!workspace || workspace_bytes < need) return W4_ERR_WORKSPACE;
+    if (!aligned16(x) || !aligned16(qweight) || !aligned16(scales) || (biases && !aligned16(biases)) ||
+        !aligned16(y) || !aligned16(workspace))
+        return W4_ERR_ALIGN;
+    if (device_cc() != 103) return W4_ERR_DEVICE;
+    CUtensorMap tx, tq;
+    if (!make_map(&tx, x, (uint64_t)K, (uint64_t)M, BK, BM)) return W4_ERR_DEVICE;
+    // Codes: 128 rows x 32 words (four 64-k steps) per copy, 128-byte swizzle.
+    if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, (uint64_t)K / 8, (uint64_t)N, (uint64_t)K / 2,
+                     32, FBN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return W4_ERR_DEVICE;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(w4gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)F_SMEM) !=
+            cudaSuccess)
+            return W4_ERR_LAUNCH;
+        attr_set[dev] = true;
+    }
+    const int sms = sm_count();
+    W4GemmArgs a;
+    a.sc = scales;
+    a.bi = biases;
+    a.y = y;
+    a.cnt = reinterpret_cast<unsigned *>(workspace);
+    a.part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) + w4gemm_counter_bytes(N));
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.f = f;
+    a.S = w4gemm_splits(M, N, K, sms);
+    a.pdl = (flags & W4A16_OVERLAP_PREVIOUS) ? 1 : 0;
+    const int units = ((N + FBN - 1) / FBN) * a.S;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(units < sms ? units : sms), 1, 1);
+    cfg.blockDim = dim3(F_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = F_SMEM;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.pdl;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, w4gemm_kernel, tx, tq, a);
+    return e == cudaSuccess ? W4A16_OK : W4_ERR_LAUNCH;
+}
+
+}  // namespace
+}  // namespace w4a16
+
+extern "C" size_t w4_gemm_workspace_bytes(int M, int N, int K) {
+    if (!w4gemm_shape_ok(M, N, K)) return 0;
+    return w4gemm_counter_bytes(N) + (size_t)kMaxSplit * M * N * 4;
+}
+
+extern "C" int w4_gemm(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales, const uint16_t *biases,
+                       uint16_t *y, int M, int N, int K, int group, void *workspace, size_t workspace_bytes,
+                       void *stream) {
+    return w4gemm_impl(x, qweight, scales, biases, y, M, N, K, group, workspace, workspace_bytes, 0u, stream);
+}
+
+extern "C" int w4_gemm_ex(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+                          const uint16_t *biases, uint16_t *y, int M, int N, int K, int group, void *workspace,
+                          size_t workspace_bytes, unsigned flags, void *stream) {
+    return w4gemm_impl(x, qweight, scales, biases, y, M, N, K, group, workspace, workspace_bytes, flags, stream);
 }
 
 namespace w4a16 {

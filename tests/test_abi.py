@@ -199,3 +199,32 @@ def test_seq_rejects_bad_operation_groups(lib):
     for bad in (-1, 16, 48, 512):
         ops = (_Op * 1)(_Op(f, f, f, f, f, 64, 256, 0, bad))
         assert lib.w4_gemv_seq(ctypes.cast(ops, P), 1, 1, f, 16, 0, None) == c["W4_ERR_GROUP"], bad
+
+
+def test_w4_gemm_host_validation(lib):
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.w4_gemm.argtypes = [P, P, P, P, P, I, I, I, I, P, Z, P]
+    lib.w4_gemm_workspace_bytes.argtypes = [I, I, I]
+    lib.w4_gemm_workspace_bytes.restype = Z
+    c = _status_codes()
+    f = FAKE
+    need = lib.w4_gemm_workspace_bytes(64, 256, 512)
+    # tile counters (256-byte block) + 8 splits of fp32 partials
+    assert need == 256 + 8 * 64 * 256 * 4
+    assert lib.w4_gemm_workspace_bytes(129, 256, 512) == 0
+    assert lib.w4_gemm_workspace_bytes(4, 12, 512) == 0
+    assert lib.w4_gemm_workspace_bytes(4, 256, 96) == 0
+    g = lib.w4_gemm
+    assert g(None, f, f, f, f, 64, 256, 512, 64, f, need, None) == c["W4_ERR_NULL"]
+    assert g(f, f, None, f, f, 64, 256, 512, 64, f, need, None) == c["W4_ERR_NULL"]
+    assert g(f, f, f, f, None, 64, 256, 512, 64, f, need, None) == c["W4_ERR_NULL"]
+    assert g(f, f, f, f, f, 0, 256, 512, 64, f, need, None) == c["W4_ERR_SHAPE"]
+    assert g(f, f, f, f, f, 129, 256, 512, 64, f, need, None) == c["W4_ERR_SHAPE"]
+    assert g(f, f, f, f, f, 64, 12, 512, 64, f, need, None) == c["W4_ERR_SHAPE"]
+    assert g(f, f, f, f, f, 64, 256, 96, 32, f, need, None) == c["W4_ERR_SHAPE"]
+    assert g(f, f, f, f, f, 64, 256, 512, 48, f, need, None) == c["W4_ERR_GROUP"]
+    assert g(f, f, f, None, f, 64, 256, 512, 1024, f, need, None) == c["W4_ERR_GROUP"]
+    assert g(f, f, f, f, f, 64, 256, 512, 64, None, need, None) == c["W4_ERR_WORKSPACE"]
+    assert g(f, f, f, f, f, 64, 256, 512, 64, f, need - 1, None) == c["W4_ERR_WORKSPACE"]
+    assert g(f + 8, f, f, f, f, 64, 256, 512, 64, f, need, None) == c["W4_ERR_ALIGN"]
+    assert g(f, f, f, f, f, 64, 256, 512, 64, f + 4, need, None) == c["W4_ERR_ALIGN"]
