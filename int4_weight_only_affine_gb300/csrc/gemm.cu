@@ -565,9 +565,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // scratch (same operand values and layout, same MMA sequence).
 // ---------------------------------------------------------------------------
 constexpr int FBN = 128;                              // weight rows per tile
-constexpr int XST = 5;                                // operand stages
+constexpr int XST = 5;                                // operand stages (>= CK + 1: see the converters)
 constexpr int CST = 3;                                // code stages
 constexpr int CK = 4;                                 // 64-k steps per code stage
+static_assert(XST >= CK + 1, "operand-stage waits rely on XST >= CK + 1");
 constexpr int FA_TILE = BM * BK * 2;                  // 16 KB: X, 128 rows x 64 k
 constexpr int FB_TILE = BK * FBN * 2;                 // 16 KB: converted weights
 constexpr int FXW = FA_TILE + FB_TILE;                // 32 KB operand stage
@@ -944,7 +945,13 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                     // 16-byte chunk 2j + kh of each row: k 64 (k0 + j) + 32 kh ...
                     const uint4 A = *reinterpret_cast<const uint4 *>(crow_a + (((2 * j + kh) ^ swa) << 4));
                     const uint4 B = *reinterpret_cast<const uint4 *>(crow_b + (((2 * j + kh) ^ swb) << 4));
-                    // The operand stage is free once the MMAs of its previous use are done.
+                    // The operand stage is free once the MMAs of its previous use
+                    // (step it - XST) are done.  The parity cannot alias: this warp's
+                    // previous step is at most CK + 1 steps back (the other team
+                    // converts one code stage of at most CK steps in between) and
+                    // waited for the MMAs XST steps before it, so with XST >= CK + 1
+                    // every earlier phase of this barrier is complete; no later one
+                    // can be (its MMAs need this step's weights).
                     if (!mbar_wait(empty_bar(s), ((it / XST) & 1) ^ 1)) {
                         ok = false;
                         break;
