@@ -16,7 +16,11 @@ blocks that share an input stored contiguously):
   kernels  - the lm_head GEMV + top-50 alone, and the 36 gate|up GEMVs
              (2048 -> 22016) back to back: per-kernel decode bandwidth;
   sym128   - the decode token again with the same shapes in the symmetric
-             group-128 format (scale only, w = scale * (q - 8)).
+             group-128 format (scale only, w = scale * (q - 8));
+  small-M  - prefill of M = 128 tokens: w4_gemm (dequantisation inside the
+             tensor-core GEMM) over the 144 blocks, beside f16_gemm at M = 128
+             on the dequantised scratch (dequant-once + GEMM = the dequant
+             part + that part).
 Each part is a CUDA graph replayed on one stream; CUDA events time each part.
 The headline `value` is the decode GEMV bandwidth (algorithmic bytes of the
 token's weights / decode time), the first quantity of the metric; the other
@@ -50,6 +54,7 @@ LAYERS = synth.QWEN25_3B_LAYERS
 PROJ = synth.QWEN25_3B
 LM_K, LM_N = synth.QWEN25_3B_LM_HEAD
 PREFILL_M = 1570
+SMALL_M = 128
 BATCH_M = 16
 TOPK = 50
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -67,6 +72,7 @@ DECODE_BYTES = LAYERS * sum(weight_bytes(N, K) for _, K, N in PROJ) + weight_byt
 DECODE_BYTES_SYM128 = LAYERS * sum(weight_bytes_sym128(N, K) for _, K, N in PROJ) + weight_bytes_sym128(LM_N, LM_K)
 PROJ_WEIGHTS = LAYERS * sum(N * K for _, K, N in PROJ)
 PREFILL_FLOPS = 2.0 * PREFILL_M * PROJ_WEIGHTS
+SMALL_FLOPS = 2.0 * SMALL_M * PROJ_WEIGHTS
 DEQUANT_BYTES = LAYERS * sum(weight_bytes(N, K) + 2 * N * K for _, K, N in PROJ)
 
 
@@ -230,6 +236,10 @@ def run_ours(args, rank, world):
           "mlp": torch.randn((PREFILL_M, 2048), device=dev).half(),
           "down": torch.randn((PREFILL_M, 11008), device=dev).half()}
     yp = {n: torch.empty((PREFILL_M, N), dtype=torch.float16, device=dev) for n, K, N, _ in FUSED}
+    xs128 = {k: v[:SMALL_M].contiguous() for k, v in xp.items()}
+    ys128 = {n: torch.empty((SMALL_M, N), dtype=torch.float16, device=dev) for n, K, N, _ in FUSED}
+    ws_gemm = w4.w4_gemm_workspace(SMALL_M, max(N for _, _, N, _ in FUSED), max(K for _, K, _, _ in FUSED),
+                                   dev)  # zero-filled once; its tile counters reset themselves
     ov = w4.OVERLAP_PREVIOUS  # weights are constant: stream them while the previous kernel finishes
     # decode M=1: the projection list, each operation waiting for all earlier ones
     seq_ops = []
@@ -257,6 +267,23 @@ def run_ours(args, rank, world):
         qw, s, b, N, K = model.lm_s128
         w4.lm_head_argmax_topk(xs1["lm"], qw, s, None, k=TOPK, idx=idx1, val=val1, workspace=ws1, stream=stream,
                                flags=ov, group=128)
+
+    def w4gemm_small():
+        first = True
+        for l in range(LAYERS):
+            for name, _, _, _ in FUSED:
+                qw, s, b, N, K = model.layers[l][name]
+                w4.w4_gemm(xs128[SRC[name]], qw, s, b, y=ys128[name], workspace=ws_gemm, stream=stream,
+                           flags=0 if first else ov)
+                first = False
+
+    def gemm_small():
+        first = True
+        for l in range(LAYERS):
+            for name, _, _, _ in FUSED:
+                w4.f16_gemm(xs128[SRC[name]], scratch[l][name], y=ys128[name], stream=stream,
+                            flags=0 if first else ov)
+                first = False
 
     def lm_only():
         qw, s, b, N, K = model.lm
@@ -301,11 +328,13 @@ def run_ours(args, rank, world):
         "lm_head_m1": lm_only,
         "gate_up_m1": gate_up_only,
         "decode_m1_s128": decode_seq_s128,
+        "w4gemm_m128": w4gemm_small,
+        "gemm_m128": gemm_small,
     }
     nb = LAYERS * len(FUSED)
     n_seq = (nb + 95) // 96
     launches = {"dequant": nb, "gemm": nb, "decode_m1": n_seq + 2, "decode_m16": nb + 2, "lm_head_m1": 2,
-                "gate_up_m1": LAYERS, "decode_m1_s128": n_seq + 2}
+                "gate_up_m1": LAYERS, "decode_m1_s128": n_seq + 2, "w4gemm_m128": nb, "gemm_m128": nb}
     # eager warm-up (sets kernel attributes), then capture one graph per part
     with torch.cuda.stream(stream):
         for f in parts.values():
@@ -321,7 +350,8 @@ def run_ours(args, rank, world):
     if w4.device_status() != 0:
         raise RuntimeError("device-side wait expired during warm-up")
 
-    order = ["dequant", "gemm", "decode_m1", "decode_m16", "lm_head_m1", "gate_up_m1", "decode_m1_s128"]
+    order = ["dequant", "gemm", "decode_m1", "decode_m16", "lm_head_m1", "gate_up_m1", "decode_m1_s128",
+             "w4gemm_m128", "gemm_m128"]
     ev = {n: [] for n in order}
 
     def step(record):
@@ -551,6 +581,9 @@ def main():
     lm_gbs = weight_bytes(LM_N, LM_K) / (pm["lm_head_m1"] / 1e3) / 1e9
     gu_gbs = LAYERS * weight_bytes(2 * 11008, 2048) / (pm["gate_up_m1"] / 1e3) / 1e9
     s128_gbs = DECODE_BYTES_SYM128 / (pm["decode_m1_s128"] / 1e3) / 1e9
+    fused_tf = SMALL_FLOPS / (pm["w4gemm_m128"] / 1e3) / 1e12
+    two_ms = pm["dequant"] + pm["gemm_m128"]
+    proj_bytes = LAYERS * sum(weight_bytes(N, K) for _, K, N in PROJ)
     line = {
         "metric": METRIC,
         "value": decode_gbs * world,
@@ -583,6 +616,10 @@ def main():
             "decode_m1_sym128": {"ms": pm["decode_m1_s128"], "GB_s": s128_gbs, "tok_s": 1e3 / pm["decode_m1_s128"],
                                  "frac_hbm": s128_gbs / hbm,
                                  "format": "symmetric int4, group 128 (scale only), same shapes"},
+            "prefill_m128_w4gemm": {"ms": pm["w4gemm_m128"], "TFLOP_s": fused_tf, "frac_tensor": fused_tf / tflops,
+                                    "weight_GB_s": proj_bytes / (pm["w4gemm_m128"] / 1e3) / 1e9},
+            "prefill_m128_dequant_then_gemm": {"ms": two_ms, "TFLOP_s": SMALL_FLOPS / (two_ms / 1e3) / 1e12,
+                                               "gemm_ms": pm["gemm_m128"]},
         },
         "roofline": {"bound": "tensor", "kernel": "f16_gemm (tcgen05)", "achieved": gemm_tflops,
                      "peak": tflops, "unit": "TFLOP/s", "frac": gemm_tflops / tflops, "traffic": None,
