@@ -27,7 +27,7 @@ token's weights / decode time), the first quantity of the metric; the other
 quantities are reported under `parts`.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-       python bench.py --profile gemv|gemm|dequant|lmhead|seq   (small case for ncu)
+       python bench.py --profile gemv|gemm|dequant|lmhead|seq|w4gemm   (small case for ncu)
 Under torchrun (N > 1) every rank runs an independent replica (the path has no
 exchange step) and rank 0 prints one JSON line.
 """
@@ -508,6 +508,15 @@ def profile_case(which, iters=3):
         ws = w4.seq_workspace(ops)
         for _ in range(iters):
             w4.w4_gemv_seq(ops, workspace=ws)
+    elif which == "w4gemm":
+        # the fused int4 GEMM at M = 64 on the q|k|v block (2048 -> 2560)
+        K, N, M = 2048, 2560, 64
+        qw, s, b = synth.make_linear(1, N, K)
+        a = [torch.from_numpy(t).to(dev) for t in (qw.view(np.int32), s, b)]
+        x = torch.from_numpy(synth.make_x(2, M, K)).to(dev)
+        ws = w4.w4_gemm_workspace(M, N, K, dev)
+        for _ in range(iters + 1):
+            w4.w4_gemm(x, *a, workspace=ws)
     elif which == "gemm":
         x = torch.randn((PREFILL_M, 2048), device=dev).half()
         w = (0.05 * torch.randn((2048, 11008), device=dev)).half()
@@ -526,7 +535,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--profile", default=None, choices=["gemv", "gemm", "dequant", "lmhead", "seq"])
+    ap.add_argument("--profile", default=None, choices=["gemv", "gemm", "dequant", "lmhead", "seq", "w4gemm"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
