@@ -605,6 +605,50 @@ __device__ __forceinline__ void mma_f16_desc(uint32_t tmem_d, uint64_t adesc, ui
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// Sum of the S fp32 partial tiles of rows [0, M) x columns [n0, n0 + 128)
+// in split order, stored as binary16: thread et of the 128 epilogue threads
+// takes 8-column chunks et, et + 128, ..., max(1, 4 / S) chunks at a time
+// with every split's loads of them in flight together.
+template <int S>
+__device__ __noinline__ void reduce_splits(const W4GemmArgs &a, int M, int N, int n0, int et) {
+    constexpr int U = S >= 4 ? 1 : 4 / S;
+    const int chunks = M * (FBN / 8);
+    for (int c0 = et; c0 < chunks; c0 += 128 * U) {
+        float4 p0[U][S], p1[U][S];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int ci = c0 + 128 * u;
+            const int r = ci / (FBN / 8), n = n0 + 8 * (ci % (FBN / 8));
+            if (ci < chunks && n < N) {
+#pragma unroll
+                for (int sp = 0; sp < S; ++sp) {
+                    const float *src = a.part + ((size_t)sp * M + r) * N + n;
+                    p0[u][sp] = __ldcg(reinterpret_cast<const float4 *>(src));
+                    p1[u][sp] = __ldcg(reinterpret_cast<const float4 *>(src + 4));
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int ci = c0 + 128 * u;
+            const int r = ci / (FBN / 8), n = n0 + 8 * (ci % (FBN / 8));
+            if (ci >= chunks || n >= N) continue;
+            float4 s0 = p0[u][0], s1 = p1[u][0];
+#pragma unroll
+            for (int sp = 1; sp < S; ++sp) {
+                s0.x += p0[u][sp].x; s0.y += p0[u][sp].y; s0.z += p0[u][sp].z; s0.w += p0[u][sp].w;
+                s1.x += p1[u][sp].x; s1.y += p1[u][sp].y; s1.z += p1[u][sp].z; s1.w += p1[u][sp].w;
+            }
+            uint4 o;
+            o.x = pack_half2(__float_as_uint(s0.x), __float_as_uint(s0.y));
+            o.y = pack_half2(__float_as_uint(s0.z), __float_as_uint(s0.w));
+            o.z = pack_half2(__float_as_uint(s1.x), __float_as_uint(s1.y));
+            o.w = pack_half2(__float_as_uint(s1.z), __float_as_uint(s1.w));
+            *reinterpret_cast<uint4 *>(a.y + (size_t)r * N + n) = o;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(F_THREADS, 1)
     w4gemm_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_constant__ CUtensorMap tma_q,
                   const __grid_constant__ W4GemmArgs a) {
@@ -827,36 +871,13 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 epi_sync();
                 if (*last_flag && ok) {
                     __threadfence();
-                    // 8-column chunks of the tile over all 128 epilogue threads;
-                    // every split's loads of a chunk are in flight together.
                     const int et = (warp - 2) * 32 + lane;
-                    for (int ci = et; ci < M * (FBN / 8); ci += 128) {
-                        const int r = ci / (FBN / 8), n = n0 + 8 * (ci % (FBN / 8));
-                        if (n >= N) continue;
-                        float4 p0[kMaxSplit], p1[kMaxSplit];
-#pragma unroll
-                        for (int sp = 0; sp < kMaxSplit; ++sp) {
-                            if (sp < S) {
-                                const float *src = a.part + ((size_t)sp * M + r) * N + n;
-                                p0[sp] = __ldcg(reinterpret_cast<const float4 *>(src));
-                                p1[sp] = __ldcg(reinterpret_cast<const float4 *>(src + 4));
-                            }
-                        }
-                        float4 s0 = p0[0], s1 = p1[0];
-#pragma unroll
-                        for (int sp = 1; sp < kMaxSplit; ++sp) {
-                            if (sp < S) {
-                                s0.x += p0[sp].x; s0.y += p0[sp].y; s0.z += p0[sp].z; s0.w += p0[sp].w;
-                                s1.x += p1[sp].x; s1.y += p1[sp].y; s1.z += p1[sp].z; s1.w += p1[sp].w;
-                            }
-                        }
-                        uint4 o;
-                        o.x = pack_half2(__float_as_uint(s0.x), __float_as_uint(s0.y));
-                        o.y = pack_half2(__float_as_uint(s0.z), __float_as_uint(s0.w));
-                        o.z = pack_half2(__float_as_uint(s1.x), __float_as_uint(s1.y));
-                        o.w = pack_half2(__float_as_uint(s1.z), __float_as_uint(s1.w));
-                        *reinterpret_cast<uint4 *>(a.y + (size_t)r * N + n) = o;
-                    }
+                    if (S == 2)
+                        reduce_splits<2>(a, M, N, n0, et);
+                    else if (S == 4)
+                        reduce_splits<4>(a, M, N, n0, et);
+                    else
+                        reduce_splits<8>(a, M, N, n0, et);
                 }
                 epi_sync();  // the flag is read by every epilogue thread before the next unit
             }
@@ -1096,19 +1117,22 @@ namespace w4a16 {
 namespace {
 
 // K splits per 128-row weight tile, S in {1, 2, 4, 8} (at most one per 64-k
-// step), from a cost estimate in units of one L2 round trip: a 64-k step
-// takes about a fifth of one (the MMA time of a 128 x 128 x 64 step), and the
-// CTA that completes a split tile pays one round trip per 8-column chunk each
-// of its 128 epilogue threads reduces (all splits' loads of a chunk in
-// flight); waves of units beyond one per SM add up.
+// step), from a cost estimate in units of one L2 round trip (fitted to
+// measured times on GB300): a 64-k step takes about half of one (the step is
+// bound by the latency of the code copies and the conversion, not by its
+// 128 x 128 x 64 MMAs), and the CTA that completes a split tile pays one
+// round trip per batch of max(1, 4 / S) 8-column chunks per epilogue
+// thread (all their loads in flight); waves of units beyond one per SM add
+// up.
 int w4gemm_splits(int M, int N, int K, int sms) {
     const int tiles = (N + FBN - 1) / FBN, nk = K / BK;
     int best = 1;
     double best_cost = 0.0;
     for (int S = 1; S <= kMaxSplit && S <= nk; S *= 2) {
         const double waves = (double)((tiles * S + sms - 1) / sms);
-        const double reduce = S > 1 ? (double)((M * (FBN / 8) + 127) / 128) : 0.0;
-        const double cost = waves * (0.2 * ((nk + S - 1) / S) + reduce);
+        const int per_batch = 128 * (S >= 4 ? 1 : 4 / S);
+        const double reduce = S > 1 ? (double)((M * (FBN / 8) + per_batch - 1) / per_batch) : 0.0;
+        const double cost = waves * (0.5 * ((nk + S - 1) / S) + reduce);
         if (S == 1 || cost < best_cost) {
             best = S;
             best_cost = cost;
