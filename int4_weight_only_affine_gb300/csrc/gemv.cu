@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
         int off[4];
         box_offsets(off, warp, lg, lt);
         const int xoff = lane_xoff(M, lg, lt), xd1 = lane_xd1(M, lg);
-        const uint32_t hmask = FMT == kFmtG32 ? g32_m1_mask(lg, lt) : 0u;
+        const int goff = FMT == kFmtG32 ? g32_offset(warp, lg, lt) : 0;
         WFmt f = a.f;
         // The fixed classes' layouts follow from ng (fewer live registers).
         if (FMT == kFmtG64) f.ngs = ng;
@@ -368,9 +368,9 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 2 : 1)
                     const uint4 *xl = reinterpret_cast<const uint4 *>(xf) + (size_t)gl * 2 * M * 4 + xoff;
                     const float *xs = xsum + gl * M * (FMT == kFmtG32 ? 2 : 1);
                     if (n == kBoxGroups && vec)
-                        box_mma<NT, M1, true, FMT>(acc, st, off, sp, f, g, n, xl, xd1, xs, M, lg, lt, hmask);
+                        box_mma<NT, M1, true, FMT>(acc, st, off, sp, f, g, n, xl, xd1, xs, M, lg, lt, goff);
                     else if (n > 0)
-                        box_mma<NT, M1, false, FMT>(acc, st, off, sp, f, g, n, xl, xd1, xs, M, lg, lt, hmask);
+                        box_mma<NT, M1, false, FMT>(acc, st, off, sp, f, g, n, xl, xd1, xs, M, lg, lt, goff);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty_bar(s));
@@ -633,7 +633,7 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
         int off[4];
         box_offsets(off, tw, lg, lt);
         const int xoff = lane_xoff(M, lg, lt), xd1 = lane_xd1(M, lg);
-        const uint32_t hmask = FMT == kFmtG32 ? g32_m1_mask(lg, lt) : 0u;
+        const int goff = FMT == kFmtG32 ? g32_offset(tw, lg, lt) : 0;
         // The workspace epoch counts completed launches; (epoch, operation)
         // names the 16-bit tag of every tagged word an operation writes, so a
         // word left by an earlier launch never matches.
@@ -711,10 +711,10 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
                         constexpr int xsg = FMT == kFmtG32 ? 2 : 1;  // sums per group and row
                         if (n == kBoxGroups)
                             box_mma<NT, M1, true, FMT>(acc, st, off, sp, f, g, n, xl, xd1, xsum + g * M * xsg, M, lg,
-                                                       lt, hmask);
+                                                       lt, goff);
                         else if (n > 0)
                             box_mma<NT, M1, false, FMT>(acc, st, off, sp, f, g, n, xl, xd1, xsum + g * M * xsg, M, lg,
-                                                        lt, hmask);
+                                                        lt, goff);
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(empty_bar(s));

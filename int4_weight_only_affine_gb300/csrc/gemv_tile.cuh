@@ -39,8 +39,11 @@ __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a -
 // 2h+1), activation row c and lane quad t, four words are stored at
 //   xf[(((gl*2 + h)*M + c)*4 + t)*4 ...]  =  {b0(2h), b1(2h), b0(2h+1), b1(2h+1)}
 // with b0(j) = (x[c][k+j], x[c][k+j+4]), b1(j) = (x[c][k+8+j], x[c][k+12+j]),
-// k = 64G + 16t.  xsum[gl*M + c] = sum of the group's 64 activations (fp32);
-// G32: xsum[(gl*M + c)*2 + h] = sum of its half h (k = 64G + 32h ...).
+// k = 64G + 16t.  xsum[gl*M + c] = sum of the group's 64 activations (fp32).
+// G32 (group-32 weights): quad t holds instead x[c][64G + 8t .. 8t+7] (half
+// 0) and x[c][64G + 32 + 8t ..] (half 1), each as {(x0, x4), (x2, x6),
+// (x1, x5) / 16, (x3, x7) / 16} in the same slots (h = half), and
+// xsum[(gl*M + c)*2 + h] = the sum of half h.
 // The operands of the MMAs for j = 1 and 3 are stored divided by 16 (exact
 // for |x| >= 2^-10; below that the halving error is at most 2^-25), because
 // their codes are extracted 4 bits higher (see group_mma).
@@ -55,6 +58,9 @@ __device__ __forceinline__ uint32_t sixteenth(uint32_t h2) {
 // high half) of one staging item, loaded with relaxed gpu-scope loads until
 // every tag equals `tag`.  Bounded: gives up (recording the expiry and
 // raising *abort) after the wait limit, or at once when *abort is raised.
+// H2: distance in words from the first 8 words to the second 8 (8: one run
+// of 16).
+template <int H2 = 8>
 __device__ __forceinline__ void load_tagged16(const uint32_t *src, uint32_t tag, uint32_t (&v)[16],
                                               volatile int *abort) {
     uint64_t t_start = 0;
@@ -63,7 +69,7 @@ __device__ __forceinline__ void load_tagged16(const uint32_t *src, uint32_t tag,
         for (int i = 0; i < 4; ++i)
             asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(v[4 * i]), "=r"(v[4 * i + 1]), "=r"(v[4 * i + 2]), "=r"(v[4 * i + 3])
-                         : "l"(src + 4 * i)
+                         : "l"(src + (i < 2 ? 4 * i : H2 + 4 * (i - 2)))
                          : "memory");
         bool ok = true;
 #pragma unroll
@@ -83,14 +89,15 @@ __device__ __forceinline__ void load_tagged16(const uint32_t *src, uint32_t tag,
     }
 }
 
-// One staging item: 16 consecutive activations of row c starting at element
-// e0 (two uint4 of half pairs), as read by stage_activations_t.
-template <bool TAGGED>
+// One staging item: 16 activations of row c (two uint4 of half pairs):
+// elements e0 .. e0+15, or for G32 e0 .. e0+7 and e0+32 .. e0+39, as read by
+// stage_activations_t.
+template <bool TAGGED, bool G32 = false>
 __device__ __forceinline__ void item_load(const uint16_t *__restrict__ x, const uint32_t *xt, uint32_t tag,
                                           size_t e0, bool coherent, volatile int *abort, uint4 &lo, uint4 &hi) {
     if (TAGGED) {
         uint32_t v[16];
-        load_tagged16(xt + e0, tag, v, abort);
+        load_tagged16<G32 ? 32 : 8>(xt + e0, tag, v, abort);
         lo.x = __byte_perm(v[0], v[1], 0x5410);
         lo.y = __byte_perm(v[2], v[3], 0x5410);
         lo.z = __byte_perm(v[4], v[5], 0x5410);
@@ -101,8 +108,34 @@ __device__ __forceinline__ void item_load(const uint16_t *__restrict__ x, const 
         hi.w = __byte_perm(v[14], v[15], 0x5410);
     } else {
         const uint4 *src = reinterpret_cast<const uint4 *>(x + e0);
+        const uint4 *src2 = G32 ? reinterpret_cast<const uint4 *>(x + e0 + 32) : src + 1;
         lo = coherent ? __ldcg(src) : __ldg(src);
-        hi = coherent ? __ldcg(src + 1) : __ldg(src + 1);
+        hi = coherent ? __ldcg(src2) : __ldg(src2);
+    }
+}
+
+// G32 item: half 0 (lo) and half 1 (hi) in fragment order; returns the sum
+// of each half's 8 activations.
+__device__ __forceinline__ void item_store_g32(uint4 lo, uint4 hi, int gl, int c, int t, int M, uint32_t *xf,
+                                               float &part0, float &part1) {
+    auto frag = [](uint4 v) {
+        uint4 f;
+        f.x = __byte_perm(v.x, v.z, 0x5410);             // (x0, x4)
+        f.y = __byte_perm(v.y, v.w, 0x5410);             // (x2, x6)
+        f.z = sixteenth(__byte_perm(v.x, v.z, 0x7632));  // (x1, x5) / 16
+        f.w = sixteenth(__byte_perm(v.y, v.w, 0x7632));  // (x3, x7) / 16
+        return f;
+    };
+    reinterpret_cast<uint4 *>(xf)[((gl * 2 + 0) * M + c) * 4 + t] = frag(lo);
+    reinterpret_cast<uint4 *>(xf)[((gl * 2 + 1) * M + c) * 4 + t] = frag(hi);
+    const uint32_t a[4] = {lo.x, lo.y, lo.z, lo.w}, b[4] = {hi.x, hi.y, hi.z, hi.w};
+    part0 = part1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        part0 += h2f((uint16_t)(a[i] & 0xFFFFu));
+        part0 += h2f((uint16_t)(a[i] >> 16));
+        part1 += h2f((uint16_t)(b[i] & 0xFFFFu));
+        part1 += h2f((uint16_t)(b[i] >> 16));
     }
 }
 
@@ -147,20 +180,28 @@ __device__ void stage_activations_t(const uint16_t *__restrict__ x, const uint32
             const int it = base + u * nthreads + tid;
             if (it < items) {
                 const int t = it & 3, c = (it >> 2) % M, gl = (it >> 2) / M;
-                item_load<TAGGED>(x, xt, tag, (size_t)c * K + (size_t)(g0 + gl) * kGroup + 16 * t, coherent, abort,
-                                  lo[u], hi[u]);
+                item_load<TAGGED, G32>(x, xt, tag, (size_t)c * K + (size_t)(g0 + gl) * kGroup + (G32 ? 8 : 16) * t,
+                                       coherent, abort, lo[u], hi[u]);
             }
         }
 #pragma unroll
         for (int u = 0; u < kB; ++u) {
             const int it = base + u * nthreads + tid;
-            float part = 0.f;
-            if (it < items) part = item_store(lo[u], hi[u], (it >> 2) / M, (it >> 2) % M, it & 3, M, xf);
-            part += __shfl_xor_sync(0xffffffffu, part, 1);
             if (G32) {
-                // Items t = 0, 1 hold the first 32 activations, t = 2, 3 the rest.
-                if (it < items && (it & 1) == 0) xsum[((it >> 2) << 1) + ((it >> 1) & 1)] = part;
+                float p0 = 0.f, p1 = 0.f;
+                if (it < items) item_store_g32(lo[u], hi[u], (it >> 2) / M, (it >> 2) % M, it & 3, M, xf, p0, p1);
+                p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+                p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+                p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
+                p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+                if (it < items && (it & 3) == 0) {
+                    xsum[(it >> 2) * 2] = p0;
+                    xsum[(it >> 2) * 2 + 1] = p1;
+                }
             } else {
+                float part = 0.f;
+                if (it < items) part = item_store(lo[u], hi[u], (it >> 2) / M, (it >> 2) % M, it & 3, M, xf);
+                part += __shfl_xor_sync(0xffffffffu, part, 1);
                 part += __shfl_xor_sync(0xffffffffu, part, 2);
                 if (it < items && (it & 3) == 0) xsum[it >> 2] = part;
             }
@@ -262,82 +303,58 @@ __device__ __forceinline__ void group_mma(Acc<NT> &acc, uint2 wa, uint2 wb, floa
     }
 }
 
-// Group 32: a 64-k group holds two quantisation groups, k 0..31 in the MMA
-// k slots of lanes t = 0, 1 and k 32..63 in those of lanes t = 2, 3.
-// sa[h], sb[h], ba[h], bb[h]: scale and bias of half h for rows g and g+8;
-// xs[c*2 + h]: half sums of activation row c.
-// M1: B column 0 keeps the first half (lanes t >= 2 of column 0 pass zero)
-// and column 1 the second half (fed by the lanes of column 1 with t < 2
-// zeroed), so the four MMAs give both halves at once: `hmask` is that
-// lane's mask.  M > 1: each fragment runs twice, masked to either half.
+// Group 32: a 64-k group holds two quantisation groups.  Lane (g, t) holds
+// word t (k 8t .. 8t+7, half 0) and word t + 4 (half 1) of rows g and g+8:
+// wa0, wa1 and wb0, wb1.  Each word feeds two MMAs of its half: codes (0, 4)
+// and (2, 6) -- one shift serves the upper byte -- against the staged
+// (x0, x4), (x2, x6), and codes (1, 5), (3, 7) at 16x against (x1, x5) / 16,
+// (x3, x7) / 16.  So each half's dot products come out of their own two
+// MMAs.  sa[h], sb[h], ba[h], bb[h]: scale and bias of half h for rows g and
+// g+8; xs[c*2 + h]: half sums of activation row c.
 template <int NT, bool M1>
-__device__ __forceinline__ void group_mma_g32(Acc<NT> &acc, uint2 wa, uint2 wb, const float (&sa)[2],
-                                              const float (&sb)[2], const float (&ba)[2], const float (&bb)[2],
-                                              const uint4 *xl, int xd1, const float *xs, int M, int lt,
-                                              uint32_t hmask) {
-    uint32_t a0[4], a1[4], a2[4], a3[4];
-    const uint32_t w8[4] = {wa.x >> 8, wb.x >> 8, wa.y >> 8, wb.y >> 8};
-    a0[0] = wa.x & kNibPair;
-    a1[0] = wb.x & kNibPair;
-    a2[0] = wa.y & kNibPair;
-    a3[0] = wb.y & kNibPair;
-    a0[1] = wa.x & kNibPairHi;
-    a1[1] = wb.x & kNibPairHi;
-    a2[1] = wa.y & kNibPairHi;
-    a3[1] = wb.y & kNibPairHi;
-    a0[2] = w8[0] & kNibPair;
-    a1[2] = w8[1] & kNibPair;
-    a2[2] = w8[2] & kNibPair;
-    a3[2] = w8[3] & kNibPair;
-    a0[3] = w8[0] & kNibPairHi;
-    a1[3] = w8[1] & kNibPairHi;
-    a2[3] = w8[2] & kNibPairHi;
-    a3[3] = w8[3] & kNibPairHi;
-    if (M1) {
-        const uint4 f0 = xl[0], f1 = xl[4];
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_16816(d, a0[0], a1[0], a2[0], a3[0], f0.x & hmask, f0.y & hmask);
-        mma_16816(d, a0[1], a1[1], a2[1], a3[1], f0.z & hmask, f0.w & hmask);
-        mma_16816(d, a0[2], a1[2], a2[2], a3[2], f1.x & hmask, f1.y & hmask);
-        mma_16816(d, a0[3], a1[3], a2[3], a3[3], f1.z & hmask, f1.w & hmask);
-        // Lanes t = 0: d[0], d[2] = first half of rows g, g+8; d[1], d[3] = second.
-        ffma2(acc.s[0][0], acc.s[0][2], sa[0], sb[0], d[0], d[2]);
-        ffma2(acc.s[0][0], acc.s[0][2], sa[1], sb[1], d[1], d[3]);
-        ffma2(acc.b[0][0], acc.b[0][2], ba[0], bb[0], xs[0], xs[0]);
-        ffma2(acc.b[0][0], acc.b[0][2], ba[1], bb[1], xs[1], xs[1]);
-        return;
-    }
-    const uint32_t lo = lt < 2 ? 0xffffffffu : 0u, hi = ~lo;
+__device__ __forceinline__ void group_mma_g32(Acc<NT> &acc, uint32_t wa0, uint32_t wa1, uint32_t wb0, uint32_t wb1,
+                                              const float (&sa)[2], const float (&sb)[2], const float (&ba)[2],
+                                              const float (&bb)[2], const uint4 *xl, int xd1, const float *xs, int M,
+                                              int lt) {
+    // A operands per half: x = codes (0, 4) / (2, 6), y = codes (1, 5) / (3, 7).
+    const uint32_t a8 = wa0 >> 8, b8 = wb0 >> 8, c8 = wa1 >> 8, d8 = wb1 >> 8;
+    const uint32_t h0x[4] = {wa0 & kNibPair, wb0 & kNibPair, a8 & kNibPair, b8 & kNibPair};
+    const uint32_t h0y[4] = {wa0 & kNibPairHi, wb0 & kNibPairHi, a8 & kNibPairHi, b8 & kNibPairHi};
+    const uint32_t h1x[4] = {wa1 & kNibPair, wb1 & kNibPair, c8 & kNibPair, d8 & kNibPair};
+    const uint32_t h1y[4] = {wa1 & kNibPairHi, wb1 & kNibPairHi, c8 & kNibPairHi, d8 & kNibPairHi};
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int xo = nt ? xd1 : 0;
-        const uint4 f0 = xl[xo];
-        const uint4 f1 = xl[xo + M * 4];
+        const uint4 f0 = xl[xo];                        // half 0 fragments
+        const uint4 f1 = xl[xo + (M1 ? 4 : M * 4)];     // half 1 fragments
         float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_16816(d0, a0[0], a1[0], a2[0], a3[0], f0.x & lo, f0.y & lo);
-        mma_16816(d0, a0[1], a1[1], a2[1], a3[1], f0.z & lo, f0.w & lo);
-        mma_16816(d0, a0[2], a1[2], a2[2], a3[2], f1.x & lo, f1.y & lo);
-        mma_16816(d0, a0[3], a1[3], a2[3], a3[3], f1.z & lo, f1.w & lo);
-        mma_16816(d1, a0[0], a1[0], a2[0], a3[0], f0.x & hi, f0.y & hi);
-        mma_16816(d1, a0[1], a1[1], a2[1], a3[1], f0.z & hi, f0.w & hi);
-        mma_16816(d1, a0[2], a1[2], a2[2], a3[2], f1.x & hi, f1.y & hi);
-        mma_16816(d1, a0[3], a1[3], a2[3], a3[3], f1.z & hi, f1.w & hi);
-        const int c0 = min(nt * 8 + 2 * lt, M - 1), c1 = min(nt * 8 + 2 * lt + 1, M - 1);
-        ffma2(acc.s[nt][0], acc.s[nt][2], sa[0], sb[0], d0[0], d0[2]);
-        ffma2(acc.s[nt][0], acc.s[nt][2], sa[1], sb[1], d1[0], d1[2]);
-        ffma2(acc.s[nt][1], acc.s[nt][3], sa[0], sb[0], d0[1], d0[3]);
-        ffma2(acc.s[nt][1], acc.s[nt][3], sa[1], sb[1], d1[1], d1[3]);
-        ffma2(acc.b[nt][0], acc.b[nt][2], ba[0], bb[0], xs[2 * c0], xs[2 * c0]);
-        ffma2(acc.b[nt][0], acc.b[nt][2], ba[1], bb[1], xs[2 * c0 + 1], xs[2 * c0 + 1]);
-        ffma2(acc.b[nt][1], acc.b[nt][3], ba[0], bb[0], xs[2 * c1], xs[2 * c1]);
-        ffma2(acc.b[nt][1], acc.b[nt][3], ba[1], bb[1], xs[2 * c1 + 1], xs[2 * c1 + 1]);
+        mma_16816(d0, h0x[0], h0x[1], h0x[2], h0x[3], f0.x, f0.y);
+        mma_16816(d0, h0y[0], h0y[1], h0y[2], h0y[3], f0.z, f0.w);
+        mma_16816(d1, h1x[0], h1x[1], h1x[2], h1x[3], f1.x, f1.y);
+        mma_16816(d1, h1y[0], h1y[1], h1y[2], h1y[3], f1.z, f1.w);
+        if (M1) {
+            ffma2(acc.s[0][0], acc.s[0][2], sa[0], sb[0], d0[0], d0[2]);
+            ffma2(acc.s[0][0], acc.s[0][2], sa[1], sb[1], d1[0], d1[2]);
+            ffma2(acc.b[0][0], acc.b[0][2], ba[0], bb[0], xs[0], xs[0]);
+            ffma2(acc.b[0][0], acc.b[0][2], ba[1], bb[1], xs[1], xs[1]);
+        } else {
+            const int c0 = min(nt * 8 + 2 * lt, M - 1), c1 = min(nt * 8 + 2 * lt + 1, M - 1);
+            ffma2(acc.s[nt][0], acc.s[nt][2], sa[0], sb[0], d0[0], d0[2]);
+            ffma2(acc.s[nt][0], acc.s[nt][2], sa[1], sb[1], d1[0], d1[2]);
+            ffma2(acc.s[nt][1], acc.s[nt][3], sa[0], sb[0], d0[1], d0[3]);
+            ffma2(acc.s[nt][1], acc.s[nt][3], sa[1], sb[1], d1[1], d1[3]);
+            ffma2(acc.b[nt][0], acc.b[nt][2], ba[0], bb[0], xs[2 * c0], xs[2 * c0]);
+            ffma2(acc.b[nt][0], acc.b[nt][2], ba[1], bb[1], xs[2 * c0 + 1], xs[2 * c0 + 1]);
+            ffma2(acc.b[nt][1], acc.b[nt][3], ba[0], bb[0], xs[2 * c1], xs[2 * c1]);
+            ffma2(acc.b[nt][1], acc.b[nt][3], ba[1], bb[1], xs[2 * c1 + 1], xs[2 * c1 + 1]);
+        }
     }
 }
 
-// The lane's B mask of the group-32 M1 path (see group_mma_g32).
-__device__ __forceinline__ uint32_t g32_m1_mask(int lg, int lt) {
-    return ((lt >> 1) == (lg & 1)) ? 0xffffffffu : 0u;
-}
+// Group 32: byte offset, within a stage, of word t of row g in box `box`
+// (group j adds ((2j + h) ^ (g % 8)) << 4 for half h; row g+8 is 1024 bytes
+// further with the same swizzle phase).
+__device__ __forceinline__ int g32_offset(int box, int lg, int lt) { return box * kBoxBytes + lg * 128 + 4 * lt; }
 
 // Shared-memory byte offsets, within a stage, of the words a lane reads for
 // group j (0..3) of box `box`: row g, 16-byte chunk 2j + t/2 under the
@@ -456,11 +473,11 @@ __device__ __forceinline__ void box_scales_g32(float (&fsa)[4][2], float (&fsb)[
 // box_vec_ok(f).  FMT: kFmtG64 reads one scale and one bias per group
 // (f.ngs groups per row), kFmtS128 one scale per two groups and no bias (the
 // bias sums then accumulate scale * sum x: see Acc::value), kFmtAny follows
-// f, kFmtG32 is the group-32 variant (hmask: see group_mma_g32).
+// f, kFmtG32 is the group-32 variant (goff: see g32_offset).
 template <int NT, bool M1, bool FULL, int FMT>
 __device__ __forceinline__ void box_mma(Acc<NT> &acc, const uint8_t *st, const int (&off)[4], const uint16_t *sp,
                                         const WFmt &f, int g, int n, const uint4 *xl, int xd1, const float *xs,
-                                        int M, int lg, int lt, uint32_t hmask = 0u) {
+                                        int M, int lg, int lt, int goff = 0) {
     const int xstep = 2 * M * 4;  // uint4 words of staged activations per group
     if (FMT == kFmtG32) {
         float fsa[4][2], fsb[4][2], fba[4][2], fbb[4][2];
@@ -468,10 +485,14 @@ __device__ __forceinline__ void box_mma(Acc<NT> &acc, const uint8_t *st, const i
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             if (FULL || j < n) {
-                const uint2 wa = *reinterpret_cast<const uint2 *>(st + off[j]);
-                const uint2 wb = *reinterpret_cast<const uint2 *>(st + off[j] + 8 * 128);
-                group_mma_g32<NT, M1>(acc, wa, wb, fsa[j], fsb[j], fba[j], fbb[j], xl + j * (M1 ? 8 : xstep), xd1,
-                                      xs + j * 2 * M, M, lt, hmask);
+                const uint8_t *p0 = st + goff + ((((2 * j) ^ (lg & 7))) << 4);
+                const uint8_t *p1 = st + goff + ((((2 * j + 1) ^ (lg & 7))) << 4);
+                const uint32_t wa0 = *reinterpret_cast<const uint32_t *>(p0);
+                const uint32_t wa1 = *reinterpret_cast<const uint32_t *>(p1);
+                const uint32_t wb0 = *reinterpret_cast<const uint32_t *>(p0 + 8 * 128);
+                const uint32_t wb1 = *reinterpret_cast<const uint32_t *>(p1 + 8 * 128);
+                group_mma_g32<NT, M1>(acc, wa0, wa1, wb0, wb1, fsa[j], fsb[j], fba[j], fbb[j],
+                                      xl + j * (M1 ? 8 : xstep), xd1, xs + j * 2 * M, M, lt);
             }
         }
         return;
