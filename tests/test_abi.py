@@ -228,3 +228,6 @@ def test_w4_gemm_host_validation(lib):
     assert g(f, f, f, f, f, 64, 256, 512, 64, f, need - 1, None) == c["W4_ERR_WORKSPACE"]
     assert g(f + 8, f, f, f, f, 64, 256, 512, 64, f, need, None) == c["W4_ERR_ALIGN"]
     assert g(f, f, f, f, f, 64, 256, 512, 64, f + 4, need, None) == c["W4_ERR_ALIGN"]
+    lib.w4_gemm_ex.argtypes = [P, P, P, P, P, I, I, I, I, P, Z, ctypes.c_uint, P]
+    for bad_flags in (2, 0x80000000):
+        assert lib.w4_gemm_ex(f, f, f, f, f, 64, 256, 512, 64, f, need, bad_flags, None) == c["W4_ERR_SHAPE"]
