@@ -32,8 +32,11 @@ def lib():
 
 def test_header_declares_the_hot_path_calls():
     names = set(_declared())
-    assert {"w4_gemv", "lm_head_argmax_topk", "lm_head_workspace_bytes", "w4_dequant_f16",
-            "f16_gemm", "w4a16_status_string", "w4a16_device_status"} <= names
+    assert {"w4_gemv", "w4_gemv_ex", "w4_gemv_seq", "w4_gemv_seq_workspace_bytes", "w4_gemv_seq_workspace_bytes_ex",
+            "lm_head_argmax_topk", "lm_head_argmax_topk_ex", "lm_head_argmax_topk_noalloc",
+            "lm_head_workspace_bytes", "w4_dequant_f16", "w4_dequant_f16_ex", "f16_gemm", "f16_gemm_ex",
+            "w4_gemm", "w4_gemm_ex", "w4_gemm_workspace_bytes", "w4a16_status_string",
+            "w4a16_device_status"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):
