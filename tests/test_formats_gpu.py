@@ -171,6 +171,24 @@ def test_dequant_formats_bit_exact(w4, group, sym, N, K):
     assert np.array_equal(got, oracle.dequant_f16_t(qw, s, b, N, K, group=group))
 
 
+@pytest.mark.parametrize("pad", [0, 5])
+def test_dequant_symmetric_golden(w4, pad):
+    """The hand-derived symmetric values (signed zeros, infinities, subnormals,
+    a rounding tie): row i holds golden line i's scale and its code at k = 0.
+    11 rows take the transpose kernel, 16 the tensor-copy kernel."""
+    from conftest import golden_lines
+    lines = [ln.split(";")[0].split() for ln in golden_lines("dequant_sym_f16.txt")]
+    N, K = len(lines) + pad, 64
+    qw = np.zeros((N, K // 8), dtype=np.uint32)
+    s = np.full((N, 1), 0x3C00, dtype=np.uint16)
+    for i, (sb, q, _) in enumerate(lines):
+        qw[i, 0] = int(q)
+        s[i, 0] = int(sb, 16)
+    got = w4.w4_dequant_f16(to_dev(qw), to_dev(s.view(np.float16)), None).cpu().numpy().view(np.uint16)
+    for i, (_, _, want) in enumerate(lines):
+        assert int(got[0, i]) == int(want, 16), (lines[i], hex(int(got[0, i])))
+
+
 @pytest.mark.parametrize("N", [512, 510])
 def test_dequant_symmetric_extreme_scales(w4, N):
     """Symmetric codes with scales from every binary16 exponent and sign

@@ -328,6 +328,16 @@ def test_dequant_symmetric_vs_fraction():
     assert np.array_equal(w[:, 16:], np.repeat(-8.0 * w[:, 9:10], 48, axis=1))
 
 
+def test_dequant_symmetric_golden():
+    for line in golden_lines("dequant_sym_f16.txt"):
+        data = line.split(";")[0].split()
+        s_bits, q, want = int(data[0], 16), int(data[1]), int(data[2], 16)
+        qw = np.full((1, 8), q, dtype=np.uint32)   # code q at k = 0, zeros elsewhere
+        s = np.array([[s_bits]], dtype=np.uint16)
+        got = int(oracle.dequant_f16_rows(qw, s, None, 64, [0])[0, 0])
+        assert got == want, (line, hex(got))
+
+
 def _linear(seed, N, K, group, sym):
     if sym:
         return synth.make_linear_sym(seed, N, K, group)
