@@ -609,7 +609,8 @@ def main():
         "config": {"workload": "qwen2.5-3b: prefill M=1570 (dequant-once + f16 GEMM), decode M=1 "
                                "(36 layers x [qkv, o, gate_up, down] GEMVs as one dependent projection list "
                                "+ lm_head top-50), batched decode M=16 (+ per-row argmax); q/k/v and gate/up "
-                               "stored as fused row blocks",
+                               "stored as fused row blocks; also the decode token in the symmetric group-128 "
+                               "format and M=128 prefill through w4_gemm (parts)",
                    "model": "Qwen2.5-3B-shaped projections x36 + lm_head 2048->151936",
                    "global_batch": 1, "seq_len": PREFILL_M, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (1.74 GB of weights per decode pass, 5.5 GB scratch)"},
