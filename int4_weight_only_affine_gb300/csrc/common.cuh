@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/w4a16.h"
 
 namespace w4a16 {
@@ -51,6 +53,31 @@ inline bool make_fmt(WFmt &f, int K, int group, bool sym) {
 inline int launch_status() {
     cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? W4A16_OK : W4_ERR_LAUNCH;
+}
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device, size) and thread-safe, so that launches
+// captured into CUDA graphs make no attribute calls.  False if the runtime
+// refuses (its error is cleared).
+inline bool set_smem_once(const void *kern, int bytes) {
+    struct Entry {
+        const void *kern;
+        int dev, bytes;
+    };
+    static std::mutex mu;
+    static Entry done[64];
+    static int n = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n; ++i)
+        if (done[i].kern == kern && done[i].dev == dev && done[i].bytes >= bytes) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (n < 64) done[n++] = Entry{kern, dev, bytes};
+    return true;
 }
 
 // Number of SMs of the current device (cached per device).

@@ -313,14 +313,7 @@ static int dequant_impl(const uint32_t *qweight, const uint16_t *scales, const u
         const bool any = !(f.gs == 1 && !f.sym);
         auto kern = any ? dequant_tma_kernel<true> : dequant_tma_kernel<false>;
         const int smem = (any ? tma_smem<true>() : tma_smem<false>()) + 1024;
-        static bool attr_set[2][64] = {{false}};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (dev >= 0 && dev < 64 && !attr_set[any][dev]) {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-                return W4_ERR_LAUNCH;
-            attr_set[any][dev] = true;
-        }
+        if (!set_smem_once(reinterpret_cast<const void *>(kern), smem)) return W4_ERR_LAUNCH;
         long long grid = (long long)sm_count() * 2;
         if (grid > ntiles) grid = ntiles;
         cudaLaunchConfig_t cfg = {};

@@ -1041,25 +1041,11 @@ static int gemm_impl(const uint16_t *x16, const uint16_t *w16, uint16_t *y, int 
     if (!make_map(&tb, w16, (uint64_t)N, (uint64_t)K, 64, BK)) return W4_ERR_DEVICE;
     // The pair kernel loads 128-row A boxes (one per CTA) and the same B boxes.
     CUtensorMap ta2 = ta, tb2 = tb;
-    static bool attr_set[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) !=
-            cudaSuccess)
-            return W4_ERR_LAUNCH;
-        attr_set[dev] = true;
-    }
+    if (!set_smem_once(reinterpret_cast<const void *>(gemm_kernel), (int)SMEM_BYTES)) return W4_ERR_LAUNCH;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (M > BM) {
         // CTA pairs: 256 x 256 tiles, half the operand traffic per SM.
-        static bool attr2_set[64] = {false};
-        if (dev >= 0 && dev < 64 && !attr2_set[dev]) {
-            if (cudaFuncSetAttribute(gemm2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)SMEM2_BYTES) != cudaSuccess)
-                return W4_ERR_LAUNCH;
-            attr2_set[dev] = true;
-        }
+        if (!set_smem_once(reinterpret_cast<const void *>(gemm2_kernel), (int)SMEM2_BYTES)) return W4_ERR_LAUNCH;
         const int tiles = ((M + 255) / 256) * ((N + BN - 1) / BN);
         int pairs = sm_count() / 2;
         if (pairs > tiles) pairs = tiles;
@@ -1167,15 +1153,7 @@ int w4gemm_impl(const uint16_t *x, const uint32_t *qweight, const uint16_t *scal
     if (!make_map_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, qweight, (uint64_t)K / 8, (uint64_t)N, (uint64_t)K / 2,
                      32, FBN, CU_TENSOR_MAP_SWIZZLE_128B))
         return W4_ERR_DEVICE;
-    static bool attr_set[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(w4gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)F_SMEM) !=
-            cudaSuccess)
-            return W4_ERR_LAUNCH;
-        attr_set[dev] = true;
-    }
+    if (!set_smem_once(reinterpret_cast<const void *>(w4gemm_kernel), (int)F_SMEM)) return W4_ERR_LAUNCH;
     const int sms = sm_count();
     W4GemmArgs a;
     a.sc = scales;
