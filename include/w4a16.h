@@ -261,7 +261,10 @@ W4A16_API int w4_dequant_f16_ex(const uint32_t *qweight, const uint16_t *scales,
  *   workspace  device buffer of at least w4_gemm_workspace_bytes(M, N, K)
  *              bytes, 16-byte aligned, ZERO-FILLED before its first use and
  *              then passed unchanged to later calls (its tile counters return
- *              to zero at the end of every call); used by one call at a time.
+ *              to zero at the end of every call).  Calls ordered on one
+ *              stream may share it, also with W4A16_OVERLAP_PREVIOUS (a call
+ *              touches it only after its dependency wait); calls that may run
+ *              concurrently need separate workspaces.
  *              Small N splits K over several blocks whose fp32 partial sums
  *              it holds.
  *   With a single K split (large N) the result equals f16_gemm on the
