@@ -1,33 +1,40 @@
-"""Benchmark of the W4A16 hot path on Qwen2.5-3B shapes (synthetic, seeded).
+"""Benchmark of the W4A16 hot path on the workloads' model shapes (synthetic, seeded).
 
-One step is one pass of the whole hot path (per layer the weights are held
-as four row blocks: q|k|v, o, gate|up, down, i.e. the 7 projections with the
-blocks that share an input stored contiguously):
-  prefill  - w4_dequant_f16 of all 144 weight blocks into the transposed half
-             scratch, then f16_gemm at M = 1570 for each block;
-  decode   - one token at M = 1: the 144 projection GEMVs in layer order as
-             one w4_gemv_seq list (a persistent launch per 96 operations;
-             every operation waits until all earlier ones are complete, as a
-             dependent chain of projections would), then the lm_head GEMV
-             fused with top-50 selection;
-  batched  - the same projection set at M = 16 activation rows (one w4_gemv
-             per block, each streaming its weights while the previous kernel
-             finishes), then per-row greedy argmax over the lm_head;
+One step is one pass of the whole hot path over every workload (per layer the
+weights are held as four row blocks: q|k|v, o, gate|up, down, i.e. the 7
+projections with the blocks that share an input stored contiguously):
+  single   - one 896 x 896 GEMV at M = 1 (Qwen2.5-0.5B q_proj), repeated on
+             the same weight (L2-resident, "warm") and over 600 distinct
+             copies (271 MB, more than twice the 129 MB L2, "rotated"); and
+             the 1000 x 896 GEMV fused with top-5 selection over 600 copies;
+  0.6B     - one Qwen3-0.6B decode token at M = 1: 28 layers x 4 blocks as
+             one dependent projection list, then the lm_head GEMV with
+             greedy argmax;
+  decode   - one Qwen2.5-3B token at M = 1: the 144 projection GEMVs in layer
+             order as one w4_gemv_seq list (a persistent launch per 96
+             operations; every operation waits until all earlier ones are
+             complete, as a dependent chain of projections would), then the
+             lm_head GEMV fused with top-50 selection;
+  batched  - the 3B projection set at M = 2, 4, 8, 16 activation rows (one
+             w4_gemv per block, each streaming its weights while the previous
+             kernel finishes), then per-row greedy argmax over the lm_head;
   kernels  - the lm_head GEMV + top-50 alone, and the 36 gate|up GEMVs
              (2048 -> 22016) back to back: per-kernel decode bandwidth;
-  sym128   - the decode token again with the same shapes in the symmetric
-             group-128 format (scale only, w = scale * (q - 8));
-  small-M  - prefill of M = 128 tokens: w4_gemm (dequantisation inside the
-             tensor-core GEMM) over the 144 blocks, beside f16_gemm at M = 128
-             on the dequantised scratch (dequant-once + GEMM = the dequant
-             part + that part).
+  sym128   - the 3B decode token again in the symmetric group-128 format
+             (scale only, w = scale * (q - 8));
+  prefill  - w4_dequant_f16 of all 144 3B weight blocks into the transposed
+             half scratch, then f16_gemm for each block at M = 128, 512, 1570
+             and 4096 tokens; and M = 128 through w4_gemm (dequantisation
+             inside the tensor-core GEMM).
 Each part is a CUDA graph replayed on one stream; CUDA events time each part.
-The headline `value` is the decode GEMV bandwidth (algorithmic bytes of the
-token's weights / decode time), the first quantity of the metric; the other
-quantities are reported under `parts`.
+The headline `value` is the 3B decode-token bandwidth (algorithmic bytes of
+the token's weights / decode time), the first quantity of the metric; the
+other quantities are reported under `parts`.  `e2e` runs the decode token
+through the public API every step (projection list + lm_head calls, pinned
+host activations copied in, the top-50 copied out).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-       python bench.py --profile gemv|gemm|dequant|lmhead|seq|w4gemm   (small case for ncu)
+       python bench.py --profile gemv|gemv16|gemm|gemm_all|dequant|lmhead|seq|w4gemm   (cases for ncu)
 Under torchrun (N > 1) every rank runs an independent replica (the path has no
 exchange step) and rank 0 prints one JSON line.
 """
@@ -53,11 +60,21 @@ METRIC = "W4A16 decode GEMV GB/s (% HBM peak); prefill TFLOP/s; 3B-shape decode 
 LAYERS = synth.QWEN25_3B_LAYERS
 PROJ = synth.QWEN25_3B
 LM_K, LM_N = synth.QWEN25_3B_LM_HEAD
+PREFILL_MS = (128, 512, 1570, 4096)
 PREFILL_M = 1570
 SMALL_M = 128
+BATCH_MS = (2, 4, 8, 16)
 BATCH_M = 16
 TOPK = 50
+ROT_COPIES = 600       # distinct single-GEMV weights per rotation (> 2x L2 of bytes)
+WARM_REPS = 200
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Datasheet peaks of one GB300: HBM3e 8 TB/s; dense FP16/BF16 tensor 2.25
+# PFLOP/s (NVIDIA's HGX B300 figure, 36 PFLOPS FP16/BF16 per 8 GPUs, is with
+# 2:4 sparsity; dense is half of it per GPU).
+SPEC_PEAKS = {"hbm_gbs": 8000.0, "fp16_dense_tflops": 2250.0}
+SPEC_SOURCE = ("GB300 datasheet: HBM3e 8 TB/s; dense FP16/BF16 tensor 2.25 PFLOP/s "
+               "(HGX B300: 36 PFLOPS per 8 GPUs with 2:4 sparsity)")
 
 
 def weight_bytes(N, K):
@@ -74,6 +91,27 @@ PROJ_WEIGHTS = LAYERS * sum(N * K for _, K, N in PROJ)
 PREFILL_FLOPS = 2.0 * PREFILL_M * PROJ_WEIGHTS
 SMALL_FLOPS = 2.0 * SMALL_M * PROJ_WEIGHTS
 DEQUANT_BYTES = LAYERS * sum(weight_bytes(N, K) + 2 * N * K for _, K, N in PROJ)
+L06, PROJ06 = synth.QWEN3_06B_LAYERS, synth.QWEN3_06B
+LM06_K, LM06_N = synth.QWEN3_06B_LM_HEAD
+DECODE06_BYTES = L06 * sum(weight_bytes(N, K) for _, K, N in PROJ06) + weight_bytes(LM06_N, LM06_K)
+SINGLE_N, SINGLE_K = 896, 896            # Qwen2.5-0.5B q_proj
+SEL_N, SEL_K, SEL_TOPK = 1000, 896, 5    # the same call with top-5 over 1000 rows
+SINGLE_BYTES = weight_bytes(SINGLE_N, SINGLE_K) + 2 * SINGLE_K + 2 * SINGLE_N   # weights + x + y
+SEL_BYTES = weight_bytes(SEL_N, SEL_K) + 2 * SEL_K
+
+CONFIG = {
+    "workload": ("qwen2.5-0.5b q_proj GEMV 896x896 M=1 (warm and rotated over 271 MB) + 1000x896 top-5; "
+                 "qwen3-0.6b decode token M=1 (28 layers as a dependent projection list + lm_head argmax); "
+                 "qwen2.5-3b decode token M=1 (36 layers x [qkv, o, gate_up, down] as one dependent projection "
+                 "list + lm_head top-50; headline); 3b batched decode M=2/4/8/16 (+ per-row argmax); "
+                 "3b prefill dequant-once + f16 GEMM at M=128/512/1570/4096 and w4_gemm at M=128; 3b decode "
+                 "token in the symmetric group-128 format (parts)"),
+    "model": "Qwen2.5-3B-shaped projections x36 + lm_head 2048->151936 (headline); Qwen3-0.6B and "
+             "Qwen2.5-0.5B shapes in parts",
+    "global_batch": 1, "seq_len": PREFILL_M,
+    "l2": "inputs larger than L2 (1.74 GB of weights per 3B decode pass, 5.5 GB scratch; single GEMVs rotated "
+          "over 600 copies), except the part marked warm",
+}
 
 
 def load_peaks():
@@ -159,53 +197,68 @@ class ClockSampler:
 # bytes and the arithmetic are those of the separate projections.
 FUSED = [("qkv", 2048, 2048 + 256 + 256, ("q", "k", "v")), ("o", 2048, 2048, ("o",)),
          ("gate_up", 2048, 2 * 11008, ("gate", "up")), ("down", 11008, 2048, ("down",))]
+FUSED06 = [("qkv", 1024, 2048 + 1024 + 1024, ("q", "k", "v")), ("o", 2048, 1024, ("o",)),
+           ("gate_up", 1024, 2 * 3072, ("gate", "up")), ("down", 3072, 1024, ("down",))]
 SRC = {"qkv": "attn", "o": "o", "gate_up": "mlp", "down": "down"}
 PROJ_SRC = {"q": "attn", "k": "attn", "v": "attn", "o": "o", "gate": "mlp", "up": "mlp", "down": "down"}
 
 
 class Model:
-    """Device-resident synthetic Qwen2.5-3B projection set + lm_head."""
+    """Device-resident synthetic weights: the Qwen2.5-3B projection set +
+    lm_head (affine group 64, and symmetric group 128), the Qwen3-0.6B set +
+    lm_head, and the rotated single-GEMV copies."""
 
     def __init__(self, torch, w4, dev):
         self.torch, self.w4, self.dev = torch, w4, dev
         t0 = time.time()
-        seeds = {name: p for p, (name, _, _) in enumerate(PROJ)}
-        rows = {name: n for name, _, n in PROJ}
-        self.layers = []
-        for l in range(LAYERS):
-            blocks = {}
-            for name, K, N, parts in FUSED:
-                mats = [synth.make_linear(synth.layer_seed(1000, l, seeds[q]), rows[q], K) for q in parts]
-                qw, s, b = (np.concatenate([m[i] for m in mats]) for i in range(3))
-                blocks[name] = (self._up(qw.view(np.int32)), self._up(s), self._up(b), N, K)
-            self.layers.append(blocks)
+        self.layers = self._blocks(PROJ, FUSED, LAYERS, 1000, sym=False)
         qw, s, b = synth.make_linear(99, LM_N, LM_K)
         self.lm = (self._up(qw.view(np.int32)), self._up(s), self._up(b), LM_N, LM_K)
         # The same shapes in the symmetric group-128 format (scales only).
-        self.layers_s128 = []
-        for l in range(LAYERS):
-            blocks = {}
-            for name, K, N, parts in FUSED:
-                mats = [synth.make_linear_sym(synth.layer_seed(5000, l, seeds[q]), rows[q], K, 128) for q in parts]
-                qw = np.concatenate([m[0] for m in mats])
-                s = np.concatenate([m[1] for m in mats])
-                blocks[name] = (self._up(qw.view(np.int32)), self._up(s), None, N, K)
-            self.layers_s128.append(blocks)
+        self.layers_s128 = self._blocks(PROJ, FUSED, LAYERS, 5000, sym=True)
         qw, s, _ = synth.make_linear_sym(98, LM_N, LM_K, 128)
         self.lm_s128 = (self._up(qw.view(np.int32)), self._up(s), None, LM_N, LM_K)
+        # Qwen3-0.6B.
+        self.layers06 = self._blocks(PROJ06, FUSED06, L06, 3000, sym=False)
+        qw, s, b = synth.make_linear(97, LM06_N, LM06_K)
+        self.lm06 = (self._up(qw.view(np.int32)), self._up(s), self._up(b), LM06_N, LM06_K)
+        # Single-GEMV weights: copy 0 is the seed-0 weight; the others rotate.
+        self.single = [self._linear(0 + i, SINGLE_N, SINGLE_K) for i in range(ROT_COPIES)]
+        self.sel = [self._linear(20000 + i, SEL_N, SEL_K) for i in range(ROT_COPIES)]
         self.setup_s = time.time() - t0
+
+    def _linear(self, seed, N, K):
+        qw, s, b = synth.make_linear(seed, N, K)
+        return self._up(qw.view(np.int32)), self._up(s), self._up(b)
+
+    def _blocks(self, proj, fused, layers, base, sym):
+        seeds = {name: p for p, (name, _, _) in enumerate(proj)}
+        rows = {name: n for name, _, n in proj}
+        out = []
+        for l in range(layers):
+            blocks = {}
+            for name, K, N, parts in fused:
+                if sym:
+                    mats = [synth.make_linear_sym(synth.layer_seed(base, l, seeds[q]), rows[q], K, 128)
+                            for q in parts]
+                    qw = np.concatenate([m[0] for m in mats])
+                    s = np.concatenate([m[1] for m in mats])
+                    blocks[name] = (self._up(qw.view(np.int32)), self._up(s), None, N, K)
+                else:
+                    mats = [synth.make_linear(synth.layer_seed(base, l, seeds[q]), rows[q], K) for q in parts]
+                    qw, s, b = (np.concatenate([m[i] for m in mats]) for i in range(3))
+                    blocks[name] = (self._up(qw.view(np.int32)), self._up(s), self._up(b), N, K)
+            out.append(blocks)
+        return out
 
     def _up(self, a):
         return self.torch.from_numpy(np.ascontiguousarray(a)).to(self.dev)
 
 
-def x_inputs(torch, dev, M, seed):
+def x_inputs(torch, dev, M, seed, dims=(2048, 2048, 2048, 11008, LM_K)):
     """Activations per block: attn (q,k,v), o, mlp (gate, up), down, lm_head."""
-    return {"attn": torch.from_numpy(synth.make_x(seed, M, 2048)).to(dev),
-            "o": torch.from_numpy(synth.make_x(seed + 100, M, 2048)).to(dev),
-            "mlp": torch.from_numpy(synth.make_x(seed + 200, M, 2048)).to(dev),
-            "down": torch.from_numpy(synth.make_x(seed + 300, M, 11008)).to(dev),
-            "lm": torch.from_numpy(synth.make_x(seed + 400, M, LM_K)).to(dev)}
+    names = ("attn", "o", "mlp", "down", "lm")
+    return {n: torch.from_numpy(synth.make_x(seed + 100 * i, M, K)).to(dev) for i, (n, K) in enumerate(zip(names, dims))}
 
 
 def run_ours(args, rank, world):
@@ -217,92 +270,129 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(dev)
     model = Model(torch, w4, dev)
     stream = torch.cuda.Stream(dev)
+    ov = w4.OVERLAP_PREVIOUS  # weights are constant: stream them while the previous kernel finishes
 
-    xs1 = x_inputs(torch, dev, 1, 10)
-    xs16 = x_inputs(torch, dev, BATCH_M, 20)
-    ys1 = {n: torch.empty((1, N), dtype=torch.float16, device=dev) for n, K, N, _ in FUSED}
-    ys16 = {n: torch.empty((BATCH_M, N), dtype=torch.float16, device=dev) for n, K, N, _ in FUSED}
-    idx1 = torch.empty((1, TOPK), dtype=torch.int32, device=dev)
-    val1 = torch.empty((1, TOPK), dtype=torch.float32, device=dev)
-    idx16 = torch.empty((BATCH_M, 1), dtype=torch.int32, device=dev)
-    val16 = torch.empty((BATCH_M, 1), dtype=torch.float32, device=dev)
-    ws1 = torch.empty(w4.lm_head_workspace_bytes(1, LM_N, TOPK), dtype=torch.uint8, device=dev)
-    ws16 = torch.empty(w4.lm_head_workspace_bytes(BATCH_M, LM_N, 1), dtype=torch.uint8, device=dev)
-    # prefill buffers: one transposed scratch per weight block; activations/outputs per kind
-    scratch = [{n: torch.empty((K, N), dtype=torch.float16, device=dev) for n, K, N, _ in FUSED}
-               for _ in range(LAYERS)]
-    xp = {"attn": torch.randn((PREFILL_M, 2048), device=dev).half(),
-          "o": torch.randn((PREFILL_M, 2048), device=dev).half(),
-          "mlp": torch.randn((PREFILL_M, 2048), device=dev).half(),
-          "down": torch.randn((PREFILL_M, 11008), device=dev).half()}
-    yp = {n: torch.empty((PREFILL_M, N), dtype=torch.float16, device=dev) for n, K, N, _ in FUSED}
-    xs128 = {k: v[:SMALL_M].contiguous() for k, v in xp.items()}
-    ys128 = {n: torch.empty((SMALL_M, N), dtype=torch.float16, device=dev) for n, K, N, _ in FUSED}
+    def new(shape, dtype=torch.float16):
+        return torch.empty(shape, dtype=dtype, device=dev)
+
+    # ---- decode buffers ----
+    xs = {M: x_inputs(torch, dev, M, 10 if M == 1 else 20 + M) for M in (1,) + BATCH_MS}
+    ys = {M: {n: new((M, N)) for n, K, N, _ in FUSED} for M in (1,) + BATCH_MS}
+    idx1, val1 = new((1, TOPK), torch.int32), new((1, TOPK), torch.float32)
+    sel_b = {M: (new((M, 1), torch.int32), new((M, 1), torch.float32),
+                 new(w4.lm_head_workspace_bytes(M, LM_N, 1), torch.uint8)) for M in BATCH_MS}
+    ws1 = new(w4.lm_head_workspace_bytes(1, LM_N, TOPK), torch.uint8)
+    ys_gu = new((1, 2 * 11008))
+    # ---- 0.6B decode buffers ----
+    xs06 = x_inputs(torch, dev, 1, 30, dims=(1024, 2048, 1024, 3072, LM06_K))
+    ys06 = {n: new((1, N)) for n, K, N, _ in FUSED06}
+    idx06, val06 = new((1, 1), torch.int32), new((1, 1), torch.float32)
+    ws06 = new(w4.lm_head_workspace_bytes(1, LM06_N, 1), torch.uint8)
+    # ---- single GEMV (config 0) ----
+    x896 = torch.from_numpy(synth.make_x(0, 1, SINGLE_K)).to(dev)
+    y896 = new((1, SINGLE_N))
+    idx5, val5 = new((1, SEL_TOPK), torch.int32), new((1, SEL_TOPK), torch.float32)
+    ws5 = new(w4.lm_head_workspace_bytes(1, SEL_N, SEL_TOPK), torch.uint8)
+    # ---- prefill buffers: one transposed scratch per weight block; x/y per kind at the largest M ----
+    scratch = [{n: new((K, N)) for n, K, N, _ in FUSED} for _ in range(LAYERS)]
+    MX = max(PREFILL_MS)
+    xp = {k: (torch.randn((MX, K), device=dev)).half() for k, K in
+          (("attn", 2048), ("o", 2048), ("mlp", 2048), ("down", 11008))}
+    yp = {n: new((MX, N)) for n, K, N, _ in FUSED}
     ws_gemm = w4.w4_gemm_workspace(SMALL_M, max(N for _, _, N, _ in FUSED), max(K for _, K, _, _ in FUSED),
                                    dev)  # zero-filled once; its tile counters reset themselves
-    ov = w4.OVERLAP_PREVIOUS  # weights are constant: stream them while the previous kernel finishes
+
     # decode M=1: the projection list, each operation waiting for all earlier ones
-    seq_ops = []
-    for l in range(LAYERS):
-        for name, _, _, _ in FUSED:
-            qw, s, b, N, K = model.layers[l][name]
-            seq_ops.append((xs1[SRC[name]], qw, s, b, ys1[name], len(seq_ops) > 0))
-    seq_ws = w4.seq_workspace(seq_ops)  # zero-filled once; its counters reset themselves
-    seq_ops_s128 = []
-    for l in range(LAYERS):
-        for name, _, _, _ in FUSED:
-            qw, s, b, N, K = model.layers_s128[l][name]
-            seq_ops_s128.append((xs1[SRC[name]], qw, s, None, ys1[name], len(seq_ops_s128) > 0, 128))
-    seq_ws_s128 = w4.seq_workspace(seq_ops_s128)
-    ys_gu = torch.empty((1, 2 * 11008), dtype=torch.float16, device=dev)
+    def seq_list(layers, fused, x, y, group=None):
+        ops = []
+        for l in range(len(layers)):
+            for name, _, _, _ in fused:
+                qw, s, b, N, K = layers[l][name]
+                op = (x[SRC[name]], qw, s, b, y[name], len(ops) > 0)
+                ops.append(op + ((group,) if group else ()))
+        return w4.GemvList(ops)
+
+    seq3b = seq_list(model.layers, FUSED, xs[1], ys[1])
+    seq3b_ws = seq3b.workspace()          # zero-filled once; its counters reset themselves
+    seq_s128 = seq_list(model.layers_s128, FUSED, xs[1], ys[1], group=128)
+    seq_s128_ws = seq_s128.workspace()
+    seq06 = seq_list(model.layers06, FUSED06, xs06, ys06)
+    seq06_ws = seq06.workspace()
 
     def decode_seq():
-        w4.w4_gemv_seq(seq_ops, workspace=seq_ws, stream=stream)
+        seq3b.run(seq3b_ws, stream)
         qw, s, b, N, K = model.lm
-        w4.lm_head_argmax_topk(xs1["lm"], qw, s, b, k=TOPK, idx=idx1, val=val1, workspace=ws1, stream=stream,
+        w4.lm_head_argmax_topk(xs[1]["lm"], qw, s, b, k=TOPK, idx=idx1, val=val1, workspace=ws1, stream=stream,
                                flags=ov)
 
     def decode_seq_s128():
-        w4.w4_gemv_seq(seq_ops_s128, workspace=seq_ws_s128, stream=stream)
+        seq_s128.run(seq_s128_ws, stream)
         qw, s, b, N, K = model.lm_s128
-        w4.lm_head_argmax_topk(xs1["lm"], qw, s, None, k=TOPK, idx=idx1, val=val1, workspace=ws1, stream=stream,
+        w4.lm_head_argmax_topk(xs[1]["lm"], qw, s, None, k=TOPK, idx=idx1, val=val1, workspace=ws1, stream=stream,
                                flags=ov, group=128)
+
+    def decode06():
+        seq06.run(seq06_ws, stream)
+        qw, s, b, N, K = model.lm06
+        w4.lm_head_argmax_topk(xs06["lm"], qw, s, b, k=1, idx=idx06, val=val06, workspace=ws06, stream=stream,
+                               flags=ov)
+
+    def single_warm():
+        qw, s, b = model.single[0]
+        for _ in range(WARM_REPS):
+            w4.w4_gemv(x896, qw, s, b, y=y896, stream=stream, flags=ov)
+
+    def single_rot():
+        for qw, s, b in model.single:
+            w4.w4_gemv(x896, qw, s, b, y=y896, stream=stream, flags=ov)
+
+    def sel_rot():
+        for qw, s, b in model.sel:
+            w4.lm_head_argmax_topk(x896, qw, s, b, k=SEL_TOPK, idx=idx5, val=val5, workspace=ws5, stream=stream,
+                                   flags=ov)
 
     def w4gemm_small():
         first = True
         for l in range(LAYERS):
-            for name, _, _, _ in FUSED:
+            for name, _, N, _ in FUSED:
                 qw, s, b, N, K = model.layers[l][name]
-                w4.w4_gemm(xs128[SRC[name]], qw, s, b, y=ys128[name], workspace=ws_gemm, stream=stream,
-                           flags=0 if first else ov)
+                w4.w4_gemm(xp[SRC[name]][:SMALL_M], qw, s, b, y=yp[name][:SMALL_M], workspace=ws_gemm,
+                           stream=stream, flags=0 if first else ov)
                 first = False
 
-    def gemm_small():
-        first = True
-        for l in range(LAYERS):
-            for name, _, _, _ in FUSED:
-                w4.f16_gemm(xs128[SRC[name]], scratch[l][name], y=ys128[name], stream=stream,
-                            flags=0 if first else ov)
-                first = False
+    def gemm_at(M):
+        def run():
+            first = True
+            for l in range(LAYERS):
+                for name, _, _, _ in FUSED:
+                    # After the first GEMM every scratch is long complete: fetch the
+                    # weights early and wait for the previous GEMM only for x and y.
+                    w4.f16_gemm(xp[SRC[name]][:M], scratch[l][name], y=yp[name][:M], stream=stream,
+                                flags=0 if first else ov)
+                    first = False
+        return run
 
     def lm_only():
         qw, s, b, N, K = model.lm
-        w4.lm_head_argmax_topk(xs1["lm"], qw, s, b, k=TOPK, idx=idx1, val=val1, workspace=ws1, stream=stream,
+        w4.lm_head_argmax_topk(xs[1]["lm"], qw, s, b, k=TOPK, idx=idx1, val=val1, workspace=ws1, stream=stream,
                                flags=ov)
 
     def gate_up_only():
         for l in range(LAYERS):
             qw, s, b, N, K = model.layers[l]["gate_up"]
-            w4.w4_gemv(xs1["mlp"], qw, s, b, y=ys_gu, stream=stream, flags=ov)
+            w4.w4_gemv(xs[1]["mlp"], qw, s, b, y=ys_gu, stream=stream, flags=ov)
 
-    def decode(xs, ys, M, k, idx, val, ws):
-        for l in range(LAYERS):
-            for name, _, _, _ in FUSED:
-                qw, s, b, N, K = model.layers[l][name]
-                w4.w4_gemv(xs[SRC[name]], qw, s, b, y=ys[name], stream=stream, flags=ov)
-        qw, s, b, N, K = model.lm
-        w4.lm_head_argmax_topk(xs["lm"], qw, s, b, k=k, idx=idx, val=val, workspace=ws, stream=stream,
-                               flags=ov)
+    def batched(M):
+        def run():
+            for l in range(LAYERS):
+                for name, _, _, _ in FUSED:
+                    qw, s, b, N, K = model.layers[l][name]
+                    w4.w4_gemv(xs[M][SRC[name]], qw, s, b, y=ys[M][name], stream=stream, flags=ov)
+            qw, s, b, N, K = model.lm
+            idx, val, ws = sel_b[M]
+            w4.lm_head_argmax_topk(xs[M]["lm"], qw, s, b, k=1, idx=idx, val=val, workspace=ws, stream=stream,
+                                   flags=ov)
+        return run
 
     def dequant_all():
         for l in range(LAYERS):
@@ -311,30 +401,30 @@ def run_ours(args, rank, world):
                 # distinct weights into distinct scratch buffers: independent calls
                 w4.w4_dequant_f16(qw, s, b, w16=scratch[l][name], stream=stream, flags=ov)
 
-    def gemm_all():
-        first = True
-        for l in range(LAYERS):
-            for name, _, _, _ in FUSED:
-                # After the first GEMM every scratch is long complete: fetch the
-                # weights early and wait for the previous GEMM only for x and y.
-                w4.f16_gemm(xp[SRC[name]], scratch[l][name], y=yp[name], stream=stream, flags=0 if first else ov)
-                first = False
-
     parts = {
         "dequant": dequant_all,
-        "gemm": gemm_all,
+        "gemm": gemm_at(PREFILL_M),
+        "gemm_m512": gemm_at(512),
+        "gemm_m4096": gemm_at(4096),
         "decode_m1": decode_seq,
-        "decode_m16": lambda: decode(xs16, ys16, BATCH_M, 1, idx16, val16, ws16),
+        **{f"decode_m{M}": batched(M) for M in BATCH_MS},
         "lm_head_m1": lm_only,
         "gate_up_m1": gate_up_only,
         "decode_m1_s128": decode_seq_s128,
+        "decode06_m1": decode06,
+        "single_warm": single_warm,
+        "single_rot": single_rot,
+        "sel5_rot": sel_rot,
         "w4gemm_m128": w4gemm_small,
-        "gemm_m128": gemm_small,
+        "gemm_m128": gemm_at(SMALL_M),
     }
     nb = LAYERS * len(FUSED)
     n_seq = (nb + 95) // 96
-    launches = {"dequant": nb, "gemm": nb, "decode_m1": n_seq + 2, "decode_m16": nb + 2, "lm_head_m1": 2,
-                "gate_up_m1": LAYERS, "decode_m1_s128": n_seq + 2, "w4gemm_m128": nb, "gemm_m128": nb}
+    n_seq06 = (L06 * len(FUSED06) + 95) // 96
+    launches = {"dequant": nb, "gemm": nb, "gemm_m512": nb, "gemm_m4096": nb, "decode_m1": n_seq + 2,
+                **{f"decode_m{M}": nb + 2 for M in BATCH_MS}, "lm_head_m1": 2, "gate_up_m1": LAYERS,
+                "decode_m1_s128": n_seq + 2, "decode06_m1": n_seq06 + 2, "single_warm": WARM_REPS,
+                "single_rot": ROT_COPIES, "sel5_rot": 2 * ROT_COPIES, "w4gemm_m128": nb, "gemm_m128": nb}
     # eager warm-up (sets kernel attributes), then capture one graph per part
     with torch.cuda.stream(stream):
         for f in parts.values():
@@ -350,8 +440,7 @@ def run_ours(args, rank, world):
     if w4.device_status() != 0:
         raise RuntimeError("device-side wait expired during warm-up")
 
-    order = ["dequant", "gemm", "decode_m1", "decode_m16", "lm_head_m1", "gate_up_m1", "decode_m1_s128",
-             "w4gemm_m128", "gemm_m128"]
+    order = list(parts)
     ev = {n: [] for n in order}
 
     def step(record):
@@ -390,34 +479,44 @@ def run_ours(args, rank, world):
     part_mean = {n: sum(a.elapsed_time(b) for a, b in ev[n]) / args.steps for n in order}
     total_ms = max_over_ranks(total_ms, world)
 
-    # ---- e2e through the public API with host buffers (decode token) ----
-    host_x = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in xs1.items()}
-    for k, v in xs1.items():
+    # ---- e2e: the decode token through the public API with host buffers ----
+    # Every step: pinned host activations copied in, the projection list and
+    # the lm_head call issued through the binding (C ABI), the top-50 copied
+    # out, and the stream synchronised; timed on the host clock.
+    host_x = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in xs[1].items()}
+    for k, v in xs[1].items():
         host_x[k].copy_(v.cpu())
     host_idx = torch.empty((1, TOPK), dtype=torch.int32, pin_memory=True)
     host_val = torch.empty((1, TOPK), dtype=torch.float32, pin_memory=True)
     h2d = sum(v.numel() * v.element_size() for v in host_x.values())
     d2h = host_idx.numel() * 4 + host_val.numel() * 4
-    e2e_times = []
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup + args.steps):
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            for k, v in host_x.items():
-                xs1[k].copy_(v, non_blocking=True)
-            graphs["decode_m1"].replay()
-            host_idx.copy_(idx1, non_blocking=True)
-            host_val.copy_(val1, non_blocking=True)
-            stream.synchronize()
-            if i >= args.warmup:
-                e2e_times.append(time.perf_counter() - t0)
-    e2e_s = max_over_ranks(statistics.median(e2e_times), world)
 
-    dec_ms = max_over_ranks(part_ms["decode_m1"], world)
+    def e2e_loop(issue):
+        times = []
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + args.steps):
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                for k, v in host_x.items():
+                    xs[1][k].copy_(v, non_blocking=True)
+                issue()
+                host_idx.copy_(idx1, non_blocking=True)
+                host_val.copy_(val1, non_blocking=True)
+                stream.synchronize()
+                if i >= args.warmup:
+                    times.append(time.perf_counter() - t0)
+        return max_over_ranks(statistics.median(times), world)
+
+    e2e_s = e2e_loop(decode_seq)                          # API calls every step
+    e2e_graph_s = e2e_loop(graphs["decode_m1"].replay)    # the same work replayed as a CUDA graph
+    if w4.device_status() != 0:
+        raise RuntimeError("device-side wait expired in the end-to-end runs")
+
+    part_ms = {n: max_over_ranks(v, world) for n, v in part_ms.items()}
     res = {
-        "total_ms": total_ms, "part_ms": part_ms, "part_mean_ms": part_mean, "decode_ms": dec_ms,
-        "e2e_s": e2e_s, "h2d": h2d, "d2h": d2h, "clocks": clk, "setup_s": model.setup_s,
-        "launches_per_step": sum(launches.values()), "launches": launches,
+        "total_ms": total_ms, "part_ms": part_ms, "part_mean_ms": part_mean, "decode_ms": part_ms["decode_m1"],
+        "e2e_s": e2e_s, "e2e_graph_s": e2e_graph_s, "h2d": h2d, "d2h": d2h, "clocks": clk,
+        "setup_s": model.setup_s, "launches_per_step": sum(launches.values()), "launches": launches,
     }
     return res
 
@@ -476,16 +575,33 @@ def profile_case(which, iters=3):
 
     import int4_weight_only_affine_gb300 as w4
     dev = torch.device("cuda:0")
-    if which in ("gemv", "dequant"):
+    if which in ("gemv", "gemv16", "dequant"):
         K, N = 2048, 22016   # gate and up projections stored as one matrix
         qw, s, b = synth.make_linear(1, N, K)
         a = [torch.from_numpy(t).to(dev) for t in (qw.view(np.int32), s, b)]
-        x = torch.from_numpy(synth.make_x(2, 1, K)).to(dev)
+        x = torch.from_numpy(synth.make_x(2, 16 if which == "gemv16" else 1, K)).to(dev)
         for _ in range(iters):
-            if which == "gemv":
-                w4.w4_gemv(x, *a)
-            else:
+            if which == "dequant":
                 w4.w4_dequant_f16(*a)
+            else:
+                w4.w4_gemv(x, *a)
+    elif which == "gemm_all":
+        # f16_gemm at M = 1570 over the 144 Qwen2.5-3B blocks, once (after a
+        # warm-up pass): the launches whose DRAM traffic the bench reports.
+        seeds = {name: p for p, (name, _, _) in enumerate(PROJ)}
+        rows = {name: n for name, _, n in PROJ}
+        xp = {K: torch.randn((PREFILL_M, K), device=dev).half() for K in (2048, 11008)}
+        blocks = []
+        for l in range(LAYERS):
+            for name, K, N, parts in FUSED:
+                mats = [synth.make_linear(synth.layer_seed(1000, l, seeds[q]), rows[q], K) for q in parts]
+                qw, s, b = (torch.from_numpy(np.ascontiguousarray(np.concatenate([m[i] for m in mats]))).to(dev)
+                            for i in range(3))
+                blocks.append((w4.w4_dequant_f16(qw.view(torch.int32), s, b), K, N))
+        y = torch.empty((PREFILL_M, 2 * 11008), dtype=torch.float16, device=dev)
+        for _ in range(2):
+            for w16, K, N in blocks:
+                w4.f16_gemm(xp[K], w16, y=y.view(-1)[:PREFILL_M * N].view(PREFILL_M, N))
     elif which == "lmhead":
         qw, s, b = synth.make_linear(1, LM_N, LM_K)
         a = [torch.from_numpy(t).to(dev) for t in (qw.view(np.int32), s, b)]
@@ -535,7 +651,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--profile", default=None, choices=["gemv", "gemm", "dequant", "lmhead", "seq", "w4gemm"])
+    ap.add_argument("--profile", default=None,
+                    choices=["gemv", "gemv16", "gemm", "gemm_all", "dequant", "lmhead", "seq", "w4gemm"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -567,10 +684,10 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic",
-                "config": {"workload": "qwen2.5-3b decode projections, M=1 (bounded sample per step)",
-                           "seq_len": 1, "global_batch": 1, "parallelism": "cpu"},
+                "config": {**CONFIG, "parallelism": "cpu"},
                 "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                                 "sample": sample},
+                                 "sample": sample + " (bounded per step; the headline quantity: int4 weight bytes "
+                                                    "of the 3B decode projections per second)"},
                 "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -581,18 +698,85 @@ def main():
     r = run_ours(args, rank, world)
     if rank != 0:
         return
-    dec_s = r["decode_ms"] / 1e3
-    decode_gbs = DECODE_BYTES / dec_s / 1e9
+    print(json.dumps(report(args, r, world, peaks, peak_src, hbm, tflops)))
+
+
+def gemm_traffic():
+    """DRAM bytes per f16_gemm launch at M = 1570 (average over the 144 blocks)
+    from the committed ncu summary, if it was taken on the current gemm.cu
+    (None otherwise: the counters would describe another kernel)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "gemm_f16_m1570_all_blocks.md")
+    src = os.path.join(ROOT, "int4_weight_only_affine_gb300", "csrc", "gemm.cu")
+    if not os.path.exists(path):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.startswith("- "):
+            k, v = line[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("gemm.cu sha256/16") != sha:
+        return None
+    try:
+        return float(vals["DRAM bytes per launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def report(args, r, world, peaks, peak_src, hbm, tflops):
     pm = r["part_ms"]
+    spec_hbm, spec_tf = SPEC_PEAKS["hbm_gbs"], SPEC_PEAKS["fp16_dense_tflops"]
+
+    def gbs(nbytes, ms):
+        return nbytes / (ms / 1e3) / 1e9
+
+    def hbm_part(nbytes, ms, **extra):
+        v = gbs(nbytes, ms)
+        return {"ms": ms, "GB_s": v, "frac_hbm": v / hbm, "frac_hbm_spec": v / spec_hbm, **extra}
+
+    def gemm_part(M, ms, **extra):
+        tf = 2.0 * M * PROJ_WEIGHTS / (ms / 1e3) / 1e12
+        return {"ms": ms, "M": M, "TFLOP_s": tf, "frac_tensor": tf / tflops, "frac_tensor_spec": tf / spec_tf,
+                **extra}
+
+    decode_gbs = gbs(DECODE_BYTES, pm["decode_m1"])
     gemm_tflops = PREFILL_FLOPS / (pm["gemm"] / 1e3) / 1e12
-    dq_gbs = DEQUANT_BYTES / (pm["dequant"] / 1e3) / 1e9
-    m16_gbs = DECODE_BYTES / (pm["decode_m16"] / 1e3) / 1e9
-    lm_gbs = weight_bytes(LM_N, LM_K) / (pm["lm_head_m1"] / 1e3) / 1e9
-    gu_gbs = LAYERS * weight_bytes(2 * 11008, 2048) / (pm["gate_up_m1"] / 1e3) / 1e9
-    s128_gbs = DECODE_BYTES_SYM128 / (pm["decode_m1_s128"] / 1e3) / 1e9
-    fused_tf = SMALL_FLOPS / (pm["w4gemm_m128"] / 1e3) / 1e12
-    two_ms = pm["dequant"] + pm["gemm_m128"]
+    lm_gbs = gbs(weight_bytes(LM_N, LM_K), pm["lm_head_m1"])
     proj_bytes = LAYERS * sum(weight_bytes(N, K) for _, K, N in PROJ)
+    two_ms = pm["dequant"] + pm["gemm_m128"]
+    parts = {
+        "single_gemv_896_m1_warm": hbm_part(SINGLE_BYTES, pm["single_warm"] / WARM_REPS,
+                                            note=f"{WARM_REPS} launches on one L2-resident weight; ms per launch"),
+        "single_gemv_896_m1_rotated": hbm_part(SINGLE_BYTES, pm["single_rot"] / ROT_COPIES,
+                                               note=f"{ROT_COPIES} distinct weights (271 MB); ms per launch"),
+        "topk5_1000x896_m1_rotated": hbm_part(SEL_BYTES, pm["sel5_rot"] / ROT_COPIES,
+                                              note=f"lm_head_argmax_topk k=5 over {ROT_COPIES} distinct weights; "
+                                                   "ms per call"),
+        "decode06_m1": hbm_part(DECODE06_BYTES, pm["decode06_m1"], tok_s=1e3 / pm["decode06_m1"],
+                                note="Qwen3-0.6B token: 112 dependent GEMVs (28 x 4 blocks) + lm_head argmax"),
+        "decode_m1": hbm_part(DECODE_BYTES, pm["decode_m1"], tok_s=1e3 / pm["decode_m1"]),
+        **{f"decode_m{M}": hbm_part(DECODE_BYTES, pm[f"decode_m{M}"], tok_s=M * 1e3 / pm[f"decode_m{M}"],
+                                    gemv_tflop_s=2.0 * M * (PROJ_WEIGHTS + LM_N * LM_K) / (pm[f"decode_m{M}"] / 1e3)
+                                    / 1e12) for M in BATCH_MS},
+        "dequant": hbm_part(DEQUANT_BYTES, pm["dequant"]),
+        "gemm_m128": gemm_part(128, pm["gemm_m128"]),
+        "gemm_m512": gemm_part(512, pm["gemm_m512"]),
+        "gemm_m1570": gemm_part(PREFILL_M, pm["gemm"]),
+        "gemm_m4096": gemm_part(4096, pm["gemm_m4096"]),
+        "lm_head_m1_top50": hbm_part(weight_bytes(LM_N, LM_K), pm["lm_head_m1"]),
+        "gemv_gate_up_m1_x36": hbm_part(LAYERS * weight_bytes(2 * 11008, 2048), pm["gate_up_m1"]),
+        "decode_m1_sym128": hbm_part(DECODE_BYTES_SYM128, pm["decode_m1_s128"], tok_s=1e3 / pm["decode_m1_s128"],
+                                     format="symmetric int4, group 128 (scale only), same shapes"),
+        "prefill_m128_w4gemm": gemm_part(SMALL_M, pm["w4gemm_m128"],
+                                         weight_GB_s=gbs(proj_bytes, pm["w4gemm_m128"])),
+        "prefill_m128_dequant_then_gemm": {"ms": two_ms, "TFLOP_s": SMALL_FLOPS / (two_ms / 1e3) / 1e12,
+                                           "gemm_ms": pm["gemm_m128"]},
+    }
+    for M in PREFILL_MS:   # dequant-once + GEMM, the prefill as the pages describe it
+        key = "gemm" if M == PREFILL_M else f"gemm_m{M}"
+        t = pm["dequant"] + pm[key]
+        parts[f"prefill_m{M}_dequant_then_gemm"] = {"ms": t, "TFLOP_s": 2.0 * M * PROJ_WEIGHTS / (t / 1e3) / 1e12}
     line = {
         "metric": METRIC,
         "value": decode_gbs * world,
@@ -606,49 +790,36 @@ def main():
         "vs_baseline": None,
         "dtype": "f16",
         "data": "synthetic",
-        "config": {"workload": "qwen2.5-3b: prefill M=1570 (dequant-once + f16 GEMM), decode M=1 "
-                               "(36 layers x [qkv, o, gate_up, down] GEMVs as one dependent projection list "
-                               "+ lm_head top-50), batched decode M=16 (+ per-row argmax); q/k/v and gate/up "
-                               "stored as fused row blocks; also the decode token in the symmetric group-128 "
-                               "format and M=128 prefill through w4_gemm (parts)",
-                   "model": "Qwen2.5-3B-shaped projections x36 + lm_head 2048->151936",
-                   "global_batch": 1, "seq_len": PREFILL_M, "parallelism": f"replicas{world}",
-                   "l2": "inputs larger than L2 (1.74 GB of weights per decode pass, 5.5 GB scratch)"},
-        "parts": {
-            "decode_m1": {"ms": pm["decode_m1"], "GB_s": decode_gbs, "tok_s": 1e3 / pm["decode_m1"],
-                          "frac_hbm": decode_gbs / hbm},
-            "decode_m16": {"ms": pm["decode_m16"], "GB_s": m16_gbs,
-                           "tok_s": BATCH_M * 1e3 / pm["decode_m16"], "frac_hbm": m16_gbs / hbm},
-            "dequant": {"ms": pm["dequant"], "GB_s": dq_gbs, "frac_hbm": dq_gbs / hbm},
-            "gemm_m1570": {"ms": pm["gemm"], "TFLOP_s": gemm_tflops, "frac_tensor": gemm_tflops / tflops},
-            "lm_head_m1_top50": {"ms": pm["lm_head_m1"], "GB_s": lm_gbs, "frac_hbm": lm_gbs / hbm},
-            "gemv_gate_up_m1_x36": {"ms": pm["gate_up_m1"], "GB_s": gu_gbs, "frac_hbm": gu_gbs / hbm},
-            "decode_m1_sym128": {"ms": pm["decode_m1_s128"], "GB_s": s128_gbs, "tok_s": 1e3 / pm["decode_m1_s128"],
-                                 "frac_hbm": s128_gbs / hbm,
-                                 "format": "symmetric int4, group 128 (scale only), same shapes"},
-            "prefill_m128_w4gemm": {"ms": pm["w4gemm_m128"], "TFLOP_s": fused_tf, "frac_tensor": fused_tf / tflops,
-                                    "weight_GB_s": proj_bytes / (pm["w4gemm_m128"] / 1e3) / 1e9},
-            "prefill_m128_dequant_then_gemm": {"ms": two_ms, "TFLOP_s": SMALL_FLOPS / (two_ms / 1e3) / 1e12,
-                                               "gemm_ms": pm["gemm_m128"]},
-        },
-        "roofline": {"bound": "tensor", "kernel": "f16_gemm (tcgen05)", "achieved": gemm_tflops,
-                     "peak": tflops, "unit": "TFLOP/s", "frac": gemm_tflops / tflops, "traffic": None,
-                     "peak_source": f"{peak_src} bf16 dense (fp16 dense taken equal)"},
-        "roofline_decode": {"bound": "hbm", "kernel": "w4_gemv_seq + lm_head (decode token, dependent chain)",
+        "config": {**CONFIG, "parallelism": f"replicas{world}"},
+        "parts": parts,
+        "roofline": {"bound": "tensor", "kernel": "f16_gemm (tcgen05), M = 1570, average over the 144 blocks",
+                     "achieved": gemm_tflops, "peak": tflops, "unit": "TFLOP/s", "frac": gemm_tflops / tflops,
+                     "traffic": gemm_traffic(), "frac_spec": gemm_tflops / spec_tf, "peak_spec": spec_tf,
+                     "frac_sustained": gemm_tflops / (peak_value(peaks, "bf16_tflops_sustained") or tflops),
+                     "peak_source": f"{peak_src} bf16 dense burst (fp16 dense taken equal); spec: {SPEC_SOURCE}"},
+        "roofline_decode": {"bound": "hbm", "kernel": "w4_gemv_seq + lm_head (3B decode token, dependent chain)",
                             "achieved": decode_gbs, "peak": hbm, "unit": "GB/s", "frac": decode_gbs / hbm,
-                            "traffic": None, "peak_source": f"{peak_src} HBM copy"},
+                            "traffic": None, "frac_spec": decode_gbs / spec_hbm, "peak_spec": spec_hbm,
+                            "peak_source": f"{peak_src} HBM copy; spec: {SPEC_SOURCE}"},
         "roofline_gemv": {"bound": "hbm", "kernel": "lm_head GEMV 2048->151936 + top-50 (largest decode GEMV)",
                           "achieved": lm_gbs, "peak": hbm, "unit": "GB/s", "frac": lm_gbs / hbm,
-                          "traffic": None, "peak_source": f"{peak_src} HBM copy"},
+                          "traffic": None, "frac_spec": lm_gbs / spec_hbm, "peak_spec": spec_hbm,
+                          "peak_source": f"{peak_src} HBM copy; spec: {SPEC_SOURCE}"},
         "e2e": {"value": DECODE_BYTES / r["e2e_s"] / 1e9 * world, "unit": "GB/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-                "note": "decode token through the Python binding: H2D activations, graph replay, D2H top-50"},
+                "ms_per_token": 1e3 * r["e2e_s"],
+                "note": "3B decode token through the public API every step (GemvList.run = w4_gemv_seq, "
+                        "lm_head_argmax_topk): pinned H2D activations, D2H top-50, stream synchronised"},
+        "e2e_graph": {"value": DECODE_BYTES / r["e2e_graph_s"] / 1e9 * world, "unit": "GB/s",
+                      "ms_per_token": 1e3 * r["e2e_graph_s"],
+                      "note": "the same token with the kernels replayed as a CUDA graph"},
         "gpu_launches": r["launches_per_step"] * args.steps,
         "clocks": r["clocks"],
+        "setup_s": r["setup_s"],
     }
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline()
-    print(json.dumps(line))
+    return line
 
 
 if __name__ == "__main__":

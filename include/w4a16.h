@@ -200,12 +200,16 @@ W4A16_API int lm_head_argmax_topk_ex(const uint16_t *x, const uint32_t *qweight,
  *   until the process exits.  This call allocates nothing (no cudaMalloc, no
  *   library allocator).
  *   Set-up: the first call on a device looks up the array's device address on
- *   that device (cudaGetSymbolAddress); make that first call before any stream
- *   capture on that device.
+ *   that device (cudaGetSymbolAddress) and caches it with the id of the CUDA
+ *   context it belongs to; the first call in a new context (e.g. after
+ *   cudaDeviceReset) looks it up again.  Make the first call on a device, and
+ *   in each new context, before any stream capture on it.
  *   Sharing: all calls use the same array and it keeps the last call's
  *   contents.  Nothing in it has to start at zero: pass 1 writes every slot
- *   pass 2 reads.  Calls whose kernels overlap on the GPU (other streams,
- *   other host threads) race on the array: order them on one stream.
+ *   pass 2 reads, so a smaller call after a larger one never sees the
+ *   larger call's leftovers.  Calls whose kernels overlap on the GPU (other
+ *   streams, other host threads) race on the array: order them on one
+ *   stream.
  * Errors: as lm_head_argmax_topk; W4_ERR_WORKSPACE if a size would need more
  * than the built-in 2 MiB; W4_ERR_DEVICE if the address lookup fails.
  */

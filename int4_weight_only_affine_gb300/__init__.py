@@ -18,8 +18,9 @@ import os
 
 import torch
 
-__all__ = ["OVERLAP_PREVIOUS", "w4_gemv", "w4_gemv_seq", "seq_workspace", "seq_workspace_bytes", "GemvOp", "lm_head_argmax_topk", "lm_head_workspace_bytes", "w4_dequant_f16",
-           "f16_gemm", "w4_gemm", "w4_gemm_workspace", "w4_gemm_workspace_bytes", "device_status", "W4A16Error", "LIB_PATH", "lib"]
+__all__ = ["OVERLAP_PREVIOUS", "w4_gemv", "w4_gemv_seq", "GemvList", "seq_workspace", "seq_workspace_bytes", "GemvOp",
+           "lm_head_argmax_topk", "lm_head_workspace_bytes", "w4_dequant_f16", "f16_gemm", "w4_gemm",
+           "w4_gemm_workspace", "w4_gemm_workspace_bytes", "device_status", "W4A16Error", "LIB_PATH", "lib"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libw4a16.so")
@@ -167,22 +168,46 @@ def seq_workspace(ops, group: int = 64) -> torch.Tensor:
     return torch.zeros(seq_workspace_bytes(ops, group), dtype=torch.uint8, device=ops[0][0].device)
 
 
+class GemvList:
+    """A projection list checked and marshalled once, for calling w4_gemv_seq
+    every decode step: run() only hands the prepared operation array to the
+    library, which in turn reuses its launch plan for an unchanged list.  The
+    tensors of `ops` (see w4_gemv_seq) are kept referenced by this object."""
+
+    def __init__(self, ops, group: int = 64):
+        self.ops = list(ops)
+        self.arr, self.M = _seq_array(self.ops, group)
+        self.ptr = ctypes.cast(self.arr, ctypes.c_void_p)
+        self.nops = len(self.ops)
+
+    def workspace_bytes(self) -> int:
+        return int(lib.w4_gemv_seq_workspace_bytes_ex(self.ptr, self.nops, self.M))
+
+    def workspace(self) -> torch.Tensor:
+        """A zero-filled workspace for this list (reuse it for every call)."""
+        return torch.zeros(self.workspace_bytes(), dtype=torch.uint8, device=self.ops[0][0].device)
+
+    def run(self, workspace: torch.Tensor, stream=None):
+        _check("w4_gemv_seq", lib.w4_gemv_seq(self.ptr, self.nops, self.M,
+                                              _dev(workspace, "workspace", (torch.uint8,)), workspace.numel(),
+                                              0, _stream(stream)))
+        return [op[4] for op in self.ops]
+
+
 def w4_gemv_seq(ops, workspace: torch.Tensor | None = None, group: int = 64, stream=None):
     """Run a list of GEMVs in one persistent launch.
 
-    ops: sequence of (x, qweight, scales, biases, y, wait_prev[, group]) with
-    torch tensors (biases None: symmetric codes); wait_prev = True when x is
-    written by an earlier operation of the list; group defaults to `group`.  All x share the same number of rows M.  workspace: from
-    seq_workspace(ops) (zero-filled before its first use, then passed
-    unchanged to every call); a fresh one is made when None.  Returns the
-    list of y."""
-    arr, M = _seq_array(ops, group)
+    ops: a GemvList, or a sequence of (x, qweight, scales, biases, y,
+    wait_prev[, group]) with torch tensors (biases None: symmetric codes);
+    wait_prev = True when x is written by an earlier operation of the list;
+    group defaults to `group`.  All x share the same number of rows M.
+    workspace: from seq_workspace(ops) (zero-filled before its first use,
+    then passed unchanged to every call); a fresh one is made when None.
+    Returns the list of y."""
+    gl = ops if isinstance(ops, GemvList) else GemvList(ops, group)
     if workspace is None:
-        workspace = seq_workspace(ops, group)
-    _check("w4_gemv_seq", lib.w4_gemv_seq(ctypes.cast(arr, ctypes.c_void_p), len(ops), M,
-                                          _dev(workspace, "workspace", (torch.uint8,)), workspace.numel(),
-                                          0, _stream(stream)))
-    return [op[4] for op in ops]
+        workspace = gl.workspace()
+    return gl.run(workspace, stream)
 
 
 def lm_head_workspace_bytes(M: int, N: int, k: int) -> int:

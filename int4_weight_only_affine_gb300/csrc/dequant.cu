@@ -285,6 +285,17 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 }  // namespace
+
+// Reads and clears this translation unit's expired-wait record.
+int dequant_wait_flag() {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_wait_expired, sizeof(int)) != cudaSuccess) return -1;
+    if (v) {
+        const int zero = 0;
+        cudaMemcpyToSymbol(g_wait_expired, &zero, sizeof(int));
+    }
+    return v;
+}
 }  // namespace w4a16
 
 using namespace w4a16;

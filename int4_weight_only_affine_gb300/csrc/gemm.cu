@@ -1203,7 +1203,8 @@ extern "C" int w4_gemm_ex(const uint16_t *x, const uint32_t *qweight, const uint
 }
 
 namespace w4a16 {
-int gemv_wait_flag();  // gemv.cu
+int gemv_wait_flag();     // gemv.cu
+int dequant_wait_flag();  // dequant.cu
 
 // Reads and clears this translation unit's expired-wait record.
 static int gemm_wait_flag() {
@@ -1219,9 +1220,9 @@ static int gemm_wait_flag() {
 
 extern "C" int w4a16_device_status(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return W4_ERR_LAUNCH;
-    const int a = gemm_wait_flag(), b = gemv_wait_flag();
-    if (a < 0 || b < 0) return W4_ERR_LAUNCH;
-    return (a || b) ? W4_ERR_TIMEOUT : W4A16_OK;
+    const int a = gemm_wait_flag(), b = gemv_wait_flag(), c = dequant_wait_flag();
+    if (a < 0 || b < 0 || c < 0) return W4_ERR_LAUNCH;
+    return (a || b || c) ? W4_ERR_TIMEOUT : W4A16_OK;
 }
 
 extern "C" const char *w4a16_status_string(int status) {

@@ -36,9 +36,11 @@
 #include <cooperative_groups.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "gemv_tile.cuh"
+#include "../../include/w4a16_testing.h"
 
 namespace cg = cooperative_groups;
 
@@ -528,6 +530,8 @@ struct SeqParams {
     CUtensorMap maps[kSeqMaxOps];  // 3-D code maps, one per operation
     SeqOp ops[kSeqMaxOps];
     unsigned *ws;                  // [0] (operation, CTA) completions, [1] launch epoch, [2] CTAs finished
+    unsigned long long wait_ns;    // limit of a completion-counter wait
+    unsigned target_bump;          // added to every counter target (0; nonzero only under the test hook)
     int nops, M, stages;
     int publish;                   // 1: some operation waits on the completion counter
     uint32_t stage_bytes, w_bytes;
@@ -655,11 +659,11 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
             const int ntl = t1 - t0;
             if (o.wait_prev && op > 0 && !o.xt && tid == 0) {
                 // Every CTA has published operations 0..op-1.
-                const unsigned target = (unsigned)op * (unsigned)G;
+                const unsigned target = (unsigned)op * (unsigned)G + P.target_bump;
                 const uint64_t t_start = global_ns();
                 while (ld_acquire_u32(P.ws) < target) {
                     if (*abort_flag) break;
-                    if (global_ns() - t_start > kWaitNs) {
+                    if (global_ns() - t_start > P.wait_ns) {
                         atomicExch(&g_wait_expired, 1);
                         *abort_flag = 1;
                         break;
@@ -1340,13 +1344,48 @@ const void *seq_kernel_ptr(int M) {
            : M <= 8 ? (const void *)seq_kernel<1, false, FMT> : (const void *)seq_kernel<2, false, FMT>;
 }
 
-int seq_launch(const w4_gemv_op *ops, int nops, int M, unsigned *ws, uint8_t *tagbuf, size_t tag_bytes,
-               cudaStream_t st) {
-    static SeqParams P;  // large: kept off the stack (calls are host-serialised per process)
+// Counter-wait settings of later launches (w4a16_testing_set_seq_wait).
+std::atomic<unsigned long long> g_seq_wait_ns{kWaitNs};
+std::atomic<unsigned> g_seq_target_bump{0u};
+
+// Launch plans (tensor maps, tagged-exchange layout, shared-memory layout) of
+// recent operation lists, so that a decode loop that passes the same list
+// every token pays for planning and tensor-map encoding once.  An entry is
+// reused only for an identical list (every field of every operation), the
+// same rows M, workspace and device.
+struct SeqPlan {
+    int dev, nops, M;
+    unsigned *ws;
+    uint8_t *tagbuf;
+    size_t tag_bytes;
+    w4_gemv_op ops[kSeqMaxOps];
+    SeqParams P;
+    size_t smem;
+    const void *kern;
+    unsigned long long used;
+};
+constexpr int kSeqPlans = 8;
+
+bool same_list(const SeqPlan &e, const w4_gemv_op *ops, int nops, int M, unsigned *ws, uint8_t *tagbuf,
+               size_t tag_bytes, int dev) {
+    if (e.nops != nops || e.M != M || e.ws != ws || e.tagbuf != tagbuf || e.tag_bytes != tag_bytes || e.dev != dev)
+        return false;
+    for (int i = 0; i < nops; ++i) {
+        const w4_gemv_op &a = e.ops[i], &b = ops[i];
+        if (a.x != b.x || a.qweight != b.qweight || a.scales != b.scales || a.biases != b.biases || a.y != b.y ||
+            a.N != b.N || a.K != b.K || a.wait_prev != b.wait_prev || a.group != b.group)
+            return false;
+    }
+    return true;
+}
+
+// Fills e.P, e.smem and e.kern for the list; a status other than W4A16_OK
+// leaves the entry unusable.
+int build_seq_plan(SeqPlan &e, const w4_gemv_op *ops, int nops, int M, unsigned *ws, uint8_t *tagbuf,
+                   size_t tag_bytes) {
     static int src[kSeqMaxOps];
     static bool tagged[kSeqMaxOps];
-    static std::mutex mu;
-    std::lock_guard<std::mutex> lock(mu);
+    SeqParams &P = e.P;
     const int G = sm_count();
     // Tagged exchange when the workspace has room for it, else the counter.
     const bool use_tags = tagbuf && seq_sources(ops, nops, M, src, tagged) <= tag_bytes;
@@ -1393,16 +1432,50 @@ int seq_launch(const w4_gemv_op *ops, int nops, int M, unsigned *ws, uint8_t *ta
     P.publish = 0;
     for (int i = 1; i < nops; ++i)
         if (P.ops[i].wait_prev && !P.ops[i].xt) P.publish = 1;
-    size_t smem = 0;
-    if (!plan_seq(P, smem, ng_max, sc_max, xs_max, ntl_max)) return W4_ERR_SHAPE;
+    if (!plan_seq(P, e.smem, ng_max, sc_max, xs_max, ntl_max)) return W4_ERR_SHAPE;
     const int fmt = fmt_class(P.ops[0].f);  // the same for every operation of a launch
-    const void *kern = fmt == kFmtG64    ? seq_kernel_ptr<kFmtG64>(M)
-                       : fmt == kFmtS128 ? seq_kernel_ptr<kFmtS128>(M)
-                       : fmt == kFmtG32  ? seq_kernel_ptr<kFmtG32>(M)
-                                         : seq_kernel_ptr<kFmtAny>(M);
+    e.kern = fmt == kFmtG64    ? seq_kernel_ptr<kFmtG64>(M)
+             : fmt == kFmtS128 ? seq_kernel_ptr<kFmtS128>(M)
+             : fmt == kFmtG32  ? seq_kernel_ptr<kFmtG32>(M)
+                               : seq_kernel_ptr<kFmtAny>(M);
+    return W4A16_OK;
+}
+
+int seq_launch(const w4_gemv_op *ops, int nops, int M, unsigned *ws, uint8_t *tagbuf, size_t tag_bytes,
+               cudaStream_t st) {
+    static SeqPlan plans[kSeqPlans];  // large: kept off the stack
+    static unsigned long long clock = 0;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return W4_ERR_DEVICE;
+    SeqPlan *e = nullptr;
+    for (int i = 0; i < kSeqPlans && !e; ++i)
+        if (plans[i].nops > 0 && same_list(plans[i], ops, nops, M, ws, tagbuf, tag_bytes, dev)) e = &plans[i];
+    if (!e) {
+        e = &plans[0];  // least recently used (or empty) entry
+        for (int i = 1; i < kSeqPlans; ++i)
+            if (plans[i].used < e->used) e = &plans[i];
+        e->nops = 0;
+        const int bs = build_seq_plan(*e, ops, nops, M, ws, tagbuf, tag_bytes);
+        if (bs != W4A16_OK) return bs;
+        e->dev = dev;
+        e->nops = nops;
+        e->M = M;
+        e->ws = ws;
+        e->tagbuf = tagbuf;
+        e->tag_bytes = tag_bytes;
+        for (int i = 0; i < nops; ++i) e->ops[i] = ops[i];
+    }
+    e->used = ++clock;
+    SeqParams &P = e->P;
+    P.wait_ns = g_seq_wait_ns.load();
+    P.target_bump = g_seq_target_bump.load();
+    const size_t smem = e->smem;
+    const void *kern = e->kern;
     if (!ensure_smem(kern, smem)) return W4_ERR_LAUNCH;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(G, 1, 1);
+    cfg.gridDim = dim3(sm_count(), 1, 1);
     cfg.blockDim = dim3(kSeqThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -1412,8 +1485,8 @@ int seq_launch(const w4_gemv_op *ops, int nops, int M, unsigned *ws, uint8_t *ta
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     void *args[] = {&P};
-    const cudaError_t e = cudaLaunchKernelExC(&cfg, kern, args);
-    if (e != cudaSuccess) {
+    const cudaError_t err = cudaLaunchKernelExC(&cfg, kern, args);
+    if (err != cudaSuccess) {
         cudaGetLastError();
         return W4_ERR_LAUNCH;
     }
@@ -1487,6 +1560,13 @@ static int seq_launch_ops(const w4_gemv_op *ops, int nops) {
 
 extern "C" size_t w4_gemv_seq_workspace_bytes(void) { return kSeqCounterBytes; }
 
+extern "C" int w4a16_testing_set_seq_wait(unsigned long long wait_ns, unsigned target_bump) {
+    if (wait_ns > kWaitNs) return W4_ERR_SHAPE;
+    g_seq_wait_ns.store(wait_ns ? wait_ns : kWaitNs);
+    g_seq_target_bump.store(target_bump);
+    return W4A16_OK;
+}
+
 extern "C" size_t w4_gemv_seq_workspace_bytes_ex(const w4_gemv_op *ops, int nops, int M) {
     if (!ops || nops < 1 || M < 1 || M > 16) return kSeqCounterBytes;
     static std::mutex mu;
@@ -1546,18 +1626,55 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = (size_t)16 * kMaxCandidates * sizeof(uint64_t);
 static __device__ __align__(256) uint64_t g_lm_scratch[kNoAllocScratchBytes / sizeof(uint64_t)];
 
-// Device address of g_lm_scratch for the current device.  The host-side name
-// is only a stand-in; the address is looked up once per device and cached.
+// Unique id of the current CUDA context (cuCtxGetId: never reused within a
+// process), or 0 if the driver does not provide it.
+unsigned long long current_context_id() {
+    typedef CUresult (*GetCurrentFn)(CUcontext *);
+    typedef CUresult (*GetIdFn)(CUcontext, unsigned long long *);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_lm_scratch in the current device's context.  The
+// host-side name is only a stand-in; the address is looked up with the device
+// current and cached per device together with the id of the context it
+// belongs to, so a new primary context (after cudaDeviceReset) gets a fresh
+// lookup.  Without context ids the address is looked up on every call.
 void *noalloc_scratch() {
     static std::mutex mu;
     static void *addr[64] = {nullptr};
+    static unsigned long long ctx_of[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    if (!addr[dev] || ctx == 0 || ctx_of[dev] != ctx) {
+        // (The lookup also makes the device's primary context current.)
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_lm_scratch) != cudaSuccess) return nullptr;
+        if (cudaGetSymbolAddress(&p, g_lm_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            addr[dev] = nullptr;
+            return nullptr;
+        }
         addr[dev] = p;
+        ctx_of[dev] = ctx ? ctx : current_context_id();
     }
     return addr[dev];
 }

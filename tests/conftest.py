@@ -21,3 +21,17 @@ def golden_lines(name):
             line = line.strip()
             if line and not line.startswith("#"):
                 yield line
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Top-k positions excluded from exact index parity (oracle near-ties),
+    per test, when GPU top-k tests ran."""
+    mod = sys.modules.get("_gpu")
+    rows = getattr(mod, "EXCLUSIONS", None) if mod else None
+    if not rows:
+        return
+    tr = terminalreporter
+    tr.section("top-k positions excluded as oracle near-ties (excluded / checked)")
+    for nodeid, excluded, positions in rows:
+        tr.write_line(f"{excluded:5d} / {positions:5d}  {nodeid}")
+    tr.write_line(f"{sum(r[1] for r in rows):5d} / {sum(r[2] for r in rows):5d}  total")

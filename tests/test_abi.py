@@ -9,12 +9,16 @@ import pytest
 from conftest import ROOT
 
 HEADER = os.path.join(ROOT, "include", "w4a16.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+                 if f.endswith(".h"))
 LIB = os.path.join(ROOT, "int4_weight_only_affine_gb300", "libw4a16.so")
 
 
 def _declared():
-    text = open(HEADER).read()
-    return re.findall(r"W4A16_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+    names = []
+    for h in HEADERS:
+        names += re.findall(r"W4A16_API\s+[\w\s\*]+?\b(\w+)\s*\(", open(h).read())
+    return names
 
 
 def _status_codes():
@@ -36,7 +40,7 @@ def test_header_declares_the_hot_path_calls():
             "lm_head_argmax_topk", "lm_head_argmax_topk_ex", "lm_head_argmax_topk_noalloc",
             "lm_head_workspace_bytes", "w4_dequant_f16", "w4_dequant_f16_ex", "f16_gemm", "f16_gemm_ex",
             "w4_gemm", "w4_gemm_ex", "w4_gemm_workspace_bytes", "w4a16_status_string",
-            "w4a16_device_status"} <= names
+            "w4a16_device_status", "w4a16_testing_set_seq_wait"} <= names
 
 
 def test_library_exports_every_declared_symbol(lib):

@@ -12,7 +12,7 @@ import pytest
 
 import oracle
 import synth
-from _gpu import require_gpu, to_dev, topk_check, within_tol
+from _gpu import note_exclusions, require_gpu, to_dev, topk_check, within_tol
 
 pytestmark = pytest.mark.gpu
 
@@ -92,9 +92,21 @@ def test_gemv_symmetric_closed_form(w4):
 
 # ------------------------------------------------------------------ token selection
 
+# The oracle's own count of near-tie positions for these seeded inputs
+# (independent of the GPU): the bound each case asserts.
+TOPK_MAX_EXCLUDED = {
+    (32, False, 1, 5): 4, (32, False, 3, 50): 140, (32, False, 16, 1): 2,
+    (128, False, 1, 5): 2, (128, False, 3, 50): 137, (128, False, 16, 1): 0,
+    (256, False, 3, 50): 131, (256, False, 16, 1): 0,
+    (32, True, 1, 5): 4, (32, True, 3, 50): 136, (32, True, 16, 1): 2,
+    (64, True, 1, 5): 3, (64, True, 3, 50): 135, (64, True, 16, 1): 1,
+    (128, True, 1, 5): 3, (128, True, 3, 50): 131, (128, True, 16, 1): 2,
+}
+
+
 @pytest.mark.parametrize("group,sym", FORMATS)
 @pytest.mark.parametrize("M,N,K,k", [(1, 1000, 896, 5), (3, 3000, 512, 50), (16, 257, 256, 1)])
-def test_topk_formats(w4, group, sym, M, N, K, k):
+def test_topk_formats(w4, request, group, sym, M, N, K, k):
     if K % group:
         pytest.skip("group does not divide K")
     import torch
@@ -103,20 +115,27 @@ def test_topk_formats(w4, group, sym, M, N, K, k):
     ws = torch.randint(0, 255, (w4.lm_head_workspace_bytes(M, N, k),), dtype=torch.uint8, device="cuda")
     idx, val = w4.lm_head_argmax_topk(to_dev(x), to_dev(qw), to_dev(s), _dv(b), k=k, workspace=ws, group=group)
     idx, val = idx.cpu().numpy(), val.cpu().numpy()
+    excluded = 0
     for m in range(M):
         lg, ad = oracle.gemv(x[m:m + 1], qw, s, b, N, K, group=group, threads=16)
-        topk_check(idx[m], val[m], lg[0], ad[0], k)
+        excluded += topk_check(idx[m], val[m], lg[0], ad[0], k)
+    note_exclusions(request, excluded, M * k)
+    assert excluded <= TOPK_MAX_EXCLUDED[(group, sym, M, k)]
 
 
-def test_topk_lm_head_symmetric_group128_full_size(w4):
-    """The 151,936 x 2048 LM head in the symmetric group-128 format, top-50."""
+def test_topk_lm_head_symmetric_group128_full_size(w4, request):
+    """The 151,936 x 2048 LM head in the symmetric group-128 format, top-50
+    on random weights (49 of the 50 ranks are oracle near-ties; the planted
+    full-vocabulary tests check every rank of this format exactly)."""
     N, K, k = 151936, 2048, 50
     qw, s, b = synth.make_linear_sym(7300, N, K, 128)
     x = synth.make_x(7301, 1, K)
     idx, val = w4.lm_head_argmax_topk(to_dev(x), to_dev(qw), to_dev(s), None, k=k, group=128)
     idx, val = idx.cpu().numpy(), val.cpu().numpy()
     lg, ad = oracle.gemv(x, qw, s, None, N, K, group=128, threads=16)
-    topk_check(idx[0], val[0], lg[0], ad[0], k)
+    excluded = topk_check(idx[0], val[0], lg[0], ad[0], k)
+    note_exclusions(request, excluded, k)
+    assert excluded <= 49
 
 
 # ------------------------------------------------------------------ projection list
