@@ -271,9 +271,10 @@ W4A16_API int w4_dequant_f16_ex(const uint32_t *qweight, const uint16_t *scales,
  *              concurrently need separate workspaces.
  *              Small N splits K over several blocks whose fp32 partial sums
  *              it holds.
- *   With a single K split (large N) the result equals f16_gemm on the
- *   w4_dequant_f16 scratch bit for bit; with several, the partial sums are
- *   added in split order (deterministic).
+ *   The products are those of f16_gemm on the w4_dequant_f16 scratch (the
+ *   same binary16 weight values); the 64-k steps of a tile are accumulated
+ *   in fp32 starting from a per-tile rotation, and with several K splits
+ *   the partial sums are added in split order.  Results are deterministic.
  * Errors: W4_ERR_NULL, W4_ERR_SHAPE, W4_ERR_GROUP, W4_ERR_ALIGN,
  * W4_ERR_WORKSPACE, W4_ERR_DEVICE, W4_ERR_LAUNCH.
  */

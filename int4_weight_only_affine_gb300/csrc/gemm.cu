@@ -535,54 +535,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // of being dequantised into a half scratch (2 B written + 2 B read per
 // weight) and then multiplied.
 //
-//  * Tiles of 128 weight rows (output columns) x all M <= 128 activation rows
-//    (one 128-row MMA tile, rows past M zero-filled by the copies).  Small-N
-//    shapes split K over several CTAs (units = tiles x splits).
-//  * Two rings.  Codes: 3 stages of 16 KB (128 rows x 256 k: four 64-k steps
-//    in one tensor copy of 128-byte rows, 128-byte swizzle), deep enough to
-//    cover HBM latency.  Operands: 5 stages of the X tile (K-major, 128-byte
-//    swizzle, from L2) and the converted weights of one 64-k step.
+// The MMA runs transposed: A = a 128-row weight tile (the MMA's M), held in
+// tensor memory; B = the activation tile X (its N = M rounded up to 16,
+// K-major in shared memory); D[n][m] = sum_k w[n][k] x[m][k] accumulates in
+// tensor memory with one weight row per lane.
+//  * Tiles of 128 weight rows.  Small-N shapes split K over several CTAs
+//    (units = tiles x splits).  A unit walks its 64-k steps from a rotation
+//    that differs between tiles, so that CTAs working at the same time read
+//    different X tiles from L2.
+//  * Codes: a ring of 6 stages of 16 KB (128 rows x 256 k: four 64-k steps
+//    per tensor copy, 128-byte rows, 128-byte swizzle).  X and converted
+//    weights: a ring of 6 stages, each an X tile (128 rows x 64 k, K-major,
+//    128-byte swizzle, from L2) and 32 tensor-memory columns (64 k of
+//    binary16 per lane), released together by one MMA commit.
 //  * Warp 0: one thread issues the code copies (weights are constants: no
 //    dependency wait).  Warp 14: one thread issues the X copies (after the
 //    dependency wait when launched as a programmatic dependent).
-//  * Warps 6-13: converters, two teams of four warps taking alternate code
-//    stages (a code slot is released after the proxy fence that also
-//    publishes the converted weights of its last step).  Lane l of team warp
-//    v turns rows 2p, 2p+1 (p = 32 (v % 2) + l) and k half v / 2 of each
-//    64-k step into binary16 pairs (w[n][k], w[n+1][k])
-//    -- exactly the w4_dequant_f16 value, RNE(scale*q + bias) -- and writes
-//    them in the layout the f16_gemm B operand has after its tensor copies
-//    (two 64 k x 64 n boxes, N-major, 128-byte swizzle).  Each store
-//    instruction of a warp fills one 128-byte k row: no bank conflicts.
-//    Scales and biases are loaded one team code stage (eight steps) ahead.
-//  * Warp 1: one thread issues tcgen05.mma.kind::f16 (M = 128, N = 128,
-//    K = 16), four per stage, and commits each operand stage back.
-//  * Warps 2-5: epilogue.  One split: round and store y.  Several: write
-//    the fp32 partial tile to the workspace; the CTA that completes a tile
-//    (arrival counter) sums the partials in split order and stores y, and
-//    resets the counter for the next call.
-// With one split the arithmetic is that of f16_gemm on the w4_dequant_f16
-// scratch (same operand values and layout, same MMA sequence).
+//  * Warps 6-13: converters, two teams of four warps taking alternate 64-k
+//    steps; warp w converts the rows of its tensor-memory lane quarter
+//    (w % 4): lane l takes row 32 (w % 4) + l, reads its 64 codes of the
+//    step (two 16-byte loads, conflict-free under the swizzle) and writes
+//    the 32 binary16 pairs (w[n][k], w[n][k+1]) -- exactly the
+//    w4_dequant_f16 value, RNE(scale*q + bias) -- with one tensor-memory
+//    store.  Scales and biases are loaded one code stage ahead.
+//  * Warp 1: one thread issues tcgen05.mma.kind::f16 with A from tensor
+//    memory (M = 128, N = M rounded up to 16, K = 16), four per step, and
+//    commits each stage back.
+//  * Warps 2-5: epilogue (lane quarter w % 4).  One split: round and store
+//    y.  Several: write the fp32 partial tile to the workspace; the CTA that
+//    completes a tile (arrival counter) sums the partials in split order and
+//    stores y, and resets the counter for the next call.
+// The binary16 operands are those of f16_gemm on the w4_dequant_f16 scratch;
+// only the order of the 64-k steps in the fp32 accumulation differs.
 // ---------------------------------------------------------------------------
 constexpr int FBN = 128;                              // weight rows per tile
-constexpr int XST = 5;                                // operand stages (>= CK + 1: see the converters)
-constexpr int CST = 3;                                // code stages
-constexpr int CK = 4;                                 // 64-k steps per code stage
-static_assert(XST >= CK + 1, "operand-stage waits rely on XST >= CK + 1");
-constexpr int FA_TILE = BM * BK * 2;                  // 16 KB: X, 128 rows x 64 k
-constexpr int FB_TILE = BK * FBN * 2;                 // 16 KB: converted weights
-constexpr int FXW = FA_TILE + FB_TILE;                // 32 KB operand stage
-constexpr int FC_TILE = FBN * 128;                    // 16 KB code stage: 128 rows x 32 words
-constexpr int F_TEAM_WARPS = 4;                       // converter warps per stage
-constexpr int F_CONV_WARP0 = 6;
-constexpr int F_XPROD_WARP = F_CONV_WARP0 + 2 * F_TEAM_WARPS;  // 14
-constexpr int F_THREADS = (F_XPROD_WARP + 1) * 32;    // 480
-constexpr int F_TMEM_COLS = 2 * FBN;
-constexpr int F_BARS = 2 * CST + 3 * XST + 5;
-constexpr size_t F_SMEM = 1024 + (size_t)XST * FXW + (size_t)CST * FC_TILE + 8 * F_BARS + 16;
+constexpr int QST = 6;                                // X and converted-weight stages
+constexpr int QCST = 6;                               // code stages
+constexpr int QCK = 4;                                // 64-k steps per code stage
+constexpr int QFX = BM * BK * 2;                      // 16 KB: X, 128 rows x 64 k
+constexpr int QFC = FBN * 128;                        // 16 KB code stage: 128 rows x 32 words
+constexpr int Q_TEAM = 4;                             // converter warps per team (one per lane quarter)
+constexpr int Q_CONV0 = 6;
+constexpr int Q_XWARP = Q_CONV0 + 2 * Q_TEAM;         // 14
+constexpr int F_THREADS = (Q_XWARP + 1) * 32;         // 480
+constexpr int Q_ACC_COLS = 128;                       // one accumulator: up to 128 activation rows
+constexpr int Q_A_COL0 = 2 * Q_ACC_COLS;              // converted weights after the two accumulators
+constexpr int F_TMEM_COLS = 512;
+constexpr int F_BARS = 2 * QCST + 3 * QST + 5;
+constexpr size_t F_SMEM = 1024 + (size_t)QST * QFX + (size_t)QCST * QFC + 8 * F_BARS + 16;
 constexpr int kMaxSplit = 8;
-constexpr uint32_t kInstrDescF = (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (1u << 16) |
-                                 ((uint32_t)(FBN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+static_assert(QST >= 2, "converted-weight stage waits rely on at least two stages");
+static_assert(Q_A_COL0 + QST * 32 <= F_TMEM_COLS, "tensor-memory columns");
 
 struct W4GemmArgs {
     const uint16_t *sc, *bi;  // scales, biases (null: symmetric codes)
@@ -593,14 +596,27 @@ struct W4GemmArgs {
     WFmt f;
     int S;                    // K splits per tile
     int pdl;
+    uint32_t idesc;           // instruction descriptor (N = M rounded up to 16)
 };
 
-__device__ __forceinline__ void mma_f16_desc(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                             uint32_t accum) {
+// D[tmem_d] (+)= A[tmem_a] * B[bdesc]: A from tensor memory.
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accum) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum));
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accum));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]),
+        "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
 }
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -656,17 +672,17 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
-    const uint32_t codes0 = base + XST * FXW;               // code ring
-    const uint32_t bar0 = codes0 + CST * FC_TILE;
-    auto code_full = [&](int c) { return bar0 + 8u * c; };             // codes landed
-    auto code_empty = [&](int c) { return bar0 + 8u * (CST + c); };    // codes read by the converters
-    auto xin_bar = [&](int s) { return bar0 + 8u * (2 * CST + s); };   // X tile landed
-    auto conv_bar = [&](int s) { return bar0 + 8u * (2 * CST + XST + s); };   // weights converted
-    auto empty_bar = [&](int s) { return bar0 + 8u * (2 * CST + 2 * XST + s); };  // MMAs done with the stage
-    auto accf_bar = [&](int x) { return bar0 + 8u * (2 * CST + 3 * XST + x); };
-    auto acce_bar = [&](int x) { return bar0 + 8u * (2 * CST + 3 * XST + 2 + x); };
-    const uint32_t done_bar = bar0 + 8u * (2 * CST + 3 * XST + 4);
-    const size_t tail_off = (size_t)XST * FXW + (size_t)CST * FC_TILE + 8 * F_BARS;
+    const uint32_t codes0 = base + QST * QFX;               // code ring
+    const uint32_t bar0 = codes0 + QCST * QFC;
+    auto code_full = [&](int c) { return bar0 + 8u * c; };                   // codes landed
+    auto code_empty = [&](int c) { return bar0 + 8u * (QCST + c); };         // codes read by every converter
+    auto x_full = [&](int s) { return bar0 + 8u * (2 * QCST + s); };         // X tile landed
+    auto a_full = [&](int s) { return bar0 + 8u * (2 * QCST + QST + s); };   // weights converted
+    auto st_empty = [&](int s) { return bar0 + 8u * (2 * QCST + 2 * QST + s); };  // MMAs done with stage s
+    auto accf_bar = [&](int x) { return bar0 + 8u * (2 * QCST + 3 * QST + x); };
+    auto acce_bar = [&](int x) { return bar0 + 8u * (2 * QCST + 3 * QST + 2 + x); };
+    const uint32_t done_bar = bar0 + 8u * (2 * QCST + 3 * QST + 4);
+    const size_t tail_off = (size_t)QST * QFX + (size_t)QCST * QFC + 8 * F_BARS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + tail_off);
     volatile int *last_flag = reinterpret_cast<volatile int *>(gbase + tail_off + 4);
 
@@ -683,16 +699,29 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         kb0 = sp * nk / S;  // S <= 8 and nk < 2^24: no overflow
         kb1 = (sp + 1) * nk / S;
     };
+    // A unit walks its k steps starting at kb0 + rot and wrapping around, rot
+    // a multiple of a code stage that differs between tiles: CTAs working on
+    // different tiles at the same time then read different X tiles, instead
+    // of all of them asking L2 for the same one.
+    auto unit_rot = [&](int u, int kb0, int kb1) {
+        const int ns = kb1 - kb0;
+        return ns % QCK ? 0 : (int)(((unsigned)(u / S) * 5u) % (unsigned)(ns / QCK)) * QCK;
+    };
+    auto seq_kb = [](int kb0, int kb1, int rot, int j) {
+        int v = j + rot;
+        if (v >= kb1 - kb0) v -= kb1 - kb0;
+        return kb0 + v;
+    };
 
     if (threadIdx.x == 0) {
-        for (int c = 0; c < CST; ++c) {
+        for (int c = 0; c < QCST; ++c) {
             mbar_init(code_full(c), 1);
-            mbar_init(code_empty(c), F_TEAM_WARPS);
+            mbar_init(code_empty(c), 2 * Q_TEAM);
         }
-        for (int s = 0; s < XST; ++s) {
-            mbar_init(xin_bar(s), 1);
-            mbar_init(conv_bar(s), F_TEAM_WARPS);
-            mbar_init(empty_bar(s), 1);
+        for (int s = 0; s < QST; ++s) {
+            mbar_init(x_full(s), 1);
+            mbar_init(a_full(s), Q_TEAM);
+            mbar_init(st_empty(s), 1);
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(accf_bar(x), 1);
@@ -724,25 +753,27 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
                 int n0, kb0, kb1;
                 unit_range(u, n0, kb0, kb1);
-                for (int k = kb0; k < kb1; k += CK, ++cs) {
-                    const int c = cs % CST;
-                    const uint32_t ph = (cs / CST) & 1;
+                const int rot = unit_rot(u, kb0, kb1);
+                for (int j = 0; j < kb1 - kb0; j += QCK, ++cs) {
+                    const int c = cs % QCST;
+                    const uint32_t ph = (cs / QCST) & 1;
                     if (!mbar_wait(code_empty(c), ph ^ 1)) {
                         ok = false;
                         break;
                     }
                     // Steps k .. k+3 (words 8k ..); past K the copy fills zeros.
-                    mbar_expect_tx(code_full(c), FC_TILE);
-                    tma_load_2d(codes0 + c * FC_TILE, &tma_q, 8 * k, n0, code_full(c));
+                    const int k = seq_kb(kb0, kb1, rot, j);
+                    mbar_expect_tx(code_full(c), QFC);
+                    tma_load_2d(codes0 + c * QFC, &tma_q, 8 * k, n0, code_full(c));
                     issued_ph = (issued_ph & ~(1u << c)) | (ph << c);
                     issued_any |= 1u << c;
                 }
             }
             // Drain: every copy this thread issued has landed before exit.
-            for (int c = 0; c < CST; ++c)
+            for (int c = 0; c < QCST; ++c)
                 if (issued_any & (1u << c)) mbar_wait(code_full(c), (issued_ph >> c) & 1);
         }
-    } else if (warp == F_XPROD_WARP) {
+    } else if (warp == Q_XWARP) {
         if (lane == 0) {
             // ---------------- X producer ----------------
             if (a.pdl) pdl_wait();  // x may be written by the previous kernel
@@ -752,21 +783,22 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
                 int n0, kb0, kb1;
                 unit_range(u, n0, kb0, kb1);
-                for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                    const int s = it % XST;
-                    const uint32_t ph = (it / XST) & 1;
-                    if (!mbar_wait(empty_bar(s), ph ^ 1)) {
+                const int rot = unit_rot(u, kb0, kb1);
+                for (int j = 0; j < kb1 - kb0; ++j, ++it) {
+                    const int s = it % QST;
+                    const uint32_t ph = (it / QST) & 1;
+                    if (!mbar_wait(st_empty(s), ph ^ 1)) {
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(xin_bar(s), FA_TILE);
-                    tma_load_2d(base + s * FXW, &tma_x, kb * BK, 0, xin_bar(s));
+                    mbar_expect_tx(x_full(s), QFX);
+                    tma_load_2d(base + s * QFX, &tma_x, seq_kb(kb0, kb1, rot, j) * BK, 0, x_full(s));
                     issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
                     issued_any |= 1u << s;
                 }
             }
-            for (int s = 0; s < XST; ++s)
-                if (issued_any & (1u << s)) mbar_wait(xin_bar(s), (issued_ph >> s) & 1);
+            for (int s = 0; s < QST; ++s)
+                if (issued_any & (1u << s)) mbar_wait(x_full(s), (issued_ph >> s) & 1);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -783,24 +815,27 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t dst = tmem + acc * FBN;
-                for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                    const int s = it % XST;
-                    const uint32_t ph = (it / XST) & 1;
-                    if (!mbar_wait(xin_bar(s), ph) || !mbar_wait(conv_bar(s), ph)) {
+                const uint32_t dst = tmem + acc * Q_ACC_COLS;
+                // Stage s: X at base + s * QFX (descriptor address field + s *
+                // QFX / 16), converted weights at tensor-memory column
+                // Q_A_COL0 + 32 s; each 16-k slice is 32 bytes (+2) or 8
+                // columns further.
+                const uint64_t xd0 = smem_desc(base, 16, 1024);
+                for (int j = 0; j < kb1 - kb0; ++j, ++it) {
+                    const int sx = it % QST;
+                    const uint32_t ph = (it / QST) & 1;
+                    if (!mbar_wait(x_full(sx), ph) || !mbar_wait(a_full(sx), ph)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = base + s * FXW;
-                    const uint32_t sb = sa + FA_TILE;
-#pragma unroll
-                    for (int ks = 0; ks < BK / 16; ++ks) {
-                        const uint64_t ad = smem_desc(sa + ks * 32, 16, 1024);
-                        const uint64_t bd = smem_desc(sb + ks * 2048, B_BOX, 1024);
-                        mma_f16_desc(dst, ad, bd, kInstrDescF, (kb != kb0 || ks != 0) ? 1u : 0u);
-                    }
-                    mma_commit(empty_bar(s));
+                    const uint64_t bd = xd0 + (uint64_t)(sx * (QFX >> 4));
+                    const uint32_t ta = tmem + Q_A_COL0 + sx * 32;
+                    mma_f16_tmem_a(dst, ta, bd, a.idesc, j != 0 ? 1u : 0u);
+                    mma_f16_tmem_a(dst, ta + 8, bd + 2, a.idesc, 1u);
+                    mma_f16_tmem_a(dst, ta + 16, bd + 4, a.idesc, 1u);
+                    mma_f16_tmem_a(dst, ta + 24, bd + 6, a.idesc, 1u);
+                    mma_commit(st_empty(sx));
                 }
                 if (!ok) break;
                 mma_commit(accf_bar(acc));
@@ -808,53 +843,42 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             mma_commit(done_bar);
             mbar_wait(done_bar, 0);
         }
-    } else if (warp >= 2 && warp < F_CONV_WARP0) {
+    } else if (warp >= 2 && warp < Q_CONV0) {
         // ---------------- epilogue: warps 2..5 ----------------
-        // After an expired wait a warp skips its work but still takes part in
-        // the named barriers of every unit (no warp is left waiting there).
-        const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31 = activation rows
-        const int row = quad * 32 + lane;
+        // Lane l of warp w holds weight row n0 + 32 (w % 4) + l; columns are
+        // activation rows.  After an expired wait a warp skips its work but
+        // still takes part in the named barriers of every unit.
+        const int quad = warp & 3;
         bool ok = true;
         int tc = 0;
+        const int ncol = (M + 31) / 32;  // 32-column chunks that hold activation rows
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++tc) {
             int n0, kb0, kb1;
             unit_range(u, n0, kb0, kb1);
             const int acc = tc & 1;
             const uint32_t aph = (tc >> 1) & 1;
+            const int n = n0 + quad * 32 + lane;
             if (ok && !mbar_wait(accf_bar(acc), aph)) ok = false;
             if (ok) tc_fence_after();
-            for (int c = 0; c < FBN / 32 && ok; ++c) {
+            for (int c = 0; c < ncol && ok; ++c) {
                 uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + acc * FBN + c * 32, r);
-                if (c == FBN / 32 - 1) {
+                tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + acc * Q_ACC_COLS + c * 32, r);
+                if (c == ncol - 1) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(acce_bar(acc));
                 }
-                if (row >= M) continue;
-                const int nc = n0 + c * 32;
+                if (n >= N) continue;
+                const int m0 = c * 32;
                 if (S == 1) {
-                    uint16_t *dst = a.y + (size_t)row * N + nc;
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        if (nc + 8 * v < N) {
-                            uint4 o;
-                            o.x = pack_half2(r[8 * v + 0], r[8 * v + 1]);
-                            o.y = pack_half2(r[8 * v + 2], r[8 * v + 3]);
-                            o.z = pack_half2(r[8 * v + 4], r[8 * v + 5]);
-                            o.w = pack_half2(r[8 * v + 6], r[8 * v + 7]);
-                            *reinterpret_cast<uint4 *>(dst + 8 * v) = o;
-                        }
-                    }
+                    for (int i = 0; i < 32; ++i)
+                        if (m0 + i < M) a.y[(size_t)(m0 + i) * N + n] = __half_as_ushort(__float2half_rn(__uint_as_float(r[i])));
                 } else {
-                    float *dst = a.part + ((size_t)(u % S) * M + row) * N + nc;
+                    float *dst = a.part + ((size_t)(u % S) * M) * N + n;
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        if (nc + 4 * v < N)
-                            __stcg(reinterpret_cast<float4 *>(dst + 4 * v),
-                                   make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                               __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
-                    }
+                    for (int i = 0; i < 32; ++i)
+                        if (m0 + i < M) __stcg(dst + (size_t)(m0 + i) * N, __uint_as_float(r[i]));
                 }
             }
             if (S > 1) {
@@ -882,132 +906,135 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 epi_sync();  // the flag is read by every epilogue thread before the next unit
             }
         }
-    } else if (warp >= F_CONV_WARP0 && warp < F_XPROD_WARP) {
+    } else if (warp >= Q_CONV0 && warp < Q_XWARP) {
         // ---------------- converters: warps 6..13, two teams ----------------
-        const int cw = warp - F_CONV_WARP0;
-        const int team = cw / F_TEAM_WARPS, v = cw % F_TEAM_WARPS;
-        const int p = 32 * (v & 1) + lane;  // row pair 2p, 2p+1 of the tile
-        const int kh = v >> 1;              // k half of the stage: k 32 kh .. 32 kh + 31
-        const int box = v & 1;              // 64-n box of the pair (n = 2p: 64 box + 2 lane)
-        // Byte offset, within the B tile, of (k = 32 kh + 8 w + e, n = 2p) is
-        //   box*8192 + (4 kh + w)*1024 + e*128 + (((lane/4) ^ e) << 4) + 4 (lane % 4).
-        const uint32_t off0 = (uint32_t)(box * B_BOX + kh * 4096 + 4 * (lane & 3));
-        const int lq = lane >> 2;
+        const int cw = warp - Q_CONV0;
+        const int team = cw / Q_TEAM;
+        const int quad = warp & 3;           // tensor-memory lane quarter of this warp
+        const int rl = quad * 32 + lane;     // the lane's row within the tile
+        const int sw = rl & 7;               // 128-byte swizzle phase of that row
         const bool sym = a.f.sym != 0;
         const __half2 koff = __float2half2_rn(sym ? 1032.f : 1024.f);
         const int ngs = a.f.ngs, gshift = a.f.gs + 5;
+        const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16) + Q_A_COL0;
         // Position of a code stage of this CTA: unit u (rows n0, steps
-        // [kb0, kb1)) and its first step k; advanced one code stage at a time.
+        // [kb0, kb1) walked from rotation rot), the sequence position j of its
+        // first step, and the CTA step index of that step.
         struct CPos {
-            int u, n0, kb0, kb1, k;
+            int u, n0, kb0, kb1, rot, j, it;
         };
         auto cstep = [&](CPos &q) {
-            q.k += CK;
-            if (q.k < q.kb1) return;
+            const int j1 = q.j + QCK;
+            if (j1 < q.kb1 - q.kb0) {
+                q.it += QCK;
+                q.j = j1;
+                return;
+            }
+            q.it += q.kb1 - q.kb0 - q.j;
             q.u += gridDim.x;
             if (q.u < units) {
                 unit_range(q.u, q.n0, q.kb0, q.kb1);
-                q.k = q.kb0;
+                q.rot = unit_rot(q.u, q.kb0, q.kb1);
+                q.j = 0;
             }
         };
-        // Scale and bias pairs (rows 2p, 2p+1) of the steps of the code stage
-        // at q, as half2 bit patterns.
-        auto load_sb = [&](const CPos &q, uint32_t (&s2)[CK], uint32_t (&b2)[CK]) {
-            const int ra = min(q.n0 + 2 * p, N - 1), rb = min(q.n0 + 2 * p + 1, N - 1);
+        // Scales (and biases) of the two 32-k halves of this team's steps of
+        // the code stage at q, as binary16 bit patterns (loaded one code
+        // stage ahead, so that no step waits for them).
+        auto load_sb = [&](const CPos &q, uint32_t (&sv)[QCK], uint32_t (&bv)[QCK]) {
+            const int row = min(q.n0 + rl, N - 1);  // rows past N: any valid scales (results unused)
+            const uint16_t *srow = a.sc + (size_t)row * ngs;
+            const uint16_t *brow = a.bi + (size_t)row * ngs;
 #pragma unroll
-            for (int j = 0; j < CK; ++j) {
-                const int gi = (min(q.k + j, q.kb1 - 1) * BK + 32 * kh) >> gshift;
-                s2[j] = (uint32_t)ld_nc_u16(a.sc + (size_t)ra * ngs + gi) |
-                        ((uint32_t)ld_nc_u16(a.sc + (size_t)rb * ngs + gi) << 16);
-                b2[j] = 0u;
-                if (!sym)
-                    b2[j] = (uint32_t)ld_nc_u16(a.bi + (size_t)ra * ngs + gi) |
-                            ((uint32_t)ld_nc_u16(a.bi + (size_t)rb * ngs + gi) << 16);
+            for (int j = 0; j < QCK; ++j) {
+                sv[j] = bv[j] = 0u;
+                if (q.j + j >= q.kb1 - q.kb0 || ((q.it + j) & 1) != team) continue;
+                const int kb = seq_kb(q.kb0, q.kb1, q.rot, q.j + j);
+                const int g0 = (kb * BK) >> gshift, g1 = (kb * BK + 32) >> gshift;
+                sv[j] = (uint32_t)ld_nc_u16(srow + g0) | ((uint32_t)ld_nc_u16(srow + g1) << 16);
+                if (!sym) bv[j] = (uint32_t)ld_nc_u16(brow + g0) | ((uint32_t)ld_nc_u16(brow + g1) << 16);
             }
         };
-        // The team converts code stages team, team + 2, ...; the scales of its
-        // next stage are loaded when it starts the current one.
         CPos pf;
         pf.u = blockIdx.x;
-        unit_range(pf.u, pf.n0, pf.kb0, pf.kb1);
-        pf.k = pf.kb0;
-        if (team) cstep(pf);
-        uint32_t nxs[CK], nxb[CK];
+        pf.it = 0;
+        if (pf.u < units) {
+            unit_range(pf.u, pf.n0, pf.kb0, pf.kb1);
+            pf.rot = unit_rot(pf.u, pf.kb0, pf.kb1);
+            pf.j = 0;
+        }
+        uint32_t nxs[QCK], nxb[QCK];
         if (pf.u < units) load_sb(pf, nxs, nxb);
         bool ok = true;
-        int cs = 0, itb = 0;  // code stages, and 64-k steps of earlier units
-        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            int n0, kb0, kb1;
-            unit_range(u, n0, kb0, kb1);
-            for (int k = kb0; k < kb1 && ok; k += CK, ++cs) {
-                if ((cs & 1) != team) continue;  // the other team's code stage
-                uint32_t cus[CK], cub[CK];
+        int cs = 0;  // code stages
+        while (pf.u < units && ok) {
+            const CPos cur = pf;
+            uint32_t cus[QCK], cub[QCK];
 #pragma unroll
-                for (int j = 0; j < CK; ++j) {
-                    cus[j] = nxs[j];
-                    cub[j] = nxb[j];
-                }
-                cstep(pf);
-                cstep(pf);
-                if (pf.u < units) load_sb(pf, nxs, nxb);
-                const int c = cs % CST;
-                if (!mbar_wait(code_full(c), (cs / CST) & 1)) {
+            for (int j = 0; j < QCK; ++j) {
+                cus[j] = nxs[j];
+                cub[j] = nxb[j];
+            }
+            cstep(pf);
+            if (pf.u < units) load_sb(pf, nxs, nxb);
+            const int c = cs % QCST;
+            if (!mbar_wait(code_full(c), (cs / QCST) & 1)) {
+                ok = false;
+                break;
+            }
+            const uint32_t crow = codes0 + c * QFC + rl * 128;
+#pragma unroll
+            for (int j = 0; j < QCK; ++j) {
+                const int it = cur.it + j;          // step position of this CTA
+                if (cur.j + j >= cur.kb1 - cur.kb0) break;
+                if ((it & 1) != team) continue;     // the other team's step
+                const uint4 qa = lds128(crow + (((2 * j) ^ sw) << 4));
+                const uint4 qb = lds128(crow + (((2 * j + 1) ^ sw) << 4));
+                const int sa = it % QST;
+                // The stage is free once the MMAs of its previous use (step
+                // it - QST) are done; this team's previous step (it - 2)
+                // waited for step it - 2 - QST, so with QST >= 2 every
+                // earlier phase of the barrier is complete and the parity
+                // cannot alias.
+                if (!mbar_wait(st_empty(sa), ((it / QST) & 1) ^ 1)) {
                     ok = false;
                     break;
                 }
-                const uint8_t *crow_a = gbase + XST * FXW + c * FC_TILE + (2 * p) * 128;
-                const uint8_t *crow_b = crow_a + 128;
-                const int swa = (2 * p) & 7, swb = (2 * p + 1) & 7;  // 128-byte swizzle phases
+                uint32_t out[32];
+                const uint32_t wd[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
-                for (int j = 0; j < CK; ++j) {
-                    if (k + j >= kb1) break;
-                    const int it = itb + (k - kb0) + j;  // operand ring position of this step
-                    const int s = it % XST;
-                    // 16-byte chunk 2j + kh of each row: k 64 (k0 + j) + 32 kh ...
-                    const uint4 A = *reinterpret_cast<const uint4 *>(crow_a + (((2 * j + kh) ^ swa) << 4));
-                    const uint4 B = *reinterpret_cast<const uint4 *>(crow_b + (((2 * j + kh) ^ swb) << 4));
-                    // The operand stage is free once the MMAs of its previous use
-                    // (step it - XST) are done.  The parity cannot alias: this warp's
-                    // previous step is at most CK + 1 steps back (the other team
-                    // converts one code stage of at most CK steps in between) and
-                    // waited for the MMAs XST steps before it, so with XST >= CK + 1
-                    // every earlier phase of this barrier is complete; no later one
-                    // can be (its MMAs need this step's weights).
-                    if (!mbar_wait(empty_bar(s), ((it / XST) & 1) ^ 1)) {
-                        ok = false;
-                        break;
+                for (int i = 0; i < 8; ++i) {
+                    // Scale and bias of the word's 32-k half, in both halves.
+                    const uint32_t sv = i < 4 ? __byte_perm(cus[j], 0, 0x1010) : __byte_perm(cus[j], 0, 0x3232);
+                    const uint32_t bv = i < 4 ? __byte_perm(cub[j], 0, 0x1010) : __byte_perm(cub[j], 0, 0x3232);
+                    const __half2 s2 = *reinterpret_cast<const __half2 *>(&sv);
+                    const __half2 b2 = *reinterpret_cast<const __half2 *>(&bv);
+                    const uint32_t w = wd[i], w4 = w >> 4;
+                    // Codes (2e, 2e + 1) of the word into the two halves:
+                    // bytes e of w and of w >> 4, low nibbles.
+                    const uint32_t p[4] = {__byte_perm(w, w4, 0x5410), __byte_perm(w, w4, 0x6521),
+                                           __byte_perm(w, w4, 0x7632), __byte_perm(w, w4, 0x7733)};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t qv = (p[e] & 0x000F000Fu) | 0x64006400u;  // 1024 + q
+                        const __half2 q2 = __hsub2(*reinterpret_cast<const __half2 *>(&qv), koff);
+                        const __half2 w2 = sym ? __hmul2(q2, s2) : __hfma2(q2, s2, b2);  // one rounding
+                        out[4 * i + e] = *reinterpret_cast<const uint32_t *>(&w2);
                     }
-                    const __half2 s2 = *reinterpret_cast<const __half2 *>(&cus[j]);
-                    const __half2 b2 = *reinterpret_cast<const __half2 *>(&cub[j]);
-                    uint8_t *bt = gbase + s * FXW + FA_TILE + off0;
-                    const uint32_t wa[4] = {A.x, A.y, A.z, A.w}, wb[4] = {B.x, B.y, B.z, B.w};
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        const uint32_t lo = __byte_perm(wa[w], wb[w], 0x5410);  // codes 0..3 of (row a, row b)
-                        const uint32_t hi = __byte_perm(wa[w], wb[w], 0x7632);  // codes 4..7
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const uint32_t src = e < 4 ? lo : hi;
-                            const uint32_t q4 = ((src >> (4 * (e & 3))) & 0x000F000Fu) | 0x64006400u;  // 1024 + q
-                            const __half2 q2 = __hsub2(*reinterpret_cast<const __half2 *>(&q4), koff);
-                            const __half2 w2 = sym ? __hmul2(q2, s2) : __hfma2(q2, s2, b2);  // one rounding
-                            *reinterpret_cast<uint32_t *>(bt + w * 1024 + e * 128 + ((lq ^ e) << 4)) =
-                                *reinterpret_cast<const uint32_t *>(&w2);
-                        }
-                    }
-                    // Generic accesses before any async-proxy access of the same
-                    // bytes: the tensor cores read the converted weights, and the
-                    // code slot is released after the last step's fence, so the
-                    // next tensor copy into it cannot overtake the code reads.
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(conv_bar(s));
                 }
-                if (!ok) break;
+                tmem_st32(trow + sa * 32, out);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(code_empty(c));
+                if (lane == 0) mbar_arrive(a_full(sa));
             }
-            itb += kb1 - kb0;
+            if (!ok) break;
+            // Every converter warp reads every code stage (its own steps);
+            // its reads are ordered before the next tensor copy into the slot.
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(code_empty(c));
+            ++cs;
         }
     }
 
@@ -1167,6 +1194,10 @@ int w4gemm_impl(const uint16_t *x, const uint32_t *qweight, const uint16_t *scal
     a.f = f;
     a.S = w4gemm_splits(M, N, K, sms);
     a.pdl = (flags & W4A16_OVERLAP_PREVIOUS) ? 1 : 0;
+    // kind::f16, fp32 accumulate, A (weights, tensor memory) and B (X) binary16
+    // and K-major, N = M rounded up to 16, M = 128 weight rows.
+    const uint32_t nmma = (uint32_t)((M + 15) / 16 * 16);
+    a.idesc = (1u << 4) | ((nmma >> 3) << 17) | ((uint32_t)(FBN >> 4) << 24);
     const int units = ((N + FBN - 1) / FBN) * a.S;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(units < sms ? units : sms), 1, 1);

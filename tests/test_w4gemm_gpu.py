@@ -69,7 +69,10 @@ def test_w4gemm_formats(w4, group, sym):
 @pytest.mark.parametrize("group,sym", [(64, False), (128, True)])
 def test_w4gemm_single_split_equals_dequant_then_gemm(w4, M, group, sym):
     """At M >= 64, N = 22016 (172 tiles for 152 SMs) runs as one K split: the
-    fused result equals f16_gemm on the w4_dequant_f16 scratch bit for bit."""
+    fused GEMM multiplies exactly the w4_dequant_f16 weight values, and only
+    the order in which it adds its 64-k steps differs from f16_gemm on that
+    scratch (a rotation per tile), so every output is within one binary16
+    unit in the last place of f16_gemm's."""
     import torch
     N, K = 22016, 2048
     qw, s, b = _linear(8300 + M, N, K, group, sym)
@@ -78,7 +81,10 @@ def test_w4gemm_single_split_equals_dequant_then_gemm(w4, M, group, sym):
     y = w4.w4_gemm(x, *args, group=group)
     w16 = w4.w4_dequant_f16(*args, group=group)
     y2 = w4.f16_gemm(x, w16)
-    assert torch.equal(y, y2)
+    ulps = (y.view(torch.int16).int() - y2.view(torch.int16).int()).abs()
+    same_sign = (y.view(torch.int16) < 0) == (y2.view(torch.int16) < 0)
+    close = (same_sign & (ulps <= 1)) | ((y.float() - y2.float()).abs() <= 1e-4)
+    assert bool(close.all()), f"{int((~close).sum())} outputs differ by more than one unit in the last place"
 
 
 FULL = sorted({(K, N) for _, K, N in synth.QWEN25_3B} | {(2048, 2560), (2048, 22016)})
