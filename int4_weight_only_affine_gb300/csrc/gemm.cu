@@ -91,6 +91,20 @@ __device__ __forceinline__ uint32_t pack_half2(uint32_t a, uint32_t b) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// The B tile of a stage: 64 k rows x BN columns of W16 as BN / 64 boxes of
+// 64 x 64 (128-byte swizzle), box j at sb + j * B_BOX.  With b3d the tensor
+// map views W16 as [N / 64][K][64] and one copy brings all BN / 64 boxes
+// (each k row's 512 bytes contiguous in memory: fewer, longer DRAM bursts).
+__device__ __forceinline__ void load_b_tile(uint32_t sb, const CUtensorMap *map, int n0, int k0, uint32_t bar,
+                                            int b3d) {
+    if (b3d) {
+        tma_load_3d(sb, map, 0, k0, n0 / 64, bar);
+    } else {
+#pragma unroll
+        for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * B_BOX, map, n0 + 64 * j, k0, bar);
+    }
+}
+
 // pdl: launched as a programmatic dependent.  The kernel releases the next
 // one at once, sets up and copies the weight (B) tiles of its first stages
 // before waiting for the previous kernel; the activation (A) copies, and so
@@ -98,7 +112,7 @@ __device__ __forceinline__ uint32_t pack_half2(uint32_t a, uint32_t b) {
 // come after the wait.
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-                uint16_t *__restrict__ y, int M, int N, int K, int pdl) {
+                uint16_t *__restrict__ y, int M, int N, int K, int pdl, int b3d) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms.
     const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
@@ -156,9 +170,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int kb = 0; kb < pre; ++kb) {  // fresh slots: no empty wait
                     mbar_expect_tx(full_bar(kb), STAGE_BYTES);
                     const uint32_t sb = base + kb * STAGE_BYTES + A_TILE;
-#pragma unroll
-                    for (int j = 0; j < BN / 64; ++j)
-                        tma_load_2d(sb + j * B_BOX, &tma_b, n0 + 64 * j, kb * BK, full_bar(kb));
+                    load_b_tile(sb, &tma_b, n0, kb * BK, full_bar(kb), b3d);
                     issued_any |= 1u << kb;
                 }
                 pdl_wait();
@@ -180,8 +192,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t sa = base + s * STAGE_BYTES;
                     const uint32_t sb = sa + A_TILE;
                     tma_load_2d(sa, &tma_a, kb * BK, m0, full_bar(s));
-#pragma unroll
-                    for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * B_BOX, &tma_b, n0 + 64 * j, kb * BK, full_bar(s));
+                    load_b_tile(sb, &tma_b, n0, kb * BK, full_bar(s), b3d);
                     issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
                     issued_any |= 1u << s;
                 }
@@ -316,6 +327,27 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                                 uint32_t leader_bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3, %4}], [%5];" ::"r"(dst),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(leader_bar)
+        : "memory");
+}
+
+// This CTA's 128 columns of a pair's B tile (two 64 x 64 boxes; with b3d one
+// copy of the [N / 64][K][64] view, as load_b_tile).
+__device__ __forceinline__ void load_b_half_pair(uint32_t sb, const CUtensorMap *map, int n0, int k0,
+                                                 uint32_t leader_bar, int b3d) {
+    if (b3d) {
+        tma_load_3d_pair(sb, map, 0, k0, n0 / 64, leader_bar);
+    } else {
+        tma_load_2d_pair(sb, map, n0, k0, leader_bar);
+        tma_load_2d_pair(sb + B_BOX, map, n0 + 64, k0, leader_bar);
+    }
+}
+
 __device__ __forceinline__ void mma_f16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
@@ -341,7 +373,7 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
 // first stages before the dependency wait and its A halves after it).
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm2_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-                 uint16_t *__restrict__ y, int M, int N, int K, int pdl) {
+                 uint16_t *__restrict__ y, int M, int N, int K, int pdl, int b3d) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -404,8 +436,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (rank == 0) mbar_expect_tx(full_bar(kb), 2 * STAGE2_BYTES);
                     const uint32_t lbar = map_to_rank(full_bar(kb), 0);
                     const uint32_t sb = base + kb * STAGE2_BYTES + A2_TILE;
-                    tma_load_2d_pair(sb, &tma_b, n0, kb * BK, lbar);
-                    tma_load_2d_pair(sb + B_BOX, &tma_b, n0 + 64, kb * BK, lbar);
+                    load_b_half_pair(sb, &tma_b, n0, kb * BK, lbar, b3d);
                     issued_any |= 1u << kb;
                 }
                 pdl_wait();
@@ -430,8 +461,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t sa = base + s * STAGE2_BYTES;
                     const uint32_t sb = sa + A2_TILE;
                     tma_load_2d_pair(sa, &tma_a, kb * BK, m0, lbar);
-                    tma_load_2d_pair(sb, &tma_b, n0, kb * BK, lbar);
-                    tma_load_2d_pair(sb + B_BOX, &tma_b, n0 + 64, kb * BK, lbar);
+                    load_b_half_pair(sb, &tma_b, n0, kb * BK, lbar, b3d);
                     issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
                     issued_any |= 1u << s;
                 }
@@ -1068,6 +1098,16 @@ static int gemm_impl(const uint16_t *x16, const uint16_t *w16, uint16_t *y, int 
     if (!make_map(&tb, w16, (uint64_t)N, (uint64_t)K, 64, BK)) return W4_ERR_DEVICE;
     // The pair kernel loads 128-row A boxes (one per CTA) and the same B boxes.
     CUtensorMap ta2 = ta, tb2 = tb;
+    // For N a multiple of 64, W16 is also viewed as [N / 64][K][64] so that
+    // one copy brings a tile's boxes (BN / 64 of them; two per CTA of a pair).
+    const int b3d = (N % 64 == 0) ? 1 : 0;
+    if (b3d) {
+        if (!make_map_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, w16, 64, (uint64_t)K, (uint64_t)N / 64, (uint64_t)N * 2,
+                         128, 64, BK, BN / 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map_3d(&tb2, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, w16, 64, (uint64_t)K, (uint64_t)N / 64,
+                         (uint64_t)N * 2, 128, 64, BK, 2, CU_TENSOR_MAP_SWIZZLE_128B))
+            return W4_ERR_DEVICE;
+    }
     if (!set_smem_once(reinterpret_cast<const void *>(gemm_kernel), (int)SMEM_BYTES)) return W4_ERR_LAUNCH;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (M > BM) {
@@ -1091,7 +1131,7 @@ static int gemm_impl(const uint16_t *x16, const uint16_t *w16, uint16_t *y, int 
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = pdl ? 2 : 1;
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm2_kernel, ta2, tb2, y, M, N, K, pdl);
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm2_kernel, ta2, tb2, y, M, N, K, pdl, b3d);
         return e == cudaSuccess ? W4A16_OK : W4_ERR_LAUNCH;
     }
     const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
@@ -1108,7 +1148,7 @@ static int gemm_impl(const uint16_t *x16, const uint16_t *w16, uint16_t *y, int 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel, ta, tb, y, M, N, K, pdl);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_kernel, ta, tb, y, M, N, K, pdl, b3d);
     return e == cudaSuccess ? W4A16_OK : W4_ERR_LAUNCH;
 }
 
