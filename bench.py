@@ -349,6 +349,20 @@ def run_ours(args, rank, world):
     seq06 = seq_barriers(model.layers06, FUSED06, xs06, ys06)
     seq06_ws = seq06.workspace()
 
+    # Batched decode at M = 2 and 4 as projection lists too (the activations
+    # of the 11008-wide down projection fit in shared memory up to M = 4).
+    seq_b = {M: seq_barriers(model.layers, FUSED, xs[M], ys[M]) for M in (2, 4)}
+    seq_b_ws = {M: seq_b[M].workspace() for M in (2, 4)}
+
+    def batched_list(M):
+        def run():
+            seq_b[M].run(seq_b_ws[M], stream)
+            qw, s, b, N, K = model.lm
+            idx, val, ws = sel_b[M]
+            w4.lm_head_argmax_topk(xs[M]["lm"], qw, s, b, k=1, idx=idx, val=val, workspace=ws, stream=stream,
+                                   flags=ov)
+        return run
+
     def decode_seq():
         seq3b.run(seq3b_ws, stream)
         qw, s, b, N, K = model.lm
@@ -445,6 +459,7 @@ def run_ours(args, rank, world):
         "decode_m1": decode_seq,
         "decode_m1_chain": decode_seq_chain,
         **{f"decode_m{M}": batched(M) for M in BATCH_MS},
+        **{f"decode_m{M}_list": batched_list(M) for M in (2, 4)},
         "lm_head_m1": lm_only,
         "gate_up_m1": gate_up_only,
         "decode_m1_s128": decode_seq_s128,
@@ -459,7 +474,8 @@ def run_ours(args, rank, world):
     n_seq = (nb + 95) // 96
     n_seq06 = (L06 * len(FUSED06) + 95) // 96
     launches = {"dequant": nb, "gemm": nb, "gemm_m512": nb, "gemm_m4096": nb, "decode_m1": n_seq + 2,
-                **{f"decode_m{M}": nb + 2 for M in BATCH_MS}, "lm_head_m1": 2, "gate_up_m1": LAYERS,
+                **{f"decode_m{M}": nb + 2 for M in BATCH_MS},
+                **{f"decode_m{M}_list": n_seq + 2 for M in (2, 4)}, "lm_head_m1": 2, "gate_up_m1": LAYERS,
                 "decode_m1_s128": n_seq + 2, "decode_m1_chain": n_seq + 2, "decode06_m1": n_seq06 + 2, "single_warm": WARM_REPS,
                 "single_rot": ROT_COPIES, "sel5_rot": 2 * ROT_COPIES, "w4gemm_m128": nb, "gemm_m128": nb}
     # eager warm-up (sets kernel attributes), then capture one graph per part
@@ -633,9 +649,10 @@ def profile_case(which, iters=3):
         for l in range(LAYERS):
             for name, K, N, parts in FUSED:
                 mats = [synth.make_linear(synth.layer_seed(1000, l, seeds[q]), rows[q], K) for q in parts]
-                qw, s, b = (torch.from_numpy(np.ascontiguousarray(np.concatenate([m[i] for m in mats]))).to(dev)
-                            for i in range(3))
-                blocks.append((w4.w4_dequant_f16(qw.view(torch.int32), s, b), K, N))
+                qw = np.concatenate([m[0] for m in mats]).view(np.int32)
+                s, b = (np.concatenate([m[i] for m in mats]) for i in (1, 2))
+                blocks.append((w4.w4_dequant_f16(*[torch.from_numpy(np.ascontiguousarray(a)).to(dev) for a in (qw, s, b)]),
+                               K, N))
         y = torch.empty((PREFILL_M, 2 * 11008), dtype=torch.float16, device=dev)
         for _ in range(2):
             for w16, K, N in blocks:
@@ -663,8 +680,8 @@ def profile_case(which, iters=3):
         for _ in range(iters):
             w4.w4_gemv_seq(ops, workspace=ws)
     elif which == "w4gemm":
-        # the fused int4 GEMM at M = 64 on the q|k|v block (2048 -> 2560)
-        K, N, M = 2048, 2560, 64
+        # the fused int4 GEMM at M = 128 on the gate|up block (2048 -> 22016)
+        K, N, M = 2048, 22016, 128
         qw, s, b = synth.make_linear(1, N, K)
         a = [torch.from_numpy(t).to(dev) for t in (qw.view(np.int32), s, b)]
         x = torch.from_numpy(synth.make_x(2, M, K)).to(dev)
@@ -739,22 +756,27 @@ def main():
     print(json.dumps(report(args, r, world, peaks, peak_src, hbm, tflops)))
 
 
+def f16_gemm_source_hash():
+    """sha256/16 of the f16_gemm kernels' source: gemm.cu up to its w4_gemm section."""
+    import hashlib
+    src = open(os.path.join(ROOT, "int4_weight_only_affine_gb300", "csrc", "gemm.cu")).read()
+    cut = src.find("// w4_gemm: the int4 GEMM")
+    return hashlib.sha256(src[:cut if cut >= 0 else len(src)].encode()).hexdigest()[:16]
+
+
 def gemm_traffic():
     """DRAM bytes per f16_gemm launch at M = 1570 (average over the 144 blocks)
-    from the committed ncu summary, if it was taken on the current gemm.cu
-    (None otherwise: the counters would describe another kernel)."""
-    import hashlib
+    from the committed ncu summary, if it was taken on the current f16_gemm
+    source (None otherwise: the counters would describe another kernel)."""
     path = os.path.join(ROOT, "profiles", "gemm_f16_m1570_all_blocks.md")
-    src = os.path.join(ROOT, "int4_weight_only_affine_gb300", "csrc", "gemm.cu")
     if not os.path.exists(path):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     vals = {}
     for line in open(path):
         if ":" in line and line.startswith("- "):
             k, v = line[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
-    if vals.get("gemm.cu sha256/16") != sha:
+    if vals.get("f16_gemm source sha256/16") != f16_gemm_source_hash():
         return None
     try:
         return float(vals["DRAM bytes per launch"])
@@ -802,6 +824,10 @@ def report(args, r, world, peaks, peak_src, hbm, tflops):
         **{f"decode_m{M}": hbm_part(DECODE_BYTES, pm[f"decode_m{M}"], tok_s=M * 1e3 / pm[f"decode_m{M}"],
                                     gemv_tflop_s=2.0 * M * (PROJ_WEIGHTS + LM_N * LM_K) / (pm[f"decode_m{M}"] / 1e3)
                                     / 1e12) for M in BATCH_MS},
+        **{f"decode_m{M}_list": hbm_part(DECODE_BYTES, pm[f"decode_m{M}_list"], tok_s=M * 1e3 / pm[f"decode_m{M}_list"],
+                                         note="the M-row token as one projection list (each operation waiting on "
+                                              "the completion counter) + per-row argmax")
+           for M in (2, 4)},
         "dequant": hbm_part(DEQUANT_BYTES, pm["dequant"]),
         "gemm_m128": gemm_part(128, pm["gemm_m128"]),
         "gemm_m512": gemm_part(512, pm["gemm_m512"]),
