@@ -575,22 +575,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //    different X tiles from L2.
 //  * Codes: a ring of 6 stages of 16 KB (128 rows x 256 k: four 64-k steps
 //    per tensor copy, 128-byte rows, 128-byte swizzle).  X and converted
-//    weights: a ring of 6 stages, each an X tile (128 rows x 64 k, K-major,
-//    128-byte swizzle, from L2) and 32 tensor-memory columns (64 k of
-//    binary16 per lane), released together by one MMA commit.
+//    weights: a ring of 4 operand stages of two 64-k steps each; a step is
+//    an X tile (128 rows x 64 k, K-major, 128-byte swizzle, from L2) and 32
+//    tensor-memory columns (64 k of binary16 per lane).  One MMA commit
+//    releases a whole operand stage.
 //  * Warp 0: one thread issues the code copies (weights are constants: no
 //    dependency wait).  Warp 14: one thread issues the X copies (after the
 //    dependency wait when launched as a programmatic dependent).
-//  * Warps 6-13: converters, two teams of four warps taking alternate 64-k
-//    steps; warp w converts the rows of its tensor-memory lane quarter
+//  * Warps 6-13: converters, two teams of four warps taking alternate
+//    operand stages; warp w converts the rows of its tensor-memory lane quarter
 //    (w % 4): lane l takes row 32 (w % 4) + l, reads its 64 codes of the
 //    step (two 16-byte loads, conflict-free under the swizzle) and writes
 //    the 32 binary16 pairs (w[n][k], w[n][k+1]) -- exactly the
 //    w4_dequant_f16 value, RNE(scale*q + bias) -- with one tensor-memory
 //    store.  Scales and biases are loaded one code stage ahead.
 //  * Warp 1: one thread issues tcgen05.mma.kind::f16 with A from tensor
-//    memory (M = 128, N = M rounded up to 16, K = 16), four per step, and
-//    commits each stage back.
+//    memory (M = 128, N = M rounded up to 16, K = 16), four per step and
+//    eight per operand stage, then one commit for the stage.
 //  * Warps 2-5: epilogue (lane quarter w % 4).  One split: round and store
 //    y.  Several: write the fp32 partial tile to the workspace; the CTA that
 //    completes a tile (arrival counter) sums the partials in split order and
@@ -599,10 +600,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // only the order of the 64-k steps in the fp32 accumulation differs.
 // ---------------------------------------------------------------------------
 constexpr int FBN = 128;                              // weight rows per tile
-constexpr int QST = 6;                                // X and converted-weight stages
+constexpr int QST = 4;                                // operand stages (X tiles + converted weights)
+constexpr int QSK = 2;                                // 64-k steps per operand stage
 constexpr int QCST = 6;                               // code stages
-constexpr int QCK = 4;                                // 64-k steps per code stage
-constexpr int QFX = BM * BK * 2;                      // 16 KB: X, 128 rows x 64 k
+constexpr int QCK = 4;                                // 64-k steps per code stage (two operand stages)
+constexpr int QFX = BM * BK * 2;                      // 16 KB: X, 128 rows x 64 k (one step)
 constexpr int QFC = FBN * 128;                        // 16 KB code stage: 128 rows x 32 words
 constexpr int Q_TEAM = 4;                             // converter warps per team (one per lane quarter)
 constexpr int Q_CONV0 = 6;
@@ -612,10 +614,12 @@ constexpr int Q_ACC_COLS = 128;                       // one accumulator: up to 
 constexpr int Q_A_COL0 = 2 * Q_ACC_COLS;              // converted weights after the two accumulators
 constexpr int F_TMEM_COLS = 512;
 constexpr int F_BARS = 2 * QCST + 3 * QST + 5;
-constexpr size_t F_SMEM = 1024 + (size_t)QST * QFX + (size_t)QCST * QFC + 8 * F_BARS + 16;
+constexpr size_t F_SMEM = 1024 + (size_t)QST * QSK * QFX + (size_t)QCST * QFC + 8 * F_BARS + 16;
 constexpr int kMaxSplit = 8;
 static_assert(QST >= 2, "converted-weight stage waits rely on at least two stages");
-static_assert(Q_A_COL0 + QST * 32 <= F_TMEM_COLS, "tensor-memory columns");
+static_assert(QCK == 2 * QSK, "a code stage holds two operand stages");
+static_assert(Q_A_COL0 + QST * QSK * 32 <= F_TMEM_COLS, "tensor-memory columns");
+static_assert(F_SMEM <= 227 * 1024, "shared memory");
 
 struct W4GemmArgs {
     const uint16_t *sc, *bi;  // scales, biases (null: symmetric codes)
@@ -702,7 +706,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
-    const uint32_t codes0 = base + QST * QFX;               // code ring
+    const uint32_t codes0 = base + QST * QSK * QFX;         // code ring
     const uint32_t bar0 = codes0 + QCST * QFC;
     auto code_full = [&](int c) { return bar0 + 8u * c; };                   // codes landed
     auto code_empty = [&](int c) { return bar0 + 8u * (QCST + c); };         // codes read by every converter
@@ -712,7 +716,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     auto accf_bar = [&](int x) { return bar0 + 8u * (2 * QCST + 3 * QST + x); };
     auto acce_bar = [&](int x) { return bar0 + 8u * (2 * QCST + 3 * QST + 2 + x); };
     const uint32_t done_bar = bar0 + 8u * (2 * QCST + 3 * QST + 4);
-    const size_t tail_off = (size_t)QST * QFX + (size_t)QCST * QFC + 8 * F_BARS;
+    const size_t tail_off = (size_t)QST * QSK * QFX + (size_t)QCST * QFC + 8 * F_BARS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + tail_off);
     volatile int *last_flag = reinterpret_cast<volatile int *>(gbase + tail_off + 4);
 
@@ -808,21 +812,24 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             // ---------------- X producer ----------------
             if (a.pdl) pdl_wait();  // x may be written by the previous kernel
             uint32_t issued_ph = 0, issued_any = 0;
-            int it = 0;
+            int g = 0;  // operand stages of this CTA
             bool ok = true;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
                 int n0, kb0, kb1;
                 unit_range(u, n0, kb0, kb1);
-                const int rot = unit_rot(u, kb0, kb1);
-                for (int j = 0; j < kb1 - kb0; ++j, ++it) {
-                    const int s = it % QST;
-                    const uint32_t ph = (it / QST) & 1;
+                const int rot = unit_rot(u, kb0, kb1), ns = kb1 - kb0;
+                for (int j = 0; j < ns; j += QSK, ++g) {
+                    const int s = g % QST;
+                    const uint32_t ph = (g / QST) & 1;
                     if (!mbar_wait(st_empty(s), ph ^ 1)) {
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(x_full(s), QFX);
-                    tma_load_2d(base + s * QFX, &tma_x, seq_kb(kb0, kb1, rot, j) * BK, 0, x_full(s));
+                    const int n = min(QSK, ns - j);  // steps of this stage
+                    mbar_expect_tx(x_full(s), n * QFX);
+                    for (int i = 0; i < n; ++i)
+                        tma_load_2d(base + (s * QSK + i) * QFX, &tma_x, seq_kb(kb0, kb1, rot, j + i) * BK, 0,
+                                    x_full(s));
                     issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
                     issued_any |= 1u << s;
                 }
@@ -833,11 +840,12 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
-            int it = 0, tc = 0;
+            int g = 0, tc = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++tc) {
                 int n0, kb0, kb1;
                 unit_range(u, n0, kb0, kb1);
+                const int ns = kb1 - kb0;
                 const int acc = tc & 1;
                 const uint32_t aph = (tc >> 1) & 1;
                 if (!mbar_wait(acce_bar(acc), aph ^ 1)) {
@@ -846,25 +854,32 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t dst = tmem + acc * Q_ACC_COLS;
-                // Stage s: X at base + s * QFX (descriptor address field + s *
-                // QFX / 16), converted weights at tensor-memory column
-                // Q_A_COL0 + 32 s; each 16-k slice is 32 bytes (+2) or 8
-                // columns further.
+                // Stage s, step i: X at base + (s * QSK + i) * QFX (descriptor
+                // address field + that / 16), converted weights at
+                // tensor-memory column Q_A_COL0 + 32 (s * QSK + i); each 16-k
+                // slice is 32 bytes (+2) or 8 columns further.
                 const uint64_t xd0 = smem_desc(base, 16, 1024);
-                for (int j = 0; j < kb1 - kb0; ++j, ++it) {
-                    const int sx = it % QST;
-                    const uint32_t ph = (it / QST) & 1;
+                for (int j = 0; j < ns; j += QSK, ++g) {
+                    const int sx = g % QST;
+                    const uint32_t ph = (g / QST) & 1;
                     if (!mbar_wait(x_full(sx), ph) || !mbar_wait(a_full(sx), ph)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t bd = xd0 + (uint64_t)(sx * (QFX >> 4));
-                    const uint32_t ta = tmem + Q_A_COL0 + sx * 32;
+                    const uint64_t bd = xd0 + (uint64_t)(sx * QSK * (QFX >> 4));
+                    const uint32_t ta = tmem + Q_A_COL0 + sx * QSK * 32;
                     mma_f16_tmem_a(dst, ta, bd, a.idesc, j != 0 ? 1u : 0u);
                     mma_f16_tmem_a(dst, ta + 8, bd + 2, a.idesc, 1u);
                     mma_f16_tmem_a(dst, ta + 16, bd + 4, a.idesc, 1u);
                     mma_f16_tmem_a(dst, ta + 24, bd + 6, a.idesc, 1u);
+                    if (j + 1 < ns) {
+                        const uint64_t bd1 = bd + (uint64_t)(QFX >> 4);
+                        mma_f16_tmem_a(dst, ta + 32, bd1, a.idesc, 1u);
+                        mma_f16_tmem_a(dst, ta + 40, bd1 + 2, a.idesc, 1u);
+                        mma_f16_tmem_a(dst, ta + 48, bd1 + 4, a.idesc, 1u);
+                        mma_f16_tmem_a(dst, ta + 56, bd1 + 6, a.idesc, 1u);
+                    }
                     mma_commit(st_empty(sx));
                 }
                 if (!ok) break;
@@ -949,18 +964,20 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16) + Q_A_COL0;
         // Position of a code stage of this CTA: unit u (rows n0, steps
         // [kb0, kb1) walked from rotation rot), the sequence position j of its
-        // first step, and the CTA step index of that step.
+        // first step, and the CTA operand-stage index gs of that step's stage
+        // (operand stages pair steps 2i, 2i + 1 of a unit and alternate
+        // between the two teams).
         struct CPos {
-            int u, n0, kb0, kb1, rot, j, it;
+            int u, n0, kb0, kb1, rot, j, gs;
         };
         auto cstep = [&](CPos &q) {
             const int j1 = q.j + QCK;
             if (j1 < q.kb1 - q.kb0) {
-                q.it += QCK;
+                q.gs += QCK / QSK;
                 q.j = j1;
                 return;
             }
-            q.it += q.kb1 - q.kb0 - q.j;
+            q.gs += (q.kb1 - q.kb0 - q.j + QSK - 1) / QSK;
             q.u += gridDim.x;
             if (q.u < units) {
                 unit_range(q.u, q.n0, q.kb0, q.kb1);
@@ -978,7 +995,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < QCK; ++j) {
                 sv[j] = bv[j] = 0u;
-                if (q.j + j >= q.kb1 - q.kb0 || ((q.it + j) & 1) != team) continue;
+                if (q.j + j >= q.kb1 - q.kb0 || ((q.gs + j / QSK) & 1) != team) continue;
                 const int kb = seq_kb(q.kb0, q.kb1, q.rot, q.j + j);
                 const int g0 = (kb * BK) >> gshift, g1 = (kb * BK + 32) >> gshift;
                 sv[j] = (uint32_t)ld_nc_u16(srow + g0) | ((uint32_t)ld_nc_u16(srow + g1) << 16);
@@ -987,7 +1004,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         };
         CPos pf;
         pf.u = blockIdx.x;
-        pf.it = 0;
+        pf.gs = 0;
         if (pf.u < units) {
             unit_range(pf.u, pf.n0, pf.kb0, pf.kb1);
             pf.rot = unit_rot(pf.u, pf.kb0, pf.kb1);
@@ -1013,46 +1030,52 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 break;
             }
             const uint32_t crow = codes0 + c * QFC + rl * 128;
+            const int ns = cur.kb1 - cur.kb0;
 #pragma unroll
-            for (int j = 0; j < QCK; ++j) {
-                const int it = cur.it + j;          // step position of this CTA
-                if (cur.j + j >= cur.kb1 - cur.kb0) break;
-                if ((it & 1) != team) continue;     // the other team's step
-                const uint4 qa = lds128(crow + (((2 * j) ^ sw) << 4));
-                const uint4 qb = lds128(crow + (((2 * j + 1) ^ sw) << 4));
-                const int sa = it % QST;
-                // The stage is free once the MMAs of its previous use (step
-                // it - QST) are done; this team's previous step (it - 2)
-                // waited for step it - 2 - QST, so with QST >= 2 every
-                // earlier phase of the barrier is complete and the parity
-                // cannot alias.
-                if (!mbar_wait(st_empty(sa), ((it / QST) & 1) ^ 1)) {
+            for (int q = 0; q < QCK / QSK; ++q) {
+                const int g = cur.gs + q;            // operand stage of steps j, j + 1
+                const int jq = cur.j + QSK * q;
+                if (jq >= ns) break;
+                if ((g & 1) != team) continue;      // the other team's stage
+                const int sa = g % QST;
+                // The stage is free once the MMAs of its previous use (stage
+                // g - QST) are done; this team's previous stage (g - 2)
+                // waited for stage g - 2 - QST, so with QST >= 2 every earlier
+                // phase of the barrier is complete and the parity cannot alias.
+                if (!mbar_wait(st_empty(sa), ((g / QST) & 1) ^ 1)) {
                     ok = false;
                     break;
                 }
-                uint32_t out[32];
-                const uint32_t wd[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    // Scale and bias of the word's 32-k half, in both halves.
-                    const uint32_t sv = i < 4 ? __byte_perm(cus[j], 0, 0x1010) : __byte_perm(cus[j], 0, 0x3232);
-                    const uint32_t bv = i < 4 ? __byte_perm(cub[j], 0, 0x1010) : __byte_perm(cub[j], 0, 0x3232);
-                    const __half2 s2 = *reinterpret_cast<const __half2 *>(&sv);
-                    const __half2 b2 = *reinterpret_cast<const __half2 *>(&bv);
-                    const uint32_t w = wd[i], w4 = w >> 4;
-                    // Codes (2e, 2e + 1) of the word into the two halves:
-                    // bytes e of w and of w >> 4, low nibbles.
-                    const uint32_t p[4] = {__byte_perm(w, w4, 0x5410), __byte_perm(w, w4, 0x6521),
-                                           __byte_perm(w, w4, 0x7632), __byte_perm(w, w4, 0x7733)};
+                for (int i = 0; i < QSK; ++i) {
+                    const int j = QSK * q + i;        // step within the code stage
+                    if (jq + i >= ns) break;
+                    const uint4 qa = lds128(crow + (((2 * j) ^ sw) << 4));
+                    const uint4 qb = lds128(crow + (((2 * j + 1) ^ sw) << 4));
+                    uint32_t out[32];
+                    const uint32_t wd[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint32_t qv = (p[e] & 0x000F000Fu) | 0x64006400u;  // 1024 + q
-                        const __half2 q2 = __hsub2(*reinterpret_cast<const __half2 *>(&qv), koff);
-                        const __half2 w2 = sym ? __hmul2(q2, s2) : __hfma2(q2, s2, b2);  // one rounding
-                        out[4 * i + e] = *reinterpret_cast<const uint32_t *>(&w2);
+                    for (int w = 0; w < 8; ++w) {
+                        // Scale and bias of the word's 32-k half, in both halves.
+                        const uint32_t sv = w < 4 ? __byte_perm(cus[j], 0, 0x1010) : __byte_perm(cus[j], 0, 0x3232);
+                        const uint32_t bv = w < 4 ? __byte_perm(cub[j], 0, 0x1010) : __byte_perm(cub[j], 0, 0x3232);
+                        const __half2 s2 = *reinterpret_cast<const __half2 *>(&sv);
+                        const __half2 b2 = *reinterpret_cast<const __half2 *>(&bv);
+                        const uint32_t x = wd[w], x4 = x >> 4;
+                        // Codes (2e, 2e + 1) of the word into the two halves:
+                        // bytes e of x and of x >> 4, low nibbles.
+                        const uint32_t p[4] = {__byte_perm(x, x4, 0x5410), __byte_perm(x, x4, 0x6521),
+                                               __byte_perm(x, x4, 0x7632), __byte_perm(x, x4, 0x7733)};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const uint32_t qv = (p[e] & 0x000F000Fu) | 0x64006400u;  // 1024 + q
+                            const __half2 q2 = __hsub2(*reinterpret_cast<const __half2 *>(&qv), koff);
+                            const __half2 w2 = sym ? __hmul2(q2, s2) : __hfma2(q2, s2, b2);  // one rounding
+                            out[4 * w + e] = *reinterpret_cast<const uint32_t *>(&w2);
+                        }
                     }
+                    tmem_st32(trow + (sa * QSK + i) * 32, out);
                 }
-                tmem_st32(trow + sa * 32, out);
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
