@@ -30,6 +30,21 @@ def test_gemm_small_full_compare(w4, M, N, K):
     assert w4.device_status() == 0
 
 
+# Every output of the CTA-pair kernel at the prefill lengths, with ragged
+# column tiles (N = 2040, 520) and ragged row tiles (M = 1570, 300); K = 64
+# keeps the full oracle comparison quick.
+@pytest.mark.parametrize("M,N", [(1570, 2040), (512, 11008), (4096, 2560), (300, 520), (1570, 2560)])
+def test_gemm_pair_full_compare(w4, M, N):
+    K = 64
+    x = synth.make_half_matrix(51 + M, M, K)
+    w = synth.make_half_matrix(52 + N, K, N, std=0.05)
+    y = w4.f16_gemm(to_dev(x), to_dev(w)).cpu().numpy()
+    yo, ad = oracle.gemm(x, w, M, N, K)
+    ok, worst = within_tol(y, yo, ad)
+    assert ok, f"worst err/tol = {worst}"
+    assert w4.device_status() == 0
+
+
 def _entries(M, N, n=1500, seed=0):
     g = np.random.default_rng(seed)
     ms = g.integers(0, M, size=n)
