@@ -257,24 +257,30 @@ W4A16_API int w4_dequant_f16_ex(const uint32_t *qweight, const uint16_t *scales,
  *   w4_dequant_f16, multiplied without writing a scratch.
  *   ("The inference engine - Mojo 1.0 on Metal", "Crossing Mojo 1.0": the
  *   prefill GEMM over dequantised weights; here the weights are dequantised
- *   tile by tile in shared memory and read from HBM only as 4-bit codes.)
+ *   tile by tile into tensor memory and read from HBM only as 4-bit codes.)
  *   x        binary16 [M][K]   activations
  *   qweight, scales, biases, group    the int4 weight (format above)
  *   y        binary16 [M][N]   output; fp32 accumulation, one rounding
  *   M 1..128;  N >= 8, N % 8 == 0;  K >= 64, K % 64 == 0.
  *   workspace  device buffer of at least w4_gemm_workspace_bytes(M, N, K)
  *              bytes, 16-byte aligned, ZERO-FILLED before its first use and
- *              then passed unchanged to later calls (its tile counters return
- *              to zero at the end of every call).  Calls ordered on one
- *              stream may share it, also with W4A16_OVERLAP_PREVIOUS (a call
- *              touches it only after its dependency wait); calls that may run
- *              concurrently need separate workspaces.
- *              Small N splits K over several blocks whose fp32 partial sums
- *              it holds.
+ *              then passed unchanged to later calls (its grid-barrier
+ *              counters are left ready for the next call).  Calls ordered on
+ *              one stream may share it, also with W4A16_OVERLAP_PREVIOUS (a
+ *              call touches it only after its dependency wait); calls that
+ *              may run concurrently need separate workspaces.
+ *              It holds the fp32 partial sums of the 128-row weight tiles
+ *              whose k steps are shared by several blocks (the tiles left
+ *              over after every block has taken whole tiles).
  *   The products are those of f16_gemm on the w4_dequant_f16 scratch (the
  *   same binary16 weight values); the 64-k steps of a tile are accumulated
- *   in fp32 starting from a per-tile rotation, and with several K splits
- *   the partial sums are added in split order.  Results are deterministic.
+ *   in fp32 starting from a per-tile rotation, and a tile shared by several
+ *   blocks adds their partial sums in ascending k.  Results are
+ *   deterministic.  For M <= 32 the last block to bring a shared tile's
+ *   partial sums adds them all.  For M > 32 the launch is cooperative
+ *   (every block resident): the blocks sharing a tile wait for each other's
+ *   partial sums and each adds a slice (bounded: on expiry the call leaves
+ *   that tile unwritten and w4a16_device_status reports W4_ERR_TIMEOUT).
  * Errors: W4_ERR_NULL, W4_ERR_SHAPE, W4_ERR_GROUP, W4_ERR_ALIGN,
  * W4_ERR_WORKSPACE, W4_ERR_DEVICE, W4_ERR_LAUNCH.
  */
@@ -289,8 +295,9 @@ W4A16_API int w4_gemm_ex(const uint16_t *x, const uint32_t *qweight, const uint1
                          const uint16_t *biases, uint16_t *y, int M, int N, int K, int group,
                          void *workspace, size_t workspace_bytes, unsigned flags, void *stream);
 
-/* Workspace bytes for w4_gemm (0 if the sizes are invalid).  Depends only on
- * its arguments. */
+/* Workspace bytes for w4_gemm (0 if the sizes are invalid): 3328 bytes of
+ * counters and flags and 2 x min(256, ceil(N / 128) x K / 64) fp32 tiles of
+ * M x 128.  Depends only on its arguments. */
 W4A16_API size_t w4_gemm_workspace_bytes(int M, int N, int K);
 
 /*

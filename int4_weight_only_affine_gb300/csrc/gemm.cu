@@ -569,10 +569,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // tensor memory; B = the activation tile X (its N = M rounded up to 16,
 // K-major in shared memory); D[n][m] = sum_k w[n][k] x[m][k] accumulates in
 // tensor memory with one weight row per lane.
-//  * Tiles of 128 weight rows.  Small-N shapes split K over several CTAs
-//    (units = tiles x splits).  A unit walks its 64-k steps from a rotation
-//    that differs between tiles, so that CTAs working at the same time read
-//    different X tiles from L2.
+//  * Tiles of 128 weight rows, one CTA per SM (G CTAs).  Each CTA takes
+//    tiles / G whole tiles (tile i G + b for CTA b); the k steps of the
+//    remaining tiles are shared out evenly (a contiguous range of the
+//    (tile, step) sequence per CTA, stream-K style), so no SM idles for a
+//    partial wave.  A unit (a whole tile, or one tile's part of a CTA's
+//    range) walks its 64-k steps from a rotation that differs between
+//    tiles, so that CTAs working at the same time read different X tiles
+//    from L2.
 //  * Codes: a ring of 6 stages of 16 KB (128 rows x 256 k: four 64-k steps
 //    per tensor copy, 128-byte rows, 128-byte swizzle).  X and converted
 //    weights: a ring of 4 operand stages of two 64-k steps each; a step is
@@ -592,10 +596,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 //  * Warp 1: one thread issues tcgen05.mma.kind::f16 with A from tensor
 //    memory (M = 128, N = M rounded up to 16, K = 16), four per step and
 //    eight per operand stage, then one commit for the stage.
-//  * Warps 2-5: epilogue (lane quarter w % 4).  One split: round and store
-//    y.  Several: write the fp32 partial tile to the workspace; the CTA that
-//    completes a tile (arrival counter) sums the partials in split order and
-//    stores y, and resets the counter for the next call.
+//  * Warps 2-5: epilogue (lane quarter w % 4).  A whole tile: round and
+//    store y.  A part of a shared tile: write the fp32 partial tile to the
+//    CTA's workspace slot.  For M > 32 the CTA flags it (the call's epoch +
+//    1); at the end each CTA waits for the flags of the CTAs it shares a tile
+//    with (the launch is cooperative: all resident) and sums its slice of
+//    that tile's partials in ascending k; the last CTA to finish advances the
+//    epoch.  For M <= 32 the CTA counts its arrival on the tile, and the
+//    last to arrive sums the whole tile (nobody waits).
 // The binary16 operands are those of f16_gemm on the w4_dequant_f16 scratch;
 // only the order of the 64-k steps in the fp32 accumulation differs.
 // ---------------------------------------------------------------------------
@@ -615,7 +623,7 @@ constexpr int Q_A_COL0 = 2 * Q_ACC_COLS;              // converted weights after
 constexpr int F_TMEM_COLS = 512;
 constexpr int F_BARS = 2 * QCST + 3 * QST + 5;
 constexpr size_t F_SMEM = 1024 + (size_t)QST * QSK * QFX + (size_t)QCST * QFC + 8 * F_BARS + 16;
-constexpr int kMaxSplit = 8;
+constexpr int kW4MaxGrid = 256;                       // CTAs per launch (>= the SMs of the GPU)
 static_assert(QST >= 2, "converted-weight stage waits rely on at least two stages");
 static_assert(QCK == 2 * QSK, "a code stage holds two operand stages");
 static_assert(Q_A_COL0 + QST * QSK * 32 <= F_TMEM_COLS, "tensor-memory columns");
@@ -624,11 +632,16 @@ static_assert(F_SMEM <= 227 * 1024, "shared memory");
 struct W4GemmArgs {
     const uint16_t *sc, *bi;  // scales, biases (null: symmetric codes)
     uint16_t *y;              // [M][N]
-    float *part;              // [S][M][N] fp32 partial tiles (S > 1)
-    unsigned *cnt;            // [tiles] arrival counters (S > 1), zero between calls
+    float *part;              // [2 * grid][M][128] fp32 partial tiles (split > 0)
+    unsigned *bar;            // [0] CTAs finished, [1] call epoch (zero before the first call)
+    unsigned *flags;          // [2 * grid] epoch + 1 once the partial tile of that slot is stored (split 1)
+    unsigned *tcnt;           // [remaining tiles] arrivals of a shared tile's CTAs (split 2), zero between calls
     int M, N, K;
     WFmt f;
-    int S;                    // K splits per tile
+    int fw;                   // whole tiles per CTA (tile w * grid + b for CTA b)
+    int spc;                  // k steps per CTA on the remaining tiles
+    int split;                // remaining tiles shared by several CTAs: 0 none; 1 the sharers wait for
+                              // each other's flags and each sums a slice; 2 the last to arrive sums it
     int pdl;
     uint32_t idesc;           // instruction descriptor (N = M rounded up to 16)
 };
@@ -653,51 +666,53 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 
-// Sum of the S fp32 partial tiles of rows [0, M) x columns [n0, n0 + 128)
-// in split order, stored as binary16: thread et of the 128 epilogue threads
-// takes 8-column chunks et, et + 128, ..., max(1, 4 / S) chunks at a time
-// with every split's loads of them in flight together.
-template <int S>
-__device__ __noinline__ void reduce_splits(const W4GemmArgs &a, int M, int N, int n0, int et) {
-    constexpr int U = S >= 4 ? 1 : 4 / S;
-    const int chunks = M * (FBN / 8);
-    for (int c0 = et; c0 < chunks; c0 += 128 * U) {
-        float4 p0[U][S], p1[U][S];
+// Item it of slice j of c of remaining tile t (shared by CTAs bf .. bf + c
+// - 1; an item is 8 columns of one row): the partial sums of its CTAs
+// (ascending CTA index = ascending k) added in that order, rounded once and
+// stored.  The loads of up to 8 partials are in flight together.
+__device__ __forceinline__ void reduce_item(const W4GemmArgs &a, int nk, int G, int rtot, int t, int bf, int c,
+                                            int it) {
+    const int M = a.M, N = a.N, spc = a.spc, bl = bf + c - 1;
+    const int m = it / (FBN / 8), cc = it % (FBN / 8);
+    const int n = (a.fw * G + t) * FBN + 8 * cc;
+    if (m >= M || n >= N) return;
+    float acc[8];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int ci = c0 + 128 * u;
-            const int r = ci / (FBN / 8), n = n0 + 8 * (ci % (FBN / 8));
-            if (ci < chunks && n < N) {
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int b0 = bf; b0 <= bl; b0 += 8) {
+        float4 p0[8], p1[8];
 #pragma unroll
-                for (int sp = 0; sp < S; ++sp) {
-                    const float *src = a.part + ((size_t)sp * M + r) * N + n;
-                    p0[u][sp] = __ldcg(reinterpret_cast<const float4 *>(src));
-                    p1[u][sp] = __ldcg(reinterpret_cast<const float4 *>(src + 4));
-                }
+        for (int q = 0; q < 8; ++q) {
+            const int b = b0 + q;
+            if (b <= bl) {
+                const int slot = 2 * b + (min((b + 1) * spc, rtot) <= (t + 1) * nk ? 1 : 0);
+                const float *src = a.part + ((size_t)slot * M + m) * FBN + 8 * cc;
+                p0[q] = __ldcg(reinterpret_cast<const float4 *>(src));
+                p1[q] = __ldcg(reinterpret_cast<const float4 *>(src + 4));
             }
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int ci = c0 + 128 * u;
-            const int r = ci / (FBN / 8), n = n0 + 8 * (ci % (FBN / 8));
-            if (ci >= chunks || n >= N) continue;
-            float4 s0 = p0[u][0], s1 = p1[u][0];
-#pragma unroll
-            for (int sp = 1; sp < S; ++sp) {
-                s0.x += p0[u][sp].x; s0.y += p0[u][sp].y; s0.z += p0[u][sp].z; s0.w += p0[u][sp].w;
-                s1.x += p1[u][sp].x; s1.y += p1[u][sp].y; s1.z += p1[u][sp].z; s1.w += p1[u][sp].w;
-            }
-            uint4 o;
-            o.x = pack_half2(__float_as_uint(s0.x), __float_as_uint(s0.y));
-            o.y = pack_half2(__float_as_uint(s0.z), __float_as_uint(s0.w));
-            o.z = pack_half2(__float_as_uint(s1.x), __float_as_uint(s1.y));
-            o.w = pack_half2(__float_as_uint(s1.z), __float_as_uint(s1.w));
-            *reinterpret_cast<uint4 *>(a.y + (size_t)r * N + n) = o;
+        for (int q = 0; q < 8; ++q) {
+            if (b0 + q > bl) break;
+            acc[0] += p0[q].x; acc[1] += p0[q].y; acc[2] += p0[q].z; acc[3] += p0[q].w;
+            acc[4] += p1[q].x; acc[5] += p1[q].y; acc[6] += p1[q].z; acc[7] += p1[q].w;
         }
     }
+    uint4 o;
+    o.x = pack_half2(__float_as_uint(acc[0]), __float_as_uint(acc[1]));
+    o.y = pack_half2(__float_as_uint(acc[2]), __float_as_uint(acc[3]));
+    o.z = pack_half2(__float_as_uint(acc[4]), __float_as_uint(acc[5]));
+    o.w = pack_half2(__float_as_uint(acc[6]), __float_as_uint(acc[7]));
+    *reinterpret_cast<uint4 *>(a.y + (size_t)m * N + n) = o;
 }
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 __global__ void __launch_bounds__(F_THREADS, 1)
     w4gemm_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_constant__ CUtensorMap tma_q,
@@ -718,28 +733,45 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     const uint32_t done_bar = bar0 + 8u * (2 * QCST + 3 * QST + 4);
     const size_t tail_off = (size_t)QST * QSK * QFX + (size_t)QCST * QFC + 8 * F_BARS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + tail_off);
-    volatile int *last_flag = reinterpret_cast<volatile int *>(gbase + tail_off + 4);
+    volatile int *bar_failed = reinterpret_cast<volatile int *>(gbase + tail_off + 4);
+    volatile unsigned *epoch_sh = reinterpret_cast<volatile unsigned *>(gbase + tail_off + 8);
+    volatile int *last_sh = reinterpret_cast<volatile int *>(gbase + tail_off + 12);
 
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int M = a.M, N = a.N, S = a.S;
+    const int M = a.M, N = a.N, G = (int)gridDim.x, blk = (int)blockIdx.x;
     const int nk = a.K / BK;
     const int tiles = (N + FBN - 1) / FBN;
-    const int units = tiles * S;
-    // Unit u: tile u / S (weight rows n0 ..), k steps [kb0, kb1) of split u % S.
-    auto unit_range = [&](int u, int &n0, int &kb0, int &kb1) {
-        const int sp = u % S;
-        n0 = (u / S) * FBN;
-        kb0 = sp * nk / S;  // S <= 8 and nk < 2^24: no overflow
-        kb1 = (sp + 1) * nk / S;
+    const int rtiles = tiles - a.fw * G;  // tiles shared out by k steps
+    const int rtot = rtiles * nk;
+    const int l0 = blk * a.spc, l1 = min(l0 + a.spc, rtot);  // this CTA's steps of them
+    // Work unit i of this CTA: first its whole tiles (tile i * G + blk, all
+    // nk steps), then the pieces of its step range [l0, l1) of the remaining
+    // tiles, one per tile it touches (step l is k step l % nk of remaining
+    // tile l / nk).  Returns false past the last unit.
+    auto unit_range = [&](int i, int &tile, int &kb0, int &kb1) {
+        if (i < a.fw) {
+            tile = i * G + blk;
+            kb0 = 0;
+            kb1 = nk;
+            return true;
+        }
+        if (l0 >= l1) return false;
+        const int t = l0 / nk + (i - a.fw);
+        const int s0 = max(l0, t * nk), s1 = min(l1, (t + 1) * nk);
+        if (s0 >= s1) return false;
+        tile = a.fw * G + t;
+        kb0 = s0 - t * nk;
+        kb1 = s1 - t * nk;
+        return true;
     };
     // A unit walks its k steps starting at kb0 + rot and wrapping around, rot
     // a multiple of a code stage that differs between tiles: CTAs working on
     // different tiles at the same time then read different X tiles, instead
     // of all of them asking L2 for the same one.
-    auto unit_rot = [&](int u, int kb0, int kb1) {
+    auto unit_rot = [&](int tile, int kb0, int kb1) {
         const int ns = kb1 - kb0;
-        return ns % QCK ? 0 : (int)(((unsigned)(u / S) * 5u) % (unsigned)(ns / QCK)) * QCK;
+        return ns % QCK ? 0 : (int)(((unsigned)tile * 5u) % (unsigned)(ns / QCK)) * QCK;
     };
     auto seq_kb = [](int kb0, int kb1, int rot, int j) {
         int v = j + rot;
@@ -762,7 +794,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             mbar_init(acce_bar(x), 4);
         }
         mbar_init(done_bar, 1);
-        *last_flag = 0;
+        *bar_failed = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tma_x) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tma_q) : "memory");
@@ -784,10 +816,10 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             uint32_t issued_ph = 0, issued_any = 0;
             int cs = 0;  // code stages issued
             bool ok = true;
-            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-                int n0, kb0, kb1;
-                unit_range(u, n0, kb0, kb1);
-                const int rot = unit_rot(u, kb0, kb1);
+            int tile, kb0, kb1;
+            for (int u = 0; ok && unit_range(u, tile, kb0, kb1); ++u) {
+                const int n0 = tile * FBN;
+                const int rot = unit_rot(tile, kb0, kb1);
                 for (int j = 0; j < kb1 - kb0; j += QCK, ++cs) {
                     const int c = cs % QCST;
                     const uint32_t ph = (cs / QCST) & 1;
@@ -814,10 +846,9 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             uint32_t issued_ph = 0, issued_any = 0;
             int g = 0;  // operand stages of this CTA
             bool ok = true;
-            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-                int n0, kb0, kb1;
-                unit_range(u, n0, kb0, kb1);
-                const int rot = unit_rot(u, kb0, kb1), ns = kb1 - kb0;
+            int tile, kb0, kb1;
+            for (int u = 0; ok && unit_range(u, tile, kb0, kb1); ++u) {
+                const int rot = unit_rot(tile, kb0, kb1), ns = kb1 - kb0;
                 for (int j = 0; j < ns; j += QSK, ++g) {
                     const int s = g % QST;
                     const uint32_t ph = (g / QST) & 1;
@@ -842,9 +873,8 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             // ---------------- MMA issuer ----------------
             int g = 0, tc = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++tc) {
-                int n0, kb0, kb1;
-                unit_range(u, n0, kb0, kb1);
+            int tile, kb0, kb1;
+            for (int u = 0; ok && unit_range(u, tile, kb0, kb1); ++u, ++tc) {
                 const int ns = kb1 - kb0;
                 const int acc = tc & 1;
                 const uint32_t aph = (tc >> 1) & 1;
@@ -891,20 +921,35 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     } else if (warp >= 2 && warp < Q_CONV0) {
         // ---------------- epilogue: warps 2..5 ----------------
         // Lane l of warp w holds weight row n0 + 32 (w % 4) + l; columns are
-        // activation rows.  After an expired wait a warp skips its work but
-        // still takes part in the named barriers of every unit.
+        // activation rows.  A unit that covers its whole tile stores y; a
+        // piece of a shared tile stores its fp32 partial sums in the slot of
+        // this CTA (2 blk for its first unit of the remaining tiles when that
+        // is not also its last, 2 blk + 1 for its last) and then flags the
+        // slot with the call's epoch + 1.  After an expired wait a warp skips
+        // its work but still takes part in the named barriers of every unit.
         const int quad = warp & 3;
-        bool ok = true;
         int tc = 0;
         const int ncol = (M + 31) / 32;  // 32-column chunks that hold activation rows
-        for (int u = blockIdx.x; u < units; u += gridDim.x, ++tc) {
-            int n0, kb0, kb1;
-            unit_range(u, n0, kb0, kb1);
+        unsigned ep1 = 0;
+        if (a.split == 1 && warp == 2 && lane == 0) {
+            pdl_wait();  // the previous call on this workspace has finished
+            unsigned e;
+            asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(e) : "l"(a.bar + 1) : "memory");
+            *epoch_sh = e;
+            ep1 = e + 1u;
+        }
+        bool ok = true;
+        int tile, kb0, kb1;
+        for (int u = 0; unit_range(u, tile, kb0, kb1); ++u, ++tc) {
+            const int n0 = tile * FBN;
             const int acc = tc & 1;
             const uint32_t aph = (tc >> 1) & 1;
             const int n = n0 + quad * 32 + lane;
             if (ok && !mbar_wait(accf_bar(acc), aph)) ok = false;
             if (ok) tc_fence_after();
+            const bool whole = kb0 == 0 && kb1 == nk;
+            const int t = tile - a.fw * G;  // remaining-tile index (whole == false only there)
+            const int slot = 2 * blk + (l1 <= (t + 1) * nk ? 1 : 0);
             for (int c = 0; c < ncol && ok; ++c) {
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + acc * Q_ACC_COLS + c * 32, r);
@@ -915,40 +960,45 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 }
                 if (n >= N) continue;
                 const int m0 = c * 32;
-                if (S == 1) {
+                if (whole) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         if (m0 + i < M) a.y[(size_t)(m0 + i) * N + n] = __half_as_ushort(__float2half_rn(__uint_as_float(r[i])));
                 } else {
-                    float *dst = a.part + ((size_t)(u % S) * M) * N + n;
+                    float *dst = a.part + (size_t)slot * M * FBN + (n - n0);
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        if (m0 + i < M) __stcg(dst + (size_t)(m0 + i) * N, __uint_as_float(r[i]));
+                        if (m0 + i < M) __stcg(dst + (size_t)(m0 + i) * FBN, __uint_as_float(r[i]));
                 }
             }
-            if (S > 1) {
-                // The CTA that brings a tile's S-th partial sums them in split order.
-                __threadfence();
+            if (!whole) {
+                // The named barrier orders the four warps' stores before the
+                // flag or the arrival (the fence is cumulative at gpu scope).
                 epi_sync();
-                if (warp == 2 && lane == 0) {
-                    const int t = u / S;
-                    const unsigned prev = atomicAdd(a.cnt + t, 1u);
-                    const int last = prev == (unsigned)(S - 1);
-                    if (last) a.cnt[t] = 0u;  // every split has arrived: ready for the next call
-                    *last_flag = last;
+                if (a.split == 1) {
+                    if (warp == 2 && lane == 0) {
+                        __threadfence();
+                        asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a.flags + slot), "r"(ep1) : "memory");
+                    }
+                } else {
+                    // The CTA that brings the tile's last partial sums them
+                    // all (no CTA waits) and resets the count for the next call.
+                    const int bf = (t * nk) / a.spc, bl = min(G - 1, ((t + 1) * nk - 1) / a.spc);
+                    if (warp == 2 && lane == 0) {
+                        __threadfence();
+                        const unsigned prev = atomicAdd(a.tcnt + t, 1u);
+                        const int last = prev == (unsigned)(bl - bf);
+                        if (last) a.tcnt[t] = 0u;
+                        *last_sh = last;
+                    }
+                    epi_sync();
+                    if (*last_sh && ok) {
+                        __threadfence();
+                        for (int it = (warp - 2) * 32 + lane; it < M * (FBN / 8); it += 128)
+                            reduce_item(a, nk, G, rtot, t, bf, bl - bf + 1, it);
+                    }
+                    epi_sync();  // every epilogue thread has read the flag before the next unit
                 }
-                epi_sync();
-                if (*last_flag && ok) {
-                    __threadfence();
-                    const int et = (warp - 2) * 32 + lane;
-                    if (S == 2)
-                        reduce_splits<2>(a, M, N, n0, et);
-                    else if (S == 4)
-                        reduce_splits<4>(a, M, N, n0, et);
-                    else
-                        reduce_splits<8>(a, M, N, n0, et);
-                }
-                epi_sync();  // the flag is read by every epilogue thread before the next unit
             }
         }
     } else if (warp >= Q_CONV0 && warp < Q_XWARP) {
@@ -969,6 +1019,16 @@ __global__ void __launch_bounds__(F_THREADS, 1)
         // between the two teams).
         struct CPos {
             int u, n0, kb0, kb1, rot, j, gs;
+            bool valid;
+        };
+        auto cset = [&](CPos &q) {
+            int tile;
+            q.valid = unit_range(q.u, tile, q.kb0, q.kb1);
+            if (q.valid) {
+                q.n0 = tile * FBN;
+                q.rot = unit_rot(tile, q.kb0, q.kb1);
+                q.j = 0;
+            }
         };
         auto cstep = [&](CPos &q) {
             const int j1 = q.j + QCK;
@@ -978,12 +1038,8 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 return;
             }
             q.gs += (q.kb1 - q.kb0 - q.j + QSK - 1) / QSK;
-            q.u += gridDim.x;
-            if (q.u < units) {
-                unit_range(q.u, q.n0, q.kb0, q.kb1);
-                q.rot = unit_rot(q.u, q.kb0, q.kb1);
-                q.j = 0;
-            }
+            ++q.u;
+            cset(q);
         };
         // Scales (and biases) of the two 32-k halves of this team's steps of
         // the code stage at q, as binary16 bit patterns (loaded one code
@@ -1003,18 +1059,14 @@ __global__ void __launch_bounds__(F_THREADS, 1)
             }
         };
         CPos pf;
-        pf.u = blockIdx.x;
+        pf.u = 0;
         pf.gs = 0;
-        if (pf.u < units) {
-            unit_range(pf.u, pf.n0, pf.kb0, pf.kb1);
-            pf.rot = unit_rot(pf.u, pf.kb0, pf.kb1);
-            pf.j = 0;
-        }
+        cset(pf);
         uint32_t nxs[QCK], nxb[QCK];
-        if (pf.u < units) load_sb(pf, nxs, nxb);
+        if (pf.valid) load_sb(pf, nxs, nxb);
         bool ok = true;
         int cs = 0;  // code stages
-        while (pf.u < units && ok) {
+        while (pf.valid && ok) {
             const CPos cur = pf;
             uint32_t cus[QCK], cub[QCK];
 #pragma unroll
@@ -1023,7 +1075,7 @@ __global__ void __launch_bounds__(F_THREADS, 1)
                 cub[j] = nxb[j];
             }
             cstep(pf);
-            if (pf.u < units) load_sb(pf, nxs, nxb);
+            if (pf.valid) load_sb(pf, nxs, nxb);
             const int c = cs % QCST;
             if (!mbar_wait(code_full(c), (cs / QCST) & 1)) {
                 ok = false;
@@ -1096,6 +1148,69 @@ __global__ void __launch_bounds__(F_THREADS, 1)
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(F_TMEM_COLS));
+    }
+    if (a.split != 1) return;
+    // The shared tiles this CTA touched (at most two: the first and last tile
+    // of its step range; the ones between are whole): wait until every CTA
+    // that shares one of them has flagged its partial tile (the launch is
+    // cooperative, so they are all resident; bounded), then sum slice
+    // blk - bf of each, both tiles' items in one pass.
+    const unsigned want = *epoch_sh + 1u;
+    int st_t[2], st_bf[2], st_c[2], nst = 0;
+    if (l0 < l1) {
+        const int tf = l0 / nk, tl = (l1 - 1) / nk;
+        for (int t = tf; t <= tl; t += (tl > tf ? tl - tf : 1)) {
+            const int bf = (t * nk) / a.spc, bl = min(G - 1, ((t + 1) * nk - 1) / a.spc);
+            if (bf == bl) continue;
+            st_t[nst] = t;
+            st_bf[nst] = bf;
+            st_c[nst] = bl - bf + 1;
+            ++nst;
+        }
+    }
+    if (nst > 0) {
+        const int cw = st_c[0] + (nst > 1 ? st_c[1] : 0);
+        for (int i = threadIdx.x; i < cw; i += blockDim.x) {
+            const int k = i < st_c[0] ? 0 : 1;
+            const int t = st_t[k], b = st_bf[k] + (k ? i - st_c[0] : i);
+            const int slot = 2 * b + (min((b + 1) * a.spc, rtot) <= (t + 1) * nk ? 1 : 0);
+            const uint64_t t0 = global_ns();
+            while (ld_acquire_u32(a.flags + slot) != want) {
+                if (*bar_failed) break;
+                if (global_ns() - t0 > kWaitNs) {
+                    atomicExch(&g_wait_expired, 1);
+                    *bar_failed = 1;
+                    break;
+                }
+            }
+        }
+        __syncthreads();
+        if (!*bar_failed) {
+            // Slice j of c of a tile: the contiguous items [j len, (j + 1) len)
+            // of its M x 16 (len = ceil(M x 16 / c)), so that neighbouring
+            // threads read neighbouring 32-byte chunks.
+            const int items = a.M * (FBN / 8);
+            int lo[2] = {0, 0}, cnt[2] = {0, 0};
+            for (int k = 0; k < nst; ++k) {
+                const int len = (items + st_c[k] - 1) / st_c[k];
+                lo[k] = (blk - st_bf[k]) * len;
+                cnt[k] = max(0, min(items, lo[k] + len) - lo[k]);
+            }
+            for (int i = threadIdx.x; i < cnt[0] + cnt[1]; i += blockDim.x) {
+                const int k = i < cnt[0] ? 0 : 1;
+                reduce_item(a, nk, G, rtot, st_t[k], st_bf[k], st_c[k], lo[k] + (k ? i - cnt[0] : i));
+            }
+        }
+    }
+    // The last CTA to finish advances the epoch for the next call.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(a.bar, 1u) == (unsigned)G - 1u) {
+            a.bar[0] = 0u;
+            __threadfence();
+            asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(a.bar + 1), "r"(want) : "memory");
+        }
     }
 }
 
@@ -1192,32 +1307,52 @@ extern "C" int f16_gemm_ex(const uint16_t *x16, const uint16_t *w16, uint16_t *y
 namespace w4a16 {
 namespace {
 
-// K splits per 128-row weight tile, S in {1, 2, 4, 8} (at most one per 64-k
-// step), from a cost estimate in units of one L2 round trip (fitted to
-// measured times on GB300): a 64-k step takes about half of one (the step is
-// bound by the latency of the code copies and the conversion, not by its
-// 128 x 128 x 64 MMAs), and the CTA that completes a split tile pays one
-// round trip per batch of max(1, 4 / S) 8-column chunks per epilogue
-// thread (all their loads in flight); waves of units beyond one per SM add
-// up.
-int w4gemm_splits(int M, int N, int K, int sms) {
+// Work split of w4_gemm over G CTAs (one per SM): fw = tiles / G whole tiles
+// per CTA, then the remaining tiles, whose k steps are shared out evenly
+// (spc per CTA, at least 8: two code stages) when that saves more than 14
+// steps per CTA: a shared tile costs its CTAs about 5 µs more at the end
+// (partial stores, the wait for or the count of the other sharers, the sum)
+// against about 0.35 µs per 64-k step.  Otherwise each remaining tile goes
+// whole to one CTA (spc = nk).  Fewer sharers per tile than one per CTA
+// (spc of at least 8) measured faster for the 32-step tiles (fewer partial
+// tiles, fewer CTAs reading activation tiles from L2 at once; GB300, M = 16
+// ... 128).  A tile touched by several CTAs gets their fp32 partial sums
+// added at the end.
+struct W4Split {
+    int grid, fw, spc, split;
+};
+
+W4Split w4gemm_split(int N, int K, int sms) {
+    W4Split w;
     const int tiles = (N + FBN - 1) / FBN, nk = K / BK;
-    int best = 1;
-    double best_cost = 0.0;
-    for (int S = 1; S <= kMaxSplit && S <= nk; S *= 2) {
-        const double waves = (double)((tiles * S + sms - 1) / sms);
-        const int per_batch = 128 * (S >= 4 ? 1 : 4 / S);
-        const double reduce = S > 1 ? (double)((M * (FBN / 8) + per_batch - 1) / per_batch) : 0.0;
-        const double cost = waves * (0.5 * ((nk + S - 1) / S) + reduce);
-        if (S == 1 || cost < best_cost) {
-            best = S;
-            best_cost = cost;
-        }
+    const int G0 = sms < kW4MaxGrid ? sms : kW4MaxGrid;
+    w.fw = tiles / G0;
+    const int rtiles = tiles - w.fw * G0;
+    const int rtot = rtiles * nk;
+    w.spc = rtot > 0 ? (rtot + G0 - 1) / G0 : 1;
+    const int floor_steps = nk < 2 * QCK ? nk : 2 * QCK;
+    if (rtot > 0 && w.spc < floor_steps) w.spc = floor_steps;
+    if (rtot > 0 && nk - w.spc <= 14) w.spc = nk;  // whole tiles only
+    w.grid = w.fw > 0 ? G0 : (rtot + w.spc - 1) / w.spc;
+    w.split = 0;
+    for (int t = 0; t < rtiles && !w.split; ++t) {
+        const int bf = (t * nk) / w.spc, bl = ((t + 1) * nk - 1) / w.spc;
+        if (bf != bl) w.split = 1;
     }
-    return best;
+    return w;
 }
 
-size_t w4gemm_counter_bytes(int N) { return (((size_t)((N + FBN - 1) / FBN) * 4 + 255) / 256) * 256; }
+// Workspace: 256 bytes of counters (CTAs finished, call epoch), one flag per
+// partial-tile slot (2 kW4MaxGrid words), one arrival counter per remaining
+// tile (kW4MaxGrid words), then two fp32 partial tiles (M x 128) per CTA for
+// at most min(kW4MaxGrid, k steps in all) CTAs.
+constexpr size_t kW4FlagsOff = 256, kW4CntOff = kW4FlagsOff + 2 * kW4MaxGrid * 4,
+                 kW4PartOff = kW4CntOff + kW4MaxGrid * 4;
+size_t w4gemm_workspace_need(int M, int N, int K) {
+    const long long steps = (long long)((N + FBN - 1) / FBN) * (K / BK);
+    const long long grid = steps < kW4MaxGrid ? steps : kW4MaxGrid;
+    return kW4PartOff + (size_t)(2 * grid) * (size_t)M * FBN * 4;
+}
 
 bool w4gemm_shape_ok(int M, int N, int K) {
     return M >= 1 && M <= BM && N >= 8 && N % 8 == 0 && K >= BK && K % BK == 0;
@@ -1231,7 +1366,7 @@ int w4gemm_impl(const uint16_t *x, const uint32_t *qweight, const uint16_t *scal
     if (!w4gemm_shape_ok(M, N, K)) return W4_ERR_SHAPE;
     WFmt f;
     if (!make_fmt(f, K, group, biases == nullptr)) return W4_ERR_GROUP;
-    const size_t need = w4gemm_counter_bytes(N) + (size_t)kMaxSplit * M * N * 4;
+    const size_t need = w4gemm_workspace_need(M, N, K);
     if (!workspace || workspace_bytes < need) return W4_ERR_WORKSPACE;
     if (!aligned16(x) || !aligned16(qweight) || !aligned16(scales) || (biases && !aligned16(biases)) ||
         !aligned16(y) || !aligned16(workspace))
@@ -1249,31 +1384,52 @@ int w4gemm_impl(const uint16_t *x, const uint32_t *qweight, const uint16_t *scal
     a.sc = scales;
     a.bi = biases;
     a.y = y;
-    a.cnt = reinterpret_cast<unsigned *>(workspace);
-    a.part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) + w4gemm_counter_bytes(N));
+    a.bar = reinterpret_cast<unsigned *>(workspace);
+    a.flags = reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(workspace) + kW4FlagsOff);
+    a.tcnt = reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(workspace) + kW4CntOff);
+    a.part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) + kW4PartOff);
     a.M = M;
     a.N = N;
     a.K = K;
     a.f = f;
-    a.S = w4gemm_splits(M, N, K, sms);
+    const W4Split w = w4gemm_split(N, K, sms);
+    a.fw = w.fw;
+    a.spc = w.spc;
+    // Small partial tiles (M <= 32) are summed by the last sharer to arrive;
+    // larger ones in slices by all sharers after they wait for each other.
+    a.split = w.split ? (M <= 32 ? 2 : 1) : 0;
     a.pdl = (flags & W4A16_OVERLAP_PREVIOUS) ? 1 : 0;
     // kind::f16, fp32 accumulate, A (weights, tensor memory) and B (X) binary16
     // and K-major, N = M rounded up to 16, M = 128 weight rows.
     const uint32_t nmma = (uint32_t)((M + 15) / 16 * 16);
     a.idesc = (1u << 4) | ((nmma >> 3) << 17) | ((uint32_t)(FBN >> 4) << 24);
-    const int units = ((N + FBN - 1) / FBN) * a.S;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(units < sms ? units : sms), 1, 1);
+    cfg.gridDim = dim3((unsigned)w.grid, 1, 1);
     cfg.blockDim = dim3(F_THREADS, 1, 1);
     cfg.dynamicSmemBytes = F_SMEM;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // CTAs that wait for each other (split 1) must all be resident: a
+    // cooperative launch (one CTA per SM fits: grid <= SMs).
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (a.split == 1) {
+        attr[na].id = cudaLaunchAttributeCooperative;
+        attr[na].val.cooperative = 1;
+        ++na;
+    }
+    if (a.pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = a.pdl;
+    cfg.numAttrs = na;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, w4gemm_kernel, tx, tq, a);
-    return e == cudaSuccess ? W4A16_OK : W4_ERR_LAUNCH;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return W4_ERR_LAUNCH;
+    }
+    return W4A16_OK;
 }
 
 }  // namespace
@@ -1281,7 +1437,7 @@ int w4gemm_impl(const uint16_t *x, const uint32_t *qweight, const uint16_t *scal
 
 extern "C" size_t w4_gemm_workspace_bytes(int M, int N, int K) {
     if (!w4gemm_shape_ok(M, N, K)) return 0;
-    return w4gemm_counter_bytes(N) + (size_t)kMaxSplit * M * N * 4;
+    return w4gemm_workspace_need(M, N, K);
 }
 
 extern "C" int w4_gemm(const uint16_t *x, const uint32_t *qweight, const uint16_t *scales, const uint16_t *biases,

@@ -216,8 +216,12 @@ def test_w4_gemm_host_validation(lib):
     c = _status_codes()
     f = FAKE
     need = lib.w4_gemm_workspace_bytes(64, 256, 512)
-    # tile counters (256-byte block) + 8 splits of fp32 partials
-    assert need == 256 + 8 * 64 * 256 * 4
+    # counters (256 bytes) + 512 slot flags + 256 tile counters + two fp32
+    # partial tiles (M x 128) per CTA for at most min(256, tiles x k steps)
+    # = 2 x 8 = 16 CTAs
+    assert need == 3328 + 2 * 16 * 64 * 128 * 4
+    # the CTA count is capped at 256 whatever the size
+    assert lib.w4_gemm_workspace_bytes(128, 22016, 2048) == 3328 + 2 * 256 * 128 * 128 * 4
     assert lib.w4_gemm_workspace_bytes(129, 256, 512) == 0
     assert lib.w4_gemm_workspace_bytes(4, 12, 512) == 0
     assert lib.w4_gemm_workspace_bytes(4, 256, 96) == 0

@@ -36,11 +36,14 @@ def _dv(a):
 SMALL = [
     (1, 8, 64),         # one k step, one partial tile
     (5, 136, 128),      # ragged tile: 136 = 128 + 8
-    (16, 256, 640),     # K splits of uneven length
+    (16, 256, 640),     # two whole tiles (sharing would save too few steps)
+    (7, 1000, 2048),    # eight tiles, each shared by four blocks, ragged last tile
     (77, 1000, 896),
     (128, 2048, 2048),
-    (128, 384, 11008),  # few tiles, long K: eight splits
-    (33, 11008, 256),   # many tiles: one split
+    (128, 384, 11008),  # few tiles, long K: 22 blocks share each tile
+    (64, 384, 11008),
+    (5, 19584, 640),    # 153 tiles: one whole tile per block and a partial wave of one
+    (33, 11008, 256),   # 86 whole tiles, nothing shared
 ]
 
 
@@ -68,11 +71,12 @@ def test_w4gemm_formats(w4, group, sym):
 @pytest.mark.parametrize("M", [64, 128])
 @pytest.mark.parametrize("group,sym", [(64, False), (128, True)])
 def test_w4gemm_single_split_equals_dequant_then_gemm(w4, M, group, sym):
-    """At M >= 64, N = 22016 (172 tiles for 152 SMs) runs as one K split: the
-    fused GEMM multiplies exactly the w4_dequant_f16 weight values, and only
-    the order in which it adds its 64-k steps differs from f16_gemm on that
-    scratch (a rotation per tile), so every output is within one binary16
-    unit in the last place of f16_gemm's."""
+    """N = 22016 (172 tiles for 152 SMs: 152 whole tiles, the other 20 shared
+    by blocks): the fused GEMM multiplies exactly the w4_dequant_f16 weight
+    values, and only the order in which it adds its 64-k steps differs from
+    f16_gemm on that scratch (a rotation per tile, partial sums of shared
+    tiles), so every output is within one binary16 unit in the last place of
+    f16_gemm's."""
     import torch
     N, K = 22016, 2048
     qw, s, b = _linear(8300 + M, N, K, group, sym)
@@ -103,11 +107,14 @@ def test_w4gemm_full_size_sampled(w4, M, K, N):
     assert ok, f"worst err/tol = {worst}"
 
 
-def test_w4gemm_repeated_calls_share_a_workspace(w4):
-    """Split-K shapes: the tile counters return to zero after every call, so
-    one zero-filled workspace serves many calls with identical results."""
+@pytest.mark.parametrize("M", [16, 64])
+def test_w4gemm_repeated_calls_share_a_workspace(w4, M):
+    """Shared tiles (summed by the last sharer at M = 16, in slices after the
+    sharers' flags at M = 64): counters and flags are left ready after every
+    call, so one zero-filled workspace serves many calls with identical
+    results."""
     import torch
-    M, N, K = 64, 1024, 4096
+    N, K = 1024, 4096
     qw, s, b = _linear(8500, N, K)
     x = synth.make_x(8501, M, K)
     ws = w4.w4_gemm_workspace(M, N, K)
@@ -119,6 +126,29 @@ def test_w4gemm_repeated_calls_share_a_workspace(w4):
     yo, ad = oracle.gemv(x, qw, s, b, N, K, threads=16)
     ok, worst = within_tol(ys[0].cpu().numpy(), yo, ad)
     assert ok, f"worst err/tol = {worst}"
+
+
+def test_w4gemm_both_sharing_forms_alternate_on_one_workspace(w4):
+    """Calls at M = 64 (flags) and M = 16 (arrival counters) alternate on one
+    workspace, back to back on a stream: each form leaves its own counters
+    ready for the next call of either form."""
+    import torch
+    N, K = 2048, 2048
+    qw, s, b = _linear(8550, N, K)
+    xs = {M: synth.make_x(8551 + M, M, K) for M in (16, 64)}
+    ws = w4.w4_gemm_workspace(64, N, K)
+    args = (to_dev(qw), to_dev(s), to_dev(b))
+    outs = {16: [], 64: []}
+    for _ in range(3):
+        for M in (64, 16):
+            outs[M].append(w4.w4_gemm(to_dev(xs[M]), *args, workspace=ws))
+    torch.cuda.synchronize()
+    assert w4.device_status() == 0
+    for M in (16, 64):
+        assert all(torch.equal(outs[M][0], o) for o in outs[M][1:])
+        yo, ad = oracle.gemv(xs[M], qw, s, b, N, K, threads=16)
+        ok, worst = within_tol(outs[M][0].cpu().numpy(), yo, ad)
+        assert ok, f"M={M}: worst err/tol = {worst}"
 
 
 def test_w4gemm_overlap_flag_keeps_the_activation_dependency(w4):
