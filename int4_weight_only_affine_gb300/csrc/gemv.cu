@@ -158,12 +158,12 @@ __device__ __forceinline__ Key2 bitonic_stage64(Key2 v, int size, int stride, in
     return Key2{keep_a ? umax64(v.a, oa) : umin64(v.a, oa), keep_b ? umax64(v.b, ob) : umin64(v.b, ob)};
 }
 
-// The network runs as loops in out-of-line functions: a single compact copy
-// of the code serves every call site.
+// The networks are unrolled (every stage's size and stride are constants) in
+// out-of-line functions: one copy of the code serves every call site.
 __device__ __noinline__ Key2 warp_sort64(Key2 v, int lane) {
-#pragma unroll 1
+#pragma unroll
     for (int size = 2; size <= 64; size <<= 1)
-#pragma unroll 1
+#pragma unroll
         for (int stride = size >> 1; stride > 0; stride >>= 1) v = bitonic_stage64(v, size, stride, lane);
     return v;
 }
@@ -173,7 +173,7 @@ __device__ __noinline__ Key2 warp_merge64(Key2 run, Key2 c, int lane) {
     const uint64_t ra = __shfl_sync(0xffffffffu, c.b, 31 - lane);  // c[63 - i] for i = lane
     const uint64_t rb = __shfl_sync(0xffffffffu, c.a, 31 - lane);  // c[63 - i] for i = 32 + lane
     Key2 v{umax64(run.a, ra), umax64(run.b, rb)};
-#pragma unroll 1
+#pragma unroll
     for (int stride = 32; stride > 0; stride >>= 1) v = bitonic_stage64(v, 64, stride, lane);
     return v;
 }
@@ -834,6 +834,7 @@ __global__ void __launch_bounds__(kPass2Threads)
     __shared__ uint64_t buf[kSurvivorCap];
     __shared__ uint64_t scratch[kPass2Threads / 32];
     __shared__ unsigned nbuf;
+    __shared__ unsigned fk_rank[kPass2Threads];
     pdl_wait();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr int kWarps = kPass2Threads / 32;
@@ -870,10 +871,23 @@ __global__ void __launch_bounds__(kPass2Threads)
         // large.  Keys are distinct, so counting the larger ones gives every
         // key its exact rank.
         buf[tid] = fk;
+        fk_rank[tid] = 0u;
         if (tid == 0) scratch[0] = 0ull;
         __syncthreads();
         if (G <= kPass2Threads) {
-            if (tid < G && rank_of(fk, buf, G) == k - 1) scratch[0] = fk;
+            // P = 1024 / G threads count the larger first keys of list c,
+            // each over a 1 / P share of the lists.
+            const int P = kPass2Threads / G;
+            if (tid < P * G) {
+                const int c = tid % G, p = tid / G;
+                const int j0 = p * G / P, j1 = (p + 1) * G / P;
+                const uint64_t key = buf[c];
+                int r = 0;
+                for (int j = j0; j < j1; ++j) r += buf[j] > key;
+                atomicAdd(&fk_rank[c], (unsigned)r);
+            }
+            __syncthreads();
+            if (tid < G && fk_rank[tid] == (unsigned)(k - 1)) scratch[0] = fk;
         } else if (warp == 0) {
             // Many lists: a looser bound, the k-th largest of the best two
             // first keys each lane sees.
