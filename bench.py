@@ -34,7 +34,7 @@ through the public API every step (projection list + lm_head calls, pinned
 host activations copied in, the top-50 copied out).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-       python bench.py --profile gemv|gemv16|gemm|gemm_all|dequant|lmhead|seq|w4gemm   (cases for ncu)
+       python bench.py --profile gemv|gemv16|gemm|gemm_all|dequant|lmhead|seq|w4gemm|w4gemm_down   (cases for ncu)
 Under torchrun (N > 1) every rank runs an independent replica (the path has no
 exchange step) and rank 0 prints one JSON line.
 """
@@ -679,9 +679,10 @@ def profile_case(which, iters=3):
         ws = w4.seq_workspace(ops)
         for _ in range(iters):
             w4.w4_gemv_seq(ops, workspace=ws)
-    elif which == "w4gemm":
+    elif which in ("w4gemm", "w4gemm_down"):
         # the fused int4 GEMM at M = 128 on the gate|up block (2048 -> 22016)
-        K, N, M = 2048, 22016, 128
+        # or the down block (11008 -> 2048)
+        K, N, M = (2048, 22016, 128) if which == "w4gemm" else (11008, 2048, 128)
         qw, s, b = synth.make_linear(1, N, K)
         a = [torch.from_numpy(t).to(dev) for t in (qw.view(np.int32), s, b)]
         x = torch.from_numpy(synth.make_x(2, M, K)).to(dev)
@@ -707,7 +708,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--profile", default=None,
-                    choices=["gemv", "gemv16", "gemm", "gemm_all", "dequant", "lmhead", "seq", "w4gemm"])
+                    choices=["gemv", "gemv16", "gemm", "gemm_all", "dequant", "lmhead", "seq", "w4gemm",
+                             "w4gemm_down"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
