@@ -341,6 +341,10 @@ def run_ours(args, rank, world):
         return w4.GemvList(ops)
 
     seq3b = seq_barriers(model.layers, FUSED, xs[1], ys[1])
+    # Diagnostic: the same 144 projections with no dependency between them
+    # (no operation waits), separating the list's own rate from its waits.
+    seq3b_free = w4.GemvList([op[:5] + (False,) for op in seq3b.ops])
+    seq3b_free_ws = seq3b_free.workspace()
     seq3b_ws = seq3b.workspace()          # zero-filled once; its counters reset themselves
     seq3b_chain = seq_chain(model.layers, FUSED, xs[1]["attn"], ys[1])
     seq3b_chain_ws = seq3b_chain.workspace()
@@ -365,6 +369,12 @@ def run_ours(args, rank, world):
 
     def decode_seq():
         seq3b.run(seq3b_ws, stream)
+        qw, s, b, N, K = model.lm
+        w4.lm_head_argmax_topk(xs[1]["lm"], qw, s, b, k=TOPK, idx=idx1, val=val1, workspace=ws1, stream=stream,
+                               flags=ov)
+
+    def decode_seq_free():
+        seq3b_free.run(seq3b_free_ws, stream)
         qw, s, b, N, K = model.lm
         w4.lm_head_argmax_topk(xs[1]["lm"], qw, s, b, k=TOPK, idx=idx1, val=val1, workspace=ws1, stream=stream,
                                flags=ov)
@@ -458,6 +468,7 @@ def run_ours(args, rank, world):
         "gemm_m4096": gemm_at(4096),
         "decode_m1": decode_seq,
         "decode_m1_chain": decode_seq_chain,
+        "decode_m1_nowait": decode_seq_free,
         **{f"decode_m{M}": batched(M) for M in BATCH_MS},
         **{f"decode_m{M}_list": batched_list(M) for M in (2, 4)},
         "lm_head_m1": lm_only,
@@ -476,7 +487,7 @@ def run_ours(args, rank, world):
     launches = {"dequant": nb, "gemm": nb, "gemm_m512": nb, "gemm_m4096": nb, "decode_m1": n_seq + 2,
                 **{f"decode_m{M}": nb + 2 for M in BATCH_MS},
                 **{f"decode_m{M}_list": n_seq + 2 for M in (2, 4)}, "lm_head_m1": 2, "gate_up_m1": LAYERS,
-                "decode_m1_s128": n_seq + 2, "decode_m1_chain": n_seq + 2, "decode06_m1": n_seq06 + 2, "single_warm": WARM_REPS,
+                "decode_m1_s128": n_seq + 2, "decode_m1_chain": n_seq + 2, "decode_m1_nowait": n_seq + 2, "decode06_m1": n_seq06 + 2, "single_warm": WARM_REPS,
                 "single_rot": ROT_COPIES, "sel5_rot": 2 * ROT_COPIES, "w4gemm_m128": nb, "gemm_m128": nb}
     # eager warm-up (sets kernel attributes), then capture one graph per part
     with torch.cuda.stream(stream):
@@ -823,6 +834,9 @@ def report(args, r, world, peaks, peak_src, hbm, tflops):
         "decode_m1_chain": hbm_part(DECODE_BYTES, pm["decode_m1_chain"], tok_s=1e3 / pm["decode_m1_chain"],
                                     note="each operation reads (a prefix of) the previous output through the "
                                          "tagged exchange; lm_head reads the last output"),
+        "decode_m1_nowait": hbm_part(DECODE_BYTES, pm["decode_m1_nowait"],
+                                     note="diagnostic, not a decode token: the same 144 projections as one list "
+                                          "with no waits (no dependencies) + lm_head top-50"),
         **{f"decode_m{M}": hbm_part(DECODE_BYTES, pm[f"decode_m{M}"], tok_s=M * 1e3 / pm[f"decode_m{M}"],
                                     gemv_tflop_s=2.0 * M * (PROJ_WEIGHTS + LM_N * LM_K) / (pm[f"decode_m{M}"] / 1e3)
                                     / 1e12) for M in BATCH_MS},
