@@ -680,17 +680,19 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
                 stage_activations<2, FMT == kFmtG32>(o.x, M, o.K, 0, ng, xf, xsum, tid, kSeqConsumers, true);
             }
             seq_sync();
-            for (int tl = team; tl < ntl; tl += 2) {
+            // Tile tl, chunks ch0, ch0 + chs, ...; its 8 warps' partials go to
+            // partial block `slot` (blocks of 8 warps x 16 x M).
+            auto run_tile = [&](int tl, int ch0, int chs, int slot) {
                 const int row0 = (t0 + tl) * kTileRows;
                 const bool tail = row0 + kTileRows > N;
                 Acc<NT> acc;
                 acc.zero();
                 // Stage index of this tile's first chunk: every earlier operation's
                 // stages, then nch per earlier tile of this operation.
-                const int it0 = base_it + tl * nch;
+                const int it0 = base_it + tl * nch + ch0;
                 int s = it0 % S;
                 uint32_t ph = (it0 / S) & 1;
-                for (int ch = 0; ch < nch; ++ch) {
+                for (int ch = ch0; ch < nch; ch += chs) {
                     const bool ok = mbar_wait(full_bar(s), ph, abort_flag);
                     const uint8_t *st = sb + (size_t)s * P.stage_bytes;
                     uint16_t *sp = reinterpret_cast<uint16_t *>(sb + (size_t)s * P.stage_bytes + P.w_bytes);
@@ -722,12 +724,13 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(empty_bar(s));
-                    if (++s == S) {
-                        s = 0;
+                    s += chs;  // chs <= 2 <= S: at most one wrap
+                    if (s >= S) {
+                        s -= S;
                         ph ^= 1;
                     }
                 }
-                float *mine = red + ((size_t)tl * kSeqTeamWarps + tw) * out16;
+                float *mine = red + ((size_t)slot * kSeqTeamWarps + tw) * out16;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -736,7 +739,14 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
                         const int col = nt * 8 + 2 * lt + (i & 1);
                         if (col < M) mine[row * M + col] = acc.template value<FMT == kFmtS128 ? -8 : 1>(nt, i);
                     }
-            }
+            };
+            // A CTA with a single tile of several chunks splits it by K (team
+            // t takes chunks t, t + 2, ...: both teams work, partial blocks 0
+            // and 1); otherwise the teams take alternate tiles.
+            if (ntl == 1 && nch >= 2)
+                run_tile(0, team, 2, team);
+            else
+                for (int tl = team; tl < ntl; tl += 2) run_tile(tl, 0, 1, tl);
             base_it += ntl * nch;
             seq_sync();
             for (int i = tid; i < ntl * out16; i += kSeqConsumers) {
@@ -745,6 +755,9 @@ __global__ void __launch_bounds__(kSeqThreads, 1) seq_kernel(const __grid_consta
                 float v = 0.f;
 #pragma unroll
                 for (int w = 0; w < kSeqTeamWarps; ++w) v += grp[w * out16 + e];
+                if (ntl == 1 && nch >= 2)  // the other team's 8 partials of the single tile
+#pragma unroll
+                    for (int w = kSeqTeamWarps; w < 2 * kSeqTeamWarps; ++w) v += grp[w * out16 + e];
                 const int row = e / M, col = e % M, r = (t0 + tl) * kTileRows + row;
                 if (r < N) {
                     const uint16_t h = __half_as_ushort(__float2half_rn(v));
@@ -1301,6 +1314,9 @@ int lmhead_checks(const uint16_t *x, const uint32_t *qw, const uint16_t *sc, con
 // group 32).
 bool plan_seq(SeqParams &P, size_t &smem, int ng_max, size_t sc_max, int xs_max, int ntl_max) {
     const int M = P.M;
+    // Partials of the 8 warps of each tile a CTA holds, and at least two
+    // tiles' worth: a single tile split by K between the two teams keeps 16.
+    if (ntl_max < 2) ntl_max = 2;
     P.w_bytes = (uint32_t)(kChunkGroups / kBoxGroups) * kBoxBytes;
     P.stage_bytes = (uint32_t)align_up((size_t)P.w_bytes + sc_max, 1024);
     const size_t fixed = align_up((size_t)ng_max * M * 128, 16) + align_up((size_t)xs_max * M * 4, 16) +
