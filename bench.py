@@ -35,7 +35,8 @@ through the public API every step (projection list + lm_head calls, pinned
 host activations copied in, the top-50 copied out).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-       python bench.py --profile gemv|gemv16|gemm|gemm_all|dequant|lmhead|seq|w4gemm|w4gemm_down   (cases for ncu)
+       python bench.py --profile gemv|gemv16|gemm|gemm_all|dequant|lmhead|seq|seq_nowait|w4gemm|w4gemm_down
+           (cases for ncu)
 Under torchrun (N > 1) every rank runs an independent replica (the path has no
 exchange step) and rank 0 prints one JSON line.
 """
@@ -697,6 +698,21 @@ def profile_case(which, iters=3):
         ws = w4.seq_workspace(ops)
         for _ in range(iters):
             w4.w4_gemv_seq(ops, workspace=ws)
+    elif which == "seq_nowait":
+        # eight independent gate|up operations (2048 -> 22016) as one list,
+        # no waits: the list kernel's consumer rate apart from dependencies
+        K, N = 2048, 22016
+        x = torch.from_numpy(synth.make_x(3, 1, K)).to(dev)
+        y = torch.empty((1, N), dtype=torch.float16, device=dev)
+        ops = []
+        for i in range(8):
+            qw, s, b = synth.make_linear(1000 + 7 * i + 2, N, K)
+            ops.append((x, *[torch.from_numpy(np.ascontiguousarray(t)).to(dev) for t in (qw.view(np.int32), s, b)],
+                        y, False))
+        gl = w4.GemvList(ops)
+        ws = gl.workspace()
+        for _ in range(iters + 1):
+            gl.run(ws)
     elif which in ("w4gemm", "w4gemm_down"):
         # the fused int4 GEMM at M = 128 on the gate|up block (2048 -> 22016)
         # or the down block (11008 -> 2048)
@@ -726,8 +742,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--profile", default=None,
-                    choices=["gemv", "gemv16", "gemm", "gemm_all", "dequant", "lmhead", "seq", "w4gemm",
-                             "w4gemm_down"])
+                    choices=["gemv", "gemv16", "gemm", "gemm_all", "dequant", "lmhead", "seq", "seq_nowait",
+                             "w4gemm", "w4gemm_down"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
