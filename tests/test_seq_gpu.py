@@ -60,6 +60,32 @@ def test_seq_chain_matches_oracle(w4, M):
         assert ok, f"op {i}: worst err/tol = {worst}"
 
 
+@pytest.mark.parametrize("M", [1, 3])
+def test_seq_single_tiles_split_by_k(w4, M):
+    """Operations with at most one 16-row tile per CTA and several 2048-k
+    chunks, where a CTA's two warp teams take alternate chunks of its tile:
+    K = 6144 (three chunks: the teams get two and one), chained to the
+    previous output through the tagged exchange, with a ragged last tile
+    (N = 2040), and K = 4096 after it; every output against the oracle."""
+    import torch
+    plan = [(2048, 6144, False), (6144, 2040, True), (4096, 2048, False)]
+    mats = [synth.make_linear(1300 + i, N, K) + (N, K) for i, (K, N, _) in enumerate(plan)]
+    chain = [c for _, _, c in plan]
+    x0 = synth.make_x(78, M, plan[0][0])
+    outs, ads, xs = _oracle_chain(M, x0, mats, chain)
+    ys = [torch.empty((M, N), dtype=torch.float16, device="cuda") for _, N, _ in plan]
+    ops = []
+    for i, ((qw, s, b, N, K), c) in enumerate(zip(mats, chain)):
+        x = ys[i - 1] if c else to_dev(xs[i])
+        ops.append((x, to_dev(qw), to_dev(s), to_dev(b), ys[i], c))
+    w4.w4_gemv_seq(ops)
+    torch.cuda.synchronize()
+    assert w4.device_status() == 0
+    for i in range(len(plan)):
+        ok, worst = within_tol(ys[i].cpu().numpy(), outs[i], ads[i])
+        assert ok, f"op {i}: worst err/tol = {worst}"
+
+
 @pytest.mark.parametrize("mode", ["tagged", "counter"])
 def test_seq_chain_repeated_calls_share_a_workspace(w4, mode):
     """Three calls on one workspace: the tagged exchange (words carry an
